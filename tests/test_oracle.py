@@ -1,0 +1,98 @@
+"""The float64 oracle against what the pages and mathematics fix (CPU only)."""
+import numpy as np
+import pytest
+
+import _pins as pins
+
+pytestmark = pytest.mark.filterwarnings("ignore::UserWarning")
+
+
+def test_e4m3_decoder_all_codes():
+    pins.check_e4m3_all_codes()
+
+
+def test_e4m3_closed_forms():
+    pins.check_e4m3_closed_forms()
+
+
+def test_bf16_decoder():
+    pins.check_bf16_codes()
+
+
+def test_plan_golden_dynamic():
+    pins.check_golden_dynamic()
+
+
+def test_plan_golden_static():
+    pins.check_golden_static()
+
+
+def test_plan_bruteforce_tiny_grid():
+    pins.check_plan_bruteforce_tiny()
+
+
+def test_plan_invariants_random():
+    pins.check_plan_random()
+
+
+def test_static_plan_random():
+    pins.check_static_random()
+
+
+def test_plan_floor_prevents_over_partitioning():
+    import oracle
+    # 3 chunks over 100 CTAs: without the floor every chunk would get its own CTA
+    p = oracle.parse_plan(oracle.plan([192], 1, 100, 2))
+    assert p["header"]["bucket"] == 2 and p["header"]["used_ctas"] == 2
+    assert [len(l) for l in p["lists"][:3]] == [1, 1, 0]
+    # the floor never shrinks a large budget
+    p = oracle.parse_plan(oracle.plan([64 * 1000], 1, 10, 2))
+    assert p["header"]["bucket"] == 100
+
+
+def test_plan_negative_length_sets_error_bit():
+    import oracle
+    p = oracle.parse_plan(oracle.plan([-5, 100], 1, 4, 1))
+    assert p["header"]["error"] & 1
+    assert p["header"]["total_chunks"] == 2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_attn_matches_torch_sdpa(dtype):
+    case = pins.small_case([1, 63, 64, 65, 200, 333], hkv=2, hq=16, dtype=dtype, seed=11)
+    pins.check_attn_vs_sdpa(case)
+
+
+def test_attn_closed_forms():
+    pins.check_attn_closed_forms()
+
+
+def test_page_permutation_invariance():
+    pins.check_page_permutation_invariance()
+
+
+def test_empty_request():
+    pins.check_empty_request()
+
+
+@pytest.mark.parametrize("C,m", [(1, 0), (3, 1), (7, 2), (16, 2), (64, 3)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_combine_of_splits_equals_unsplit(C, m, dtype):
+    case = pins.small_case([37, 128, 300, 1000, 0, 5], hkv=2, hq=16, dtype=dtype, seed=12)
+    pins.check_combine_equals_full(case, C, m)
+
+
+def test_split_partials_are_plain_attention_over_their_range():
+    case = pins.small_case([37, 128, 300, 1000], hkv=1, hq=8, seed=13)
+    pins.check_split_ranges(case, 16, 2)
+
+
+def test_single_chunk_is_plain_attention():
+    # L <= 64: one chunk, one descriptor, the partial is the whole attention
+    import oracle
+    case = pins.small_case([50], seed=14)
+    pb = oracle.plan(case["seq_lens"], 1, 8, 1)
+    so, sl = oracle.attn_splits(pb, case)
+    o, lse = oracle.attn_rows(case)
+    assert so.shape[0] == 1
+    assert np.array_equal(so[0], o) and np.array_equal(sl[0], lse)
