@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark of the load-balanced paged GQA decode-attention step on GB300.
+
+One step = plan (task map from device lengths) + persistent attention +
+combine over one synthetic decode batch resident in HBM. Default workload:
+the mixed-length Hy3-shape batch (64 requests, lengths log-uniform in
+[128, 65536], 64 query / 8 KV heads, head dim 128, BF16 KV, page size 64).
+
+Prints one JSON line. `value` = effective KV GB/s = (live K+V bytes + Q bytes
++ split-partial bytes written and read) / device time per step. The KV stream
+(2.75 GB) is larger than L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload mixed|uniform|skew|fp8|tiny]
+
+--impl reference times the float64 CPU oracle on the host cores (a bounded
+sample of the same workload, scaled to the whole batch).
+Under torchrun (N > 1) each rank runs its own batch (weak scaling, no
+collective on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step and effective KV GB/s (fraction of GB300 HBM peak)"
+UNIT = "GB/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-static", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(w, rank):
+    from dataclasses import replace
+    return w if rank == 0 else replace(w, seed=w.seed + 1000 * rank)
+
+
+def step_bytes(lens, w, n_splits):
+    """Algorithmic bytes of one step: live K+V (+e4m3 scales), Q, and the split
+    partials (8 x (128 + 1) float32 per split, written once and read once)."""
+    from load_balanced_paged_02_gb300 import workloads as wl
+    kv = wl.kv_bytes(lens, w.num_kv_heads, w.kv_dtype)
+    q = len(lens) * w.num_q_heads * 128 * 2
+    part = n_splits * 8 * 129 * 4
+    pages = int(wl.chunk_counts(lens).sum()) * 4
+    return dict(kv=kv, q=q, partials_rw=2 * part, metric=kv + q + 2 * part,
+                attn=kv + q + part + pages, out=len(lens) * w.num_q_heads * 128 * 2)
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("attn.cu", "hpc_internal.cuh"):
+        with open(os.path.join(ROOT, "load_balanced_paged_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, dtype):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(f"{workload}:{dtype}")
+    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(case, w, seconds):
+    """Time the float64 oracle on a bounded sample of requests and scale the
+    rate to the whole batch. Returns (seconds per full step, cores, sample text)."""
+    import oracle
+    from load_balanced_paged_02_gb300 import workloads as wl
+    lens = case["seq_lens"].cpu().numpy().astype(np.int64)
+    total_tok = float(np.maximum(lens, 0).sum())
+    order = np.random.default_rng(99).permutation(len(lens))
+    # grow the sample until it takes about `seconds` of oracle time
+    t_used, tok_done, reqs = 0.0, 0.0, []
+    i = 0
+    per_tok = None
+    while i < len(order) and t_used < seconds:
+        b = int(order[i])
+        i += 1
+        if per_tok is not None and t_used + per_tok * lens[b] > 1.5 * seconds and reqs:
+            continue
+        host = wl.to_numpy_case(case, requests=[b])
+        t0 = time.perf_counter()
+        oracle.attn_rows(host)
+        dt = time.perf_counter() - t0
+        t_used += dt
+        tok_done += lens[b]
+        reqs.append(b)
+        per_tok = t_used / max(tok_done, 1.0)
+    full = per_tok * total_tok
+    text = (f"{len(reqs)} of {len(lens)} requests ({int(tok_done)} of {int(total_tok)} tokens, "
+            f"all {w.num_q_heads} query heads), {t_used:.1f} s of oracle time, scaled by token count")
+    return full, oracle.num_threads(), text
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from load_balanced_paged_02_gb300 import workloads as wl
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    case = wl.make_case(w, device="cpu")
+    lens = case["seq_lens"].numpy()
+    byt = step_bytes(lens, w, 0)
+    times = []
+    sample = None
+    for k in range(args.warmup + args.steps):
+        full, cores, sample = oracle_sample(case, w, max(1.0, args.cpu_seconds / max(args.steps, 1)))
+        if k >= args.warmup:
+            times.append(full)
+    t = float(np.mean(times))
+    value = byt["metric"] / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "detail": w.note},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+
+    from load_balanced_paged_02_gb300 import _build
+    from load_balanced_paged_02_gb300 import binding as hb
+    from load_balanced_paged_02_gb300 import workloads as wl
+    _build.build()
+    hb.lib()
+
+    w = rank_workload(wl.WORKLOADS[args.workload], rank)
+    case = wl.make_case(w, device=dev)
+    kvd = hb.kv_dtype_of(case["k_cache"])
+    C = hb.default_num_ctas(kvd)
+    Hkv = w.num_kv_heads
+    lens = case["seq_lens"].cpu().numpy()
+    stream = torch.cuda.current_stream(dev)
+
+    plan = hb.Plan(w.batch, Hkv, C, dev)
+    hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
+    so, sl = hb.split_buffers(plan)
+    out = torch.empty_like(case["q"])
+    lse = torch.empty(case["q"].shape[:2], dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    n_splits = int(plan.buf[3].item())
+    byt = step_bytes(lens, w, n_splits)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
+        if ev is not None:
+            ev[1].record(stream)
+        hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
+                           case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
+                           num_pages=case["num_pages"])
+        if ev is not None:
+            ev[2].record(stream)
+        hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if hb.hpc_decode_read_error(plan) != 0:
+        raise RuntimeError("device error word set during warm-up")
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_stop)
+    plan_us = 1e3 * float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    attn_us = 1e3 * float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    comb_us = 1e3 * float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    ms_step = max_over_ranks(total_ms / args.steps, dist, dev)
+    if dist is not None:
+        dist.barrier()
+
+    peak, peak_kind = measured_peaks()
+    units_all = world * byt["metric"]
+    value = units_all / (ms_step * 1e-3) / 1e9
+    attn_gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
+
+    result = None
+    if rank == 0:
+        clocks = clk.summary()
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if kvd == hb.KV_BF16 else "e4m3",
+            "data": "synthetic",
+            "config": {"workload": w.name, "detail": w.note, "num_ctas": C, "min_chunks": w.min_chunks,
+                       "live_tokens": int(lens.sum()), "splits": n_splits,
+                       "bytes_per_step": byt, "l2": "inputs larger than L2 (no flush)",
+                       "us_per_step": {"plan": plan_us, "attn": attn_us, "combine": comb_us,
+                                       "total": ms_step * 1e3}},
+            "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": attn_gbs / peak, "peak_kind": peak_kind,
+                         "traffic": recorded_traffic(w.name, "bf16" if kvd == hb.KV_BF16 else "e4m3"),
+                         "kernel": "decode_attn_kernel", "algorithmic_bytes_per_launch": byt["attn"]},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+
+    # ---- static split-KV schedule of the same kernel (comparison)
+    if not args.no_static and rank == 0:
+        splan = hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits)
+        sso, ssl = hb.split_buffers(splan)
+        n_static = max(10, args.steps // 3)
+
+        def sstep():
+            hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits, plan=splan)
+            hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
+                               case["seq_lens"], splan, sso, ssl, case["k_scale"], case["v_scale"],
+                               num_pages=case["num_pages"])
+            hb.hpc_decode_combine(splan, sso, ssl, out, lse, Hkv)
+        for _ in range(3):
+            sstep()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_static):
+            sstep()
+        b.record(stream)
+        torch.cuda.synchronize()
+        sms = a.elapsed_time(b) / n_static
+        sbytes = step_bytes(lens, w, int(splan.buf[3].item()))
+        result["static_split_kv"] = {"num_splits": w.static_splits, "ms_per_step": sms,
+                                     "value": sbytes["metric"] / (sms * 1e-3) / 1e9,
+                                     "speedup_of_balanced": sms / ms_step}
+        del sso, ssl, splan
+
+    # ---- end to end through the C ABI with host buffers
+    if not args.no_e2e:
+        B, Hq, D = case["q"].shape
+        h_q = case["q"].cpu().pin_memory()
+        h_sl = case["seq_lens"].cpu().pin_memory()
+        h_pt = case["page_table"].cpu().pin_memory()
+        h_out = torch.empty_like(h_q).pin_memory()
+        h_lse = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+        ws = torch.empty(hb.step_workspace_bytes(B, Hq, Hkv, h_pt.shape[1], C), dtype=torch.uint8,
+                         device=dev)
+
+        def estep():
+            hb.hpc_decode_step_host(h_q, h_sl, h_pt, case["k_cache"], case["v_cache"], ws, h_out, h_lse,
+                                    k_scale=case["k_scale"], v_scale=case["v_scale"], num_ctas=C,
+                                    min_chunks_per_cta=w.min_chunks, num_pages=case["num_pages"])
+            stream.synchronize()
+        for _ in range(3):
+            estep()
+        n_e2e = max(10, args.steps // 3)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            estep()
+        e_ms = (time.perf_counter() - t0) * 1e3 / n_e2e
+        e_ms = max_over_ranks(e_ms, dist, dev)
+        if rank == 0:
+            h2d = h_q.numel() * 2 + h_sl.numel() * 4 + h_pt.numel() * 4
+            d2h = h_out.numel() * 2 + h_lse.numel() * 4
+            result["e2e"] = {"value": world * byt["metric"] / (e_ms * 1e-3) / 1e9, "unit": UNIT,
+                             "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                             "api": "hpc_decode_step_host (pinned host q/seq_lens/page_table in, "
+                                    "out/lse back; KV cache resident in HBM)"}
+
+    # ---- CPU oracle baseline (rank 0 only, N = 1 only)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        full_s, cores, text = oracle_sample(case, w, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": byt["metric"] / full_s / 1e9, "unit": UNIT, "cores": cores,
+                                  "kind": "oracle", "sample": text, "ms_per_step": full_s * 1e3}
+
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

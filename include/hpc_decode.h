@@ -1,0 +1,241 @@
+/*
+ * hpc_decode.h - C ABI of the load-balanced paged GQA decode attention
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * The method (two blog posts on the HPC-Ops attention backend):
+ *   [SGL]  "HPC-Ops, integrated into SGLang", sections "Attention: load
+ *          balancing for mixed-length decode" and "Scheduling around live KV
+ *          work".
+ *   [VLLM] "vLLM x HPC-Ops: High-Performance Attention and MoE Backends from
+ *          Tencent Hunyuan", sub-section "解决方案：按步负载均衡的 decode
+ *          调度器" (assign -> compute and combine), and "关于 Hy3 系列模型的
+ *          简要说明" (GQA shape: 64 query heads, 8 KV heads, head dim 128).
+ *
+ * One decode step is three calls on one stream:
+ *   hpc_decode_plan     once per step: live lengths -> task map (reused by
+ *                       every layer of the step)
+ *   hpc_decode_attn     per layer: persistent grid drains the task map and
+ *                       writes one partial output + LSE per descriptor
+ *   hpc_decode_combine  per layer: LSE-weighted merge into the BF16 output
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented as "device" are device pointers; h_*
+ *     are host pointers. The caller owns all memory. The library never
+ *     allocates, frees or synchronises inside these calls (except
+ *     hpc_decode_read_error, which synchronises by design).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued asynchronously on it.
+ *   - Supported shapes: head_dim == 128, page_size == 64 (one chunk is one
+ *     page), num_q_heads == 8 * num_kv_heads. Anything else returns
+ *     HPC_ERR_UNSUPPORTED before any work is enqueued.
+ *   - Host-side argument checks return HPC_ERR_INVALID_ARG and enqueue
+ *     nothing. Launch failures return HPC_ERR_CUDA. No call traps or aborts.
+ *   - Device-side checks (negative length, page id out of range, a
+ *     descriptor outside the shapes, a bounded wait that ran out) set bits in
+ *     the error word stored in the task map (HPC_DEVERR_*) and skip the
+ *     offending work; read it with hpc_decode_read_error.
+ *
+ * Data layouts (row-major, contiguous):
+ *   q          bf16 [batch][num_q_heads][128]; query head qh belongs to KV
+ *              head qh / 8 (contiguous GQA groups).
+ *   k_cache,   [num_pages][64][num_kv_heads][128], bf16 or e4m3 (OCP
+ *   v_cache    e4m3fn). Token t of request b lives in page
+ *              page_table[b * page_table_stride + t / 64], slot t % 64.
+ *   k_scale,   e4m3 caches only: float32 [num_pages][num_kv_heads][64], one
+ *   v_scale    scale per (token, KV head); the value is code * scale.
+ *   page_table int32 [batch][page_table_stride]; only entries
+ *              [0, ceil(seq_lens[b] / 64)) of row b are read.
+ *   seq_lens   int32 [batch], live KV length of each request (>= 0).
+ *   split_o    float32 [split_capacity][8][128]: normalised partial output of
+ *              each descriptor for the 8 query heads of its KV head.
+ *   split_lse  float32 [split_capacity][8]: natural-log LSE of each partial
+ *              (scores scaled by 1/sqrt(128)).
+ *   out        bf16 [batch][num_q_heads][128] (round to nearest even).
+ *   out_lse    float32 [batch][num_q_heads] (nullable). A request of length 0
+ *              gets out = 0 and out_lse = -inf.
+ */
+#ifndef HPC_DECODE_H
+#define HPC_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hpc_status {
+    HPC_OK = 0,
+    HPC_ERR_INVALID_ARG = 1,
+    HPC_ERR_UNSUPPORTED = 2,
+    HPC_ERR_WORKSPACE_TOO_SMALL = 3,
+    HPC_ERR_CUDA = 4,
+    HPC_ERR_DEVICE_CHECK = 5
+} hpc_status;
+
+typedef enum hpc_kv_dtype { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
+
+/* Bits of the device error word (hpc_decode_read_error). */
+#define HPC_DEVERR_NEGATIVE_LENGTH 1u    /* planner saw seq_lens[b] < 0 (counted as 0) */
+#define HPC_DEVERR_CHUNK_OVERFLOW 2u     /* chunk total over all heads exceeds INT32_MAX */
+#define HPC_DEVERR_PAGE_OUT_OF_RANGE 4u  /* a page id outside [0, num_pages): chunk skipped */
+#define HPC_DEVERR_WAIT_TIMEOUT 8u       /* a bounded wait inside the kernel ran out */
+#define HPC_DEVERR_BAD_DESCRIPTOR 16u    /* a task descriptor outside the call's shapes */
+
+/* Limits checked on the host. */
+#define HPC_MAX_BATCH 16384
+#define HPC_MAX_KV_HEADS 256
+#define HPC_MAX_CTAS (1 << 22)
+
+/*
+ * Task map ([SGL] "Scheduling around live KV work": a global task map built
+ * once per decode step from device-side lengths and reused across layers).
+ * The caller fills `buf` (device memory of at least hpc_decode_plan_bytes)
+ * and `bytes`; hpc_decode_plan / hpc_decode_plan_static fill the rest.
+ *
+ * Byte layout of buf (int32):
+ *   [0, 16)            header {total_chunks, bucket, used_ctas, total_splits,
+ *                      num_ctas, batch, num_kv_heads, min_chunks (or the
+ *                      static split count), max_tasks, mode, chunks_per_head,
+ *                      chunk_tokens (64), error word, 0, 0, 0}
+ *   [16, 16 + C + 1)   first task row of each CTA's list; entry C = end
+ *   tasks              32-byte aligned, max_tasks rows of 8 int32
+ *                      {kv_head, request, chunk_begin, chunk_end, split,
+ *                       rank_in_pair, splits_in_pair, 0}; each CTA's list is
+ *                      closed by a row of -1 (terminator); unused rows are -1
+ *   pair_nsplit        [num_kv_heads * batch], pair p = kv_head * batch + b
+ *   pair_split0        [num_kv_heads * batch], first split of pair p
+ *   max_tasks = num_kv_heads * batch + 2 * num_ctas.
+ * The buffer is deterministic: the same lengths give the same bytes.
+ */
+typedef struct hpc_plan {
+    int32_t* buf;      /* device, caller-owned */
+    size_t bytes;      /* size of buf in bytes */
+    int batch;         /* filled by the planner from here on */
+    int num_kv_heads;
+    int num_ctas;      /* grid size hpc_decode_attn launches */
+    int min_chunks;    /* floor m (dynamic) or split count S (static) */
+    int mode;          /* 0 load-balanced, 1 static split count */
+    int max_tasks;
+} hpc_plan;
+
+/* Bytes of the task map for (batch, num_kv_heads, num_ctas); independent of
+ * the lengths, so one buffer serves every step. 0 on invalid sizes. */
+size_t hpc_decode_plan_bytes(int batch, int num_kv_heads, int num_ctas);
+
+/* Rows needed in split_o / split_lse: num_kv_heads * batch + num_ctas - 1
+ * (at least 1). A descriptor is a maximal run of one (kv head, request) inside
+ * one bucket, so each used CTA adds at most one split beyond one per pair.
+ * For a static plan pass num_ctas = num_kv_heads * batch * num_splits. */
+size_t hpc_decode_split_capacity(int batch, int num_kv_heads, int num_ctas);
+
+/* Persistent CTA count for the attention kernel on the current device:
+ * SM count x resident CTAs per SM of the kernel instance for `kv_dtype`.
+ * Returns 0 if the device cannot be queried. */
+int hpc_decode_default_num_ctas(int kv_dtype);
+
+/*
+ * Load-balanced planner ([SGL] "Scheduling around live KV work"; [VLLM]
+ * "解决方案：按步负载均衡的 decode 调度器", assign stage). For each request
+ * n_b = ceil(seq_lens[b] / 64); T = num_kv_heads * sum(n_b);
+ * bucket = max(ceil(T / num_ctas), min_chunks_per_cta, 1). Chunks are walked
+ * kv head by kv head, request by request, chunk by chunk; global chunk g goes
+ * to CTA g / bucket, and each maximal run of one (kv head, request) inside one
+ * CTA is one descriptor. One block, integer only, reads d_seq_lens on the
+ * device (no host synchronisation).
+ *   d_seq_lens  device int32 [batch]
+ *   plan        caller fills buf/bytes; other fields are written here
+ * Errors: HPC_ERR_INVALID_ARG (null pointers, sizes outside the limits,
+ * min_chunks_per_cta < 0), HPC_ERR_WORKSPACE_TOO_SMALL, HPC_ERR_CUDA.
+ */
+hpc_status hpc_decode_plan(const int32_t* d_seq_lens, int batch, int num_kv_heads, int num_ctas,
+                           int min_chunks_per_cta, hpc_plan* plan, void* stream);
+
+/*
+ * Static split-KV comparison schedule ([SGL] "Attention: load balancing for
+ * mixed-length decode", policy (1): a fixed split count). One virtual CTA per
+ * (kv head, request, split s), num_ctas = num_kv_heads * batch * num_splits;
+ * split s of a pair with n chunks covers [s*q, min((s+1)*q, n)) with
+ * q = ceil(n / num_splits) and is empty when s*q >= n. Same layout and same
+ * attention kernel as the load-balanced map.
+ */
+hpc_status hpc_decode_plan_static(const int32_t* d_seq_lens, int batch, int num_kv_heads,
+                                  int num_splits, hpc_plan* plan, void* stream);
+
+/*
+ * Persistent decode attention ([SGL] "Scheduling around live KV work", the
+ * paragraph on execution; [VLLM] compute stage). Launches plan->num_ctas CTAs;
+ * CTA j walks its descriptor list until the terminator. For descriptor
+ * (h, b, c0, c1, s) and each j < 8 it writes
+ *   split_o[s][j][:]  = sum_t softmax_t(q[b][8h+j] . k_t / sqrt(128)) v_t
+ *   split_lse[s][j]   = ln sum_t exp(q[b][8h+j] . k_t / sqrt(128))
+ * over tokens t in [64*c0, min(64*c1, seq_lens[b])) of KV head h.
+ *   q, k_cache, v_cache   device, 16-byte aligned (TMA sources)
+ *   k_scale, v_scale      device float32, 16-byte aligned, e4m3 only (NULL
+ *                         for bf16)
+ *   num_pages             physical pages in each cache (page ids outside
+ *                         [0, num_pages) set HPC_DEVERR_PAGE_OUT_OF_RANGE)
+ *   seq_lens              device int32 [batch], the lengths the plan saw
+ *   split_o, split_lse    device float32, hpc_decode_split_capacity rows
+ * Errors: HPC_ERR_INVALID_ARG, HPC_ERR_UNSUPPORTED, HPC_ERR_CUDA.
+ */
+hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                           const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
+                           const int32_t* page_table, int page_table_stride,
+                           const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                           int head_dim, int page_size, const hpc_plan* plan, float* split_o,
+                           float* split_lse, void* stream);
+
+/*
+ * Combine ([SGL] the paragraph on execution; [VLLM] combine stage). For every
+ * (request b, query head qh) with h = qh / 8, j = qh % 8 and the pair's
+ * n = pair_nsplit[h*batch+b] partials starting at s0 = pair_split0[...]:
+ * M = max_i lse_i, w_i = exp(lse_i - M), out = sum w_i o_i / sum w_i (to
+ * bf16, round to nearest even), out_lse = M + ln sum w_i. n == 0 gives 0 and
+ * -inf. One warp per output row.
+ *   out       device bf16 [batch][num_q_heads][128], 8-byte aligned
+ *   out_lse   device float32 [batch][num_q_heads] or NULL
+ */
+hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse,
+                              void* out, float* out_lse, int batch, int num_q_heads,
+                              int num_kv_heads, int head_dim, void* stream);
+
+/*
+ * Workspace bytes for hpc_decode_step_host: device copies of q, seq_lens and
+ * the page table, the task map, the split buffers and the outputs, each
+ * 256-byte aligned. 0 on invalid sizes.
+ */
+size_t hpc_decode_step_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                       int page_table_stride, int num_ctas);
+
+/*
+ * One decode step from host buffers: copies h_q, h_seq_lens and h_page_table
+ * into d_workspace (cudaMemcpyAsync, host -> device), plans with num_ctas and
+ * min_chunks_per_cta, runs attention over the device-resident caches,
+ * combines, and copies out (and out_lse, if h_out_lse is non-NULL) back to the
+ * host. Everything is enqueued on `stream`; the caller synchronises the
+ * stream before reading h_out. Host buffers should be pinned for the copies
+ * to be asynchronous. Same errors as the calls it chains.
+ */
+hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens,
+                                const int32_t* h_page_table, int page_table_stride,
+                                const void* d_k_cache, const void* d_v_cache,
+                                const float* d_k_scale, const float* d_v_scale, int kv_dtype,
+                                int num_pages, int batch, int num_q_heads, int num_kv_heads,
+                                int head_dim, int page_size, int num_ctas, int min_chunks_per_cta,
+                                void* d_workspace, size_t workspace_bytes, void* h_out,
+                                float* h_out_lse, void* stream);
+
+/* Synchronises the device, then reads the task map's error word into
+ * *device_error_word. Returns HPC_ERR_DEVICE_CHECK when it is non-zero.
+ * For tests and diagnostics, not for the hot loop. */
+hpc_status hpc_decode_read_error(const hpc_plan* plan, int* device_error_word);
+
+/* Static string for a status code. */
+const char* hpc_status_string(hpc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HPC_DECODE_H */

@@ -1,0 +1,275 @@
+"""Thin ctypes binding of libhpcdecode (include/hpc_decode.h).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of the library. Torch tensors supply device pointers and the current
+CUDA stream; nothing here computes attention, and every call raises HpcError
+when the library is missing or returns a non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+HEAD_DIM = 128
+PAGE = 64
+GROUP = 8
+
+_STATUS = {0: "HPC_OK", 1: "HPC_ERR_INVALID_ARG", 2: "HPC_ERR_UNSUPPORTED",
+           3: "HPC_ERR_WORKSPACE_TOO_SMALL", 4: "HPC_ERR_CUDA", 5: "HPC_ERR_DEVICE_CHECK"}
+
+# Every function include/hpc_decode.h declares: name -> (restype, argtypes).
+_i = ctypes.c_int
+_sz = ctypes.c_size_t
+_vp = ctypes.c_void_p
+
+
+class HpcError(RuntimeError):
+    def __init__(self, where, status=None, detail=""):
+        self.status = status
+        name = _STATUS.get(status, str(status)) if status is not None else ""
+        super().__init__(f"{where}: {name} {detail}".strip())
+
+
+class PlanStruct(ctypes.Structure):
+    _fields_ = [("buf", _vp), ("bytes", _sz), ("batch", _i), ("num_kv_heads", _i),
+                ("num_ctas", _i), ("min_chunks", _i), ("mode", _i), ("max_tasks", _i)]
+
+
+_P = ctypes.POINTER(PlanStruct)
+SIGNATURES = {
+    "hpc_decode_plan_bytes": (_sz, [_i, _i, _i]),
+    "hpc_decode_split_capacity": (_sz, [_i, _i, _i]),
+    "hpc_decode_default_num_ctas": (_i, [_i]),
+    "hpc_decode_plan": (_i, [_vp, _i, _i, _i, _i, _P, _vp]),
+    "hpc_decode_plan_static": (_i, [_vp, _i, _i, _i, _P, _vp]),
+    "hpc_decode_attn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _P,
+                             _vp, _vp, _vp]),
+    "hpc_decode_combine": (_i, [_P, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "hpc_decode_step_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "hpc_decode_step_host": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                  _i, _i, _vp, _sz, _vp, _vp, _vp]),
+    "hpc_decode_read_error": (_i, [_P, ctypes.POINTER(_i)]),
+    "hpc_status_string": (ctypes.c_char_p, [_i]),
+}
+
+_lock = threading.Lock()
+_LIB = None
+
+
+def build(force: bool = False) -> str:
+    """Compile libhpcdecode.so for sm_103a in-tree (nvcc)."""
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded library; raises HpcError if it has not been built."""
+    global _LIB
+    with _lock:
+        if _LIB is None:
+            if not os.path.exists(_build.LIB_PATH):
+                raise HpcError("libhpcdecode.so", detail="is not built; call "
+                               "load_balanced_paged_02_gb300.build() (needs nvcc)")
+            L = ctypes.CDLL(_build.LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _LIB = L
+        return _LIB
+
+
+def _check(name, rc):
+    if rc != 0:
+        msg = lib().hpc_status_string(rc).decode()
+        raise HpcError(name, rc, f"({msg})")
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda_i32(t, what):
+    if not (t.is_cuda and t.dtype == torch.int32 and t.is_contiguous()):
+        raise HpcError(what, detail="must be a contiguous int32 CUDA tensor")
+    return t
+
+
+def kv_dtype_of(cache: torch.Tensor) -> int:
+    if cache.dtype == torch.bfloat16:
+        return KV_BF16
+    if cache.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return KV_FP8_E4M3
+    raise HpcError("k_cache", detail=f"unsupported dtype {cache.dtype}")
+
+
+def sm_count(device=None) -> int:
+    return torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
+
+
+def default_num_ctas(kv_dtype: int = KV_BF16) -> int:
+    n = lib().hpc_decode_default_num_ctas(kv_dtype)
+    if n <= 0:
+        raise HpcError("hpc_decode_default_num_ctas", detail="device query failed")
+    return n
+
+
+class Plan:
+    """A task map in caller-owned device memory (``buf``) plus its host header."""
+
+    def __init__(self, batch: int, num_kv_heads: int, num_ctas: int, device):
+        nbytes = lib().hpc_decode_plan_bytes(batch, num_kv_heads, num_ctas)
+        if nbytes == 0:
+            raise HpcError("hpc_decode_plan_bytes", detail="sizes outside the supported limits")
+        self.buf = torch.empty(nbytes // 4, dtype=torch.int32, device=device)
+        self.struct = PlanStruct(self.buf.data_ptr(), nbytes, 0, 0, 0, 0, 0, 0)
+        self.capacity_ctas = num_ctas
+        self.split_capacity = int(lib().hpc_decode_split_capacity(batch, num_kv_heads, num_ctas))
+
+    @property
+    def num_ctas(self):
+        return self.struct.num_ctas
+
+    @property
+    def mode(self):
+        return self.struct.mode
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+def hpc_decode_plan(seq_lens: torch.Tensor, num_kv_heads: int, num_ctas: int | None = None,
+                    min_chunks_per_cta: int = 2, plan: Plan | None = None, stream=None) -> Plan:
+    """Load-balanced task map from device-side lengths (one launch, no host sync)."""
+    _cuda_i32(seq_lens, "seq_lens")
+    B = seq_lens.numel()
+    if num_ctas is None:
+        num_ctas = default_num_ctas(KV_BF16)
+    if plan is None:
+        plan = Plan(B, num_kv_heads, num_ctas, seq_lens.device)
+    rc = lib().hpc_decode_plan(_ptr(seq_lens), B, num_kv_heads, num_ctas, min_chunks_per_cta,
+                               plan.ref(), _stream(stream))
+    _check("hpc_decode_plan", rc)
+    plan.split_capacity = int(lib().hpc_decode_split_capacity(B, num_kv_heads, num_ctas))
+    return plan
+
+
+def hpc_decode_plan_static(seq_lens: torch.Tensor, num_kv_heads: int, num_splits: int = 16,
+                           plan: Plan | None = None, stream=None) -> Plan:
+    """Static split-KV task map with a fixed split count (the comparison schedule)."""
+    _cuda_i32(seq_lens, "seq_lens")
+    B = seq_lens.numel()
+    C = num_kv_heads * B * num_splits
+    if plan is None:
+        plan = Plan(B, num_kv_heads, C, seq_lens.device)
+    rc = lib().hpc_decode_plan_static(_ptr(seq_lens), B, num_kv_heads, num_splits, plan.ref(),
+                                      _stream(stream))
+    _check("hpc_decode_plan_static", rc)
+    plan.split_capacity = int(lib().hpc_decode_split_capacity(B, num_kv_heads, C))
+    return plan
+
+
+def split_buffers(plan: Plan, device=None):
+    """Allocate split_o [capacity, 8, 128] and split_lse [capacity, 8] (float32)."""
+    device = device or plan.buf.device
+    cap = plan.split_capacity
+    return (torch.empty((cap, GROUP, HEAD_DIM), dtype=torch.float32, device=device),
+            torch.empty((cap, GROUP), dtype=torch.float32, device=device))
+
+
+def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split_o, split_lse,
+                    k_scale=None, v_scale=None, num_pages: int | None = None, stream=None):
+    """Persistent attention over the task map; writes split_o / split_lse."""
+    kvd = kv_dtype_of(k_cache)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (split_o, "split_o"),
+                 (split_lse, "split_lse")):
+        if not (t.is_cuda and t.is_contiguous()):
+            raise HpcError(n, detail="must be a contiguous CUDA tensor")
+    _cuda_i32(page_table, "page_table")
+    _cuda_i32(seq_lens, "seq_lens")
+    if split_o.shape[0] < plan.split_capacity or split_lse.shape[0] < plan.split_capacity:
+        raise HpcError("split buffers", detail=f"need {plan.split_capacity} rows")
+    rc = lib().hpc_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd,
+        int(num_pages if num_pages is not None else k_cache.shape[0]), _ptr(page_table),
+        int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D, int(k_cache.shape[1]), plan.ref(),
+        _ptr(split_o), _ptr(split_lse), _stream(stream))
+    _check("hpc_decode_attn", rc)
+
+
+def hpc_decode_combine(plan: Plan, split_o, split_lse, out, out_lse=None, num_kv_heads=None,
+                       stream=None):
+    """LSE-weighted merge of the partials into out (bf16) and out_lse (float32)."""
+    B, Hq, D = out.shape
+    Hkv = num_kv_heads if num_kv_heads is not None else Hq // GROUP
+    rc = lib().hpc_decode_combine(plan.ref(), _ptr(split_o), _ptr(split_lse), _ptr(out),
+                                  _ptr(out_lse), B, Hq, Hkv, D, _stream(stream))
+    _check("hpc_decode_combine", rc)
+
+
+def decode(q, k_cache, v_cache, page_table, seq_lens, k_scale=None, v_scale=None,
+           num_ctas: int | None = None, min_chunks_per_cta: int = 2, static_splits: int | None = None,
+           stream=None):
+    """plan -> attn -> combine with freshly allocated buffers. Returns (out, lse, plan)."""
+    Hkv = k_cache.shape[2]
+    if static_splits:
+        plan = hpc_decode_plan_static(seq_lens, Hkv, static_splits, stream=stream)
+    else:
+        if num_ctas is None:
+            num_ctas = default_num_ctas(kv_dtype_of(k_cache))
+        plan = hpc_decode_plan(seq_lens, Hkv, num_ctas, min_chunks_per_cta, stream=stream)
+    so, sl = split_buffers(plan)
+    hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan, so, sl, k_scale, v_scale,
+                    stream=stream)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    hpc_decode_combine(plan, so, sl, out, lse, Hkv, stream=stream)
+    return out, lse, plan
+
+
+def hpc_decode_read_error(plan: Plan) -> int:
+    """Synchronise and read the task map's device error word (HPC_DEVERR_* bits)."""
+    w = ctypes.c_int(0)
+    rc = lib().hpc_decode_read_error(plan.ref(), ctypes.byref(w))
+    if rc not in (0, 5):
+        _check("hpc_decode_read_error", rc)
+    return int(w.value)
+
+
+def step_workspace_bytes(batch, num_q_heads, num_kv_heads, page_table_stride, num_ctas) -> int:
+    return int(lib().hpc_decode_step_workspace_bytes(batch, num_q_heads, num_kv_heads,
+                                                      page_table_stride, num_ctas))
+
+
+def hpc_decode_step_host(h_q, h_seq_lens, h_page_table, k_cache, v_cache, workspace, h_out,
+                         h_out_lse=None, k_scale=None, v_scale=None, num_ctas=None,
+                         min_chunks_per_cta: int = 2, num_pages=None, stream=None):
+    """One step from host tensors (pinned CPU): H2D copies, plan, attn, combine, D2H.
+    Asynchronous on ``stream``; synchronise before reading h_out."""
+    B, Hq, D = h_q.shape
+    Hkv = k_cache.shape[2]
+    if num_ctas is None:
+        num_ctas = default_num_ctas(kv_dtype_of(k_cache))
+    rc = lib().hpc_decode_step_host(
+        _ptr(h_q), _ptr(h_seq_lens), _ptr(h_page_table), int(h_page_table.shape[1]),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype_of(k_cache),
+        int(num_pages if num_pages is not None else k_cache.shape[0]), B, Hq, Hkv, D,
+        int(k_cache.shape[1]), num_ctas, min_chunks_per_cta, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(h_out), _ptr(h_out_lse), _stream(stream))
+    _check("hpc_decode_step_host", rc)

@@ -1,0 +1,248 @@
+// extern "C" entry points of libhpcdecode (declared in include/hpc_decode.h):
+// host-side argument checks, then the launches in plan.cu, attn.cu and
+// combine.cu. Nothing here allocates device memory or synchronises, except
+// hpc_decode_read_error.
+#include "hpc_internal.cuh"
+
+using namespace hpc;
+
+namespace {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool sizes_ok(int batch, int num_kv_heads, long long num_ctas) {
+    return batch >= 1 && batch <= HPC_MAX_BATCH && num_kv_heads >= 1 &&
+           num_kv_heads <= HPC_MAX_KV_HEADS && num_ctas >= 1 && num_ctas <= HPC_MAX_CTAS;
+}
+
+size_t plan_bytes_ll(int batch, int num_kv_heads, long long num_ctas) {
+    if (!sizes_ok(batch, num_kv_heads, num_ctas)) return 0;
+    return (size_t)plan_layout(batch, num_kv_heads, num_ctas).total_ints * sizeof(int32_t);
+}
+
+hpc_status shape_check(int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
+    if (num_q_heads < 1 || num_kv_heads < 1) return HPC_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim || page_size != kChunk || num_q_heads != kGroup * num_kv_heads)
+        return HPC_ERR_UNSUPPORTED;
+    return HPC_OK;
+}
+
+hpc_status plan_check(const hpc_plan* plan, int batch, int num_kv_heads) {
+    if (!plan || !plan->buf) return HPC_ERR_INVALID_ARG;
+    if (plan->batch != batch || plan->num_kv_heads != num_kv_heads) return HPC_ERR_INVALID_ARG;
+    if (plan->num_ctas < 1 || plan->bytes < plan_bytes_ll(batch, num_kv_heads, plan->num_ctas))
+        return HPC_ERR_INVALID_ARG;
+    return HPC_OK;
+}
+
+struct StepWorkspace {
+    size_t q, seq_lens, page_table, plan, split_o, split_lse, out, out_lse, total;
+};
+
+StepWorkspace step_workspace(int batch, int num_q_heads, int num_kv_heads, int pt_stride, int num_ctas) {
+    StepWorkspace w{};
+    const size_t cap = hpc_decode_split_capacity(batch, num_kv_heads, num_ctas);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    w.q = take((size_t)batch * num_q_heads * kHeadDim * 2);
+    w.seq_lens = take((size_t)batch * 4);
+    w.page_table = take((size_t)batch * pt_stride * 4);
+    w.plan = take(hpc_decode_plan_bytes(batch, num_kv_heads, num_ctas));
+    w.split_o = take(cap * kGroup * kHeadDim * 4);
+    w.split_lse = take(cap * kGroup * 4);
+    w.out = take((size_t)batch * num_q_heads * kHeadDim * 2);
+    w.out_lse = take((size_t)batch * num_q_heads * 4);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t hpc_decode_plan_bytes(int batch, int num_kv_heads, int num_ctas) {
+    return plan_bytes_ll(batch, num_kv_heads, num_ctas);
+}
+
+size_t hpc_decode_split_capacity(int batch, int num_kv_heads, int num_ctas) {
+    if (!sizes_ok(batch, num_kv_heads, num_ctas)) return 0;
+    long long cap = (long long)num_kv_heads * batch + num_ctas - 1;
+    return (size_t)(cap < 1 ? 1 : cap);
+}
+
+int hpc_decode_default_num_ctas(int kv_dtype) {
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return 0;
+    return attn_default_ctas(kv_dtype == HPC_KV_FP8_E4M3);
+}
+
+hpc_status hpc_decode_plan(const int32_t* d_seq_lens, int batch, int num_kv_heads, int num_ctas,
+                           int min_chunks_per_cta, hpc_plan* plan, void* stream) {
+    if (!d_seq_lens || !plan || !plan->buf || min_chunks_per_cta < 0) return HPC_ERR_INVALID_ARG;
+    if (!sizes_ok(batch, num_kv_heads, num_ctas)) return HPC_ERR_INVALID_ARG;
+    if ((long long)num_kv_heads * batch > HPC_MAX_CTAS || !aligned(plan->buf, 16)) return HPC_ERR_INVALID_ARG;
+    if (plan->bytes < plan_bytes_ll(batch, num_kv_heads, num_ctas)) return HPC_ERR_WORKSPACE_TOO_SMALL;
+    plan->batch = batch;
+    plan->num_kv_heads = num_kv_heads;
+    plan->num_ctas = num_ctas;
+    plan->min_chunks = min_chunks_per_cta;
+    plan->mode = 0;
+    plan->max_tasks = (int)plan_layout(batch, num_kv_heads, num_ctas).max_tasks;
+    cudaError_t e = launch_plan(d_seq_lens, batch, num_kv_heads, num_ctas, min_chunks_per_cta, plan->buf,
+                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+hpc_status hpc_decode_plan_static(const int32_t* d_seq_lens, int batch, int num_kv_heads, int num_splits,
+                                  hpc_plan* plan, void* stream) {
+    if (!d_seq_lens || !plan || !plan->buf || num_splits < 1) return HPC_ERR_INVALID_ARG;
+    const long long C = (long long)num_kv_heads * batch * num_splits;
+    if (!sizes_ok(batch, num_kv_heads, C) || !aligned(plan->buf, 16)) return HPC_ERR_INVALID_ARG;
+    if (plan->bytes < plan_bytes_ll(batch, num_kv_heads, C)) return HPC_ERR_WORKSPACE_TOO_SMALL;
+    plan->batch = batch;
+    plan->num_kv_heads = num_kv_heads;
+    plan->num_ctas = (int)C;
+    plan->min_chunks = num_splits;
+    plan->mode = 1;
+    plan->max_tasks = (int)plan_layout(batch, num_kv_heads, C).max_tasks;
+    cudaError_t e = launch_plan_static(d_seq_lens, batch, num_kv_heads, num_splits, plan->buf,
+                                       static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, int kv_dtype, int num_pages, const int32_t* page_table,
+                           int page_table_stride, const int32_t* seq_lens, int batch, int num_q_heads,
+                           int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
+                           float* split_o, float* split_lse, void* stream) {
+    hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
+    if (st != HPC_OK) return st;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !split_o || !split_lse)
+        return HPC_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return HPC_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(split_o, 16))
+        return HPC_ERR_INVALID_ARG;
+    if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) return HPC_ERR_INVALID_ARG;
+    if (num_pages < 1 || (long long)num_pages * kChunk > 2147483647LL || page_table_stride < 1)
+        return HPC_ERR_INVALID_ARG;
+    if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
+    AttnArgs a;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.k_scale = fp8 ? k_scale : nullptr;
+    a.v_scale = fp8 ? v_scale : nullptr;
+    a.fp8 = fp8;
+    a.num_pages = num_pages;
+    a.page_table = page_table;
+    a.pt_stride = page_table_stride;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.plan = plan->buf;
+    a.num_ctas = plan->num_ctas;
+    a.mode = plan->mode;
+    a.split_cap = (long long)hpc_decode_split_capacity(batch, num_kv_heads, plan->num_ctas);
+    a.split_o = split_o;
+    a.split_lse = split_lse;
+    cudaError_t e = launch_attn(a, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue) return HPC_ERR_INVALID_ARG;
+    return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse, void* out,
+                              float* out_lse, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                              void* stream) {
+    hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, kChunk);
+    if (st != HPC_OK) return st;
+    if (!split_o || !split_lse || !out || !aligned(split_o, 16) || !aligned(out, 8)) return HPC_ERR_INVALID_ARG;
+    if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
+    cudaError_t e = launch_combine(plan->buf, plan->num_ctas, split_o, split_lse,
+                                   static_cast<__nv_bfloat16*>(out), out_lse, batch, num_q_heads, num_kv_heads,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+size_t hpc_decode_step_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int page_table_stride,
+                                       int num_ctas) {
+    if (!sizes_ok(batch, num_kv_heads, num_ctas) || page_table_stride < 1 || num_q_heads < 1) return 0;
+    return step_workspace(batch, num_q_heads, num_kv_heads, page_table_stride, num_ctas).total;
+}
+
+hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens, const int32_t* h_page_table,
+                                int page_table_stride, const void* d_k_cache, const void* d_v_cache,
+                                const float* d_k_scale, const float* d_v_scale, int kv_dtype, int num_pages,
+                                int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                int num_ctas, int min_chunks_per_cta, void* d_workspace,
+                                size_t workspace_bytes, void* h_out, float* h_out_lse, void* stream) {
+    hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
+    if (st != HPC_OK) return st;
+    if (!h_q || !h_seq_lens || !h_page_table || !d_workspace || !h_out) return HPC_ERR_INVALID_ARG;
+    if (!sizes_ok(batch, num_kv_heads, num_ctas) || page_table_stride < 1 || !aligned(d_workspace, 256))
+        return HPC_ERR_INVALID_ARG;
+    const StepWorkspace w = step_workspace(batch, num_q_heads, num_kv_heads, page_table_stride, num_ctas);
+    if (workspace_bytes < w.total) return HPC_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+    const size_t q_bytes = (size_t)batch * num_q_heads * kHeadDim * 2;
+    if (cudaMemcpyAsync(ws + w.q, h_q, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+        cudaMemcpyAsync(ws + w.seq_lens, h_seq_lens, (size_t)batch * 4, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(ws + w.page_table, h_page_table, (size_t)batch * page_table_stride * 4,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return HPC_ERR_CUDA;
+    hpc_plan plan{};
+    plan.buf = reinterpret_cast<int32_t*>(ws + w.plan);
+    plan.bytes = hpc_decode_plan_bytes(batch, num_kv_heads, num_ctas);
+    const int32_t* d_sl = reinterpret_cast<const int32_t*>(ws + w.seq_lens);
+    if ((st = hpc_decode_plan(d_sl, batch, num_kv_heads, num_ctas, min_chunks_per_cta, &plan, stream)) != HPC_OK)
+        return st;
+    float* so = reinterpret_cast<float*>(ws + w.split_o);
+    float* sl = reinterpret_cast<float*>(ws + w.split_lse);
+    if ((st = hpc_decode_attn(ws + w.q, d_k_cache, d_v_cache, d_k_scale, d_v_scale, kv_dtype, num_pages,
+                              reinterpret_cast<const int32_t*>(ws + w.page_table), page_table_stride, d_sl,
+                              batch, num_q_heads, num_kv_heads, head_dim, page_size, &plan, so, sl, stream)) !=
+        HPC_OK)
+        return st;
+    float* d_lse = reinterpret_cast<float*>(ws + w.out_lse);
+    if ((st = hpc_decode_combine(&plan, so, sl, ws + w.out, d_lse, batch, num_q_heads, num_kv_heads, head_dim,
+                                 stream)) != HPC_OK)
+        return st;
+    if (cudaMemcpyAsync(h_out, ws + w.out, q_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return HPC_ERR_CUDA;
+    if (h_out_lse &&
+        cudaMemcpyAsync(h_out_lse, d_lse, (size_t)batch * num_q_heads * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return HPC_ERR_CUDA;
+    return HPC_OK;
+}
+
+hpc_status hpc_decode_read_error(const hpc_plan* plan, int* device_error_word) {
+    if (!plan || !plan->buf || !device_error_word) return HPC_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return HPC_ERR_CUDA;
+    int w = 0;
+    if (cudaMemcpy(&w, plan->buf + kHError, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return HPC_ERR_CUDA;
+    *device_error_word = w;
+    return w ? HPC_ERR_DEVICE_CHECK : HPC_OK;
+}
+
+const char* hpc_status_string(hpc_status status) {
+    switch (status) {
+        case HPC_OK: return "ok";
+        case HPC_ERR_INVALID_ARG: return "invalid argument";
+        case HPC_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case HPC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case HPC_ERR_CUDA: return "CUDA launch or copy failed";
+        case HPC_ERR_DEVICE_CHECK: return "device-side check failed (see the error word)";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

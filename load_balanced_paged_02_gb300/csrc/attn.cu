@@ -1,0 +1,647 @@
+// Persistent paged GQA decode attention (compute stage of the load-balanced
+// scheduler: HPC-Ops/SGLang blog, "Scheduling around live KV work", the
+// paragraph on execution; vLLM x HPC-Ops blog, "解决方案：按步负载均衡的
+// decode 调度器", compute-and-combine stage).
+//
+// CTA j drains its task list: for every descriptor (kv head h, request b,
+// chunks [c0, c1), split s) it computes, for the 8 query heads of h, softmax
+// attention over tokens [64*c0, min(64*c1, L_b)) and writes the normalised
+// partial output and its natural-log LSE to row s of the split buffers.
+//
+// Block = NG*4 consumer warps + 1 producer warp.
+//  * Producer warp: walks the same list; its lanes fetch 32 page ids at a
+//    time, lane 0 streams each 64-token chunk (= one page) of K and V into a
+//    STAGES-deep shared-memory ring with TMA (3-D tensor maps over
+//    [pages*64, Hkv, 128], 128-byte swizzle, L2 evict-first) and the Q rows of
+//    each descriptor (2 KB bulk copy) into a 2-slot ring. mbarrier full/empty
+//    pairs hand stages over; a per-stage word carries the chunk's valid token
+//    count (0 = skip: page id out of range).
+//  * Consumer warps: group gi takes the chunks whose running index is gi mod
+//    NG; inside a chunk warp w takes tokens [16w, 16w+16). Tokens are the M
+//    dimension of mma.m16n8k16 and the GQA group of 8 query heads is N, so
+//    S^T = K Q^T and O^T += V^T P^T need no padding: the S^T accumulator is
+//    turned into the P^T operand by movmatrix.trans. Each warp keeps its own
+//    online-softmax state (log2 domain) and the warps' states are merged
+//    through shared memory at the end of each descriptor.
+//  * e4m3 caches: codes are widened exactly to f16 (Q to f16 once per
+//    descriptor). K scales multiply the score rows; V scales (x256, undone at
+//    the end) fold into P. The k index of S^T and the m index of O^T are
+//    permuted so that each thread reads whole 16-byte rows without bank
+//    conflicts; the permutation is undone when the merge writes dims back.
+// Every wait is bounded (2 s by %globaltimer); on expiry the CTA records
+// HPC_DEVERR_WAIT_TIMEOUT, the producer waits (bounded) for its copies in
+// flight, and the CTA returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "hpc_internal.cuh"
+
+namespace hpc {
+namespace {
+
+constexpr int kQSlotBytes = kGroup * kHeadDim * 2;  // 2 KB of bf16 Q rows
+constexpr int kScratchStride = 132;                 // floats per (warp, query) merge row
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <bool FP8>
+struct KvCfg;
+template <>
+struct KvCfg<false> {
+    static constexpr int kStageBytes = 32768;  // K dims 0-63 | K 64-127 | V 0-63 | V 64-127
+    static constexpr uint32_t kTxBytes = 32768;
+    static constexpr float kPScale = 1.0f;
+};
+template <>
+struct KvCfg<true> {
+    static constexpr int kStageBytes = 17408;  // K 8 KB | V 8 KB | K scales 256 B | V scales 256 B
+    static constexpr uint32_t kTxBytes = 16384 + 512;
+    static constexpr float kPScale = 256.0f;
+};
+
+template <bool FP8, int STAGES, int NG>
+struct Layout {
+    static constexpr int kNCW = NG * 4;
+    static constexpr size_t kQ = (size_t)STAGES * KvCfg<FP8>::kStageBytes;
+    static constexpr size_t kScratch = kQ + 2 * kQSlotBytes;
+    static constexpr size_t kML = kScratch + (size_t)kNCW * kGroup * kScratchStride * 4;
+    static constexpr size_t kMeta = kML + (size_t)kNCW * kGroup * 8;
+    static constexpr size_t kBars = (kMeta + STAGES * 4 + 7) / 8 * 8;
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr size_t kFlag = kBars + kNumBars * 8;
+    static constexpr size_t kTotal = kFlag + 16;
+    static constexpr size_t kAlloc = kTotal + 1024;  // base is rounded up to 1 KB (128B swizzle)
+    static constexpr int kThreads = (kNCW + 1) * 32;
+};
+
+struct Params {
+    const __nv_bfloat16* q;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* page_table;
+    long long pt_stride;
+    const int32_t* seq_lens;
+    int batch, num_q_heads, num_kv_heads, num_pages;
+    const int32_t* cta_off;
+    const int32_t* tasks;
+    int* err;
+    long long split_cap;
+    float* split_o;
+    float* split_lse;
+    float scale_log2;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool desc_ok(const Params& p, int h, int b, int c0, int c1, int s) {
+    return h < p.num_kv_heads && b >= 0 && b < p.batch && c0 >= 0 && c1 > c0 && c1 <= p.pt_stride &&
+           s >= 0 && s < p.split_cap;
+}
+
+// ------------------------------------------------------------------ consumer math
+
+template <bool FP8>
+__device__ __forceinline__ void load_q_frags(uint32_t qbase, int lane, uint32_t (&qf)[8][2]) {
+    if constexpr (!FP8) {
+        // Q^T B-fragments: rows are the 8 query heads, 16-byte columns are dims.
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+            uint32_t r[4];
+            ldsm_x4(r, qbase + (uint32_t)(lane & 7) * 256u + (uint32_t)(4 * kp + (lane >> 3)) * 16u);
+            qf[2 * kp][0] = r[0];
+            qf[2 * kp][1] = r[1];
+            qf[2 * kp + 1][0] = r[2];
+            qf[2 * kp + 1][1] = r[3];
+        }
+    } else {
+        // Thread (g, c) holds dims [32c, 32c+32) of query g; k-step ks uses
+        // dims 32c+4ks+{0,1} (b0b1) and 32c+4ks+{2,3} (b2b3), widened to f16.
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t base = qbase + (uint32_t)g * 256u + (uint32_t)c * 64u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = lds128(base + 16u * i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int word = 4 * i + j;  // dims 32c + 2*word, +1
+                __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+                const float2 f = __bfloat1622float2(bv);
+                qf[word >> 1][word & 1] = pack_f16x2(f.x, f.y);
+            }
+        }
+    }
+}
+
+// Online-softmax update of one warp's state with a 16-token x 8-query score
+// tile s (log2 domain, masked entries -inf). Returns P in p.
+__device__ __forceinline__ void softmax_step(float (&s)[4], float (&m)[2], float (&l)[2],
+                                             float (&o)[8][4], float (&p)[4]) {
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
+    const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
+    const float al0 = fast_exp2(m[0] - mu0), al1 = fast_exp2(m[1] - mu1);
+    m[0] = mn0;
+    m[1] = mn1;
+    p[0] = fast_exp2(s[0] - mu0);
+    p[1] = fast_exp2(s[1] - mu1);
+    p[2] = fast_exp2(s[2] - mu0);
+    p[3] = fast_exp2(s[3] - mu1);
+    l[0] = l[0] * al0 + p[0] + p[2];
+    l[1] = l[1] * al1 + p[1] + p[3];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al1;
+        o[i][2] *= al0;
+        o[i][3] *= al1;
+    }
+}
+
+// Zero V rows [16*wq + nv, 16*wq + 16) of a stage (tokens past the live length
+// in the last page may hold any bits, and 0 * NaN would poison P V).
+template <bool FP8>
+__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int wq, int nv, int lane) {
+    constexpr int kVecPerRow = FP8 ? 8 : 16;
+    const int n = (16 - nv) * kVecPerRow;
+    for (int i = lane; i < n; i += 32) {
+        const int r = 16 * wq + nv + i / kVecPerRow;
+        const int part = i % kVecPerRow;
+        uint8_t* dst;
+        if constexpr (FP8)
+            dst = stage + 8192 + r * 128 + part * 16;
+        else
+            dst = stage + 16384 + (part >> 3) * 8192 + r * 128 + (part & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+}
+
+template <bool FP8>
+__device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, int nv,
+                                              const uint32_t (&qf)[8][2], float (&o)[8][4],
+                                              float (&m)[2], float (&l)[2], float scale_log2) {
+    const int g = lane >> 2, c = lane & 3;
+    const uint32_t sb = smem_u32(stage);
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    float s[4], p[4];
+    if (nv < 16) zero_v_tail<FP8>(stage, wq, nv, lane);
+
+    if constexpr (!FP8) {
+        // ---- S^T = K Q^T over 8 k-steps of 16 dims (two independent chains)
+        const int rr = lane & 7;
+        const uint32_t krow = sb + (uint32_t)(16 * wq + ((lane >> 3) & 1) * 8 + rr) * 128u;
+        const uint32_t kx = (uint32_t)((lane >> 4) ^ rr);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, krow + (uint32_t)(ks >> 2) * 8192u + (((uint32_t)(2 * (ks & 3)) ^ kx) << 4));
+            if (ks & 1)
+                mma_bf16(acc1, a, qf[ks][0], qf[ks][1]);
+            else
+                mma_bf16(acc0, a, qf[ks][0], qf[ks][1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i] = (acc0[i] + acc1[i]) * scale_log2;
+        if (nv < 16) {
+            if (g >= nv) s[0] = s[1] = kNegInf;
+            if (g + 8 >= nv) s[2] = s[3] = kNegInf;
+        }
+        softmax_step(s, m, l, o, p);
+        const uint32_t pb0 = movmatrix_t(pack_bf16x2(p[0], p[1]));
+        const uint32_t pb1 = movmatrix_t(pack_bf16x2(p[2], p[3]));
+        // ---- O^T += V^T P^T, 8 m-tiles of 16 dims
+        const uint32_t vrow = sb + 16384u + (uint32_t)(16 * wq + (lane >> 4) * 8 + rr) * 128u;
+        const uint32_t vx = (uint32_t)(((lane >> 3) & 1) ^ rr);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t a[4];
+            ldsm_x4_t(a, vrow + (uint32_t)(i >> 2) * 8192u + (((uint32_t)(2 * (i & 3)) ^ vx) << 4));
+            mma_bf16(o[i], a, pb0, pb1);
+        }
+    } else {
+        const float* ksc = reinterpret_cast<const float*>(stage + 16384);
+        const float* vsc = ksc + 64;
+        const int r0 = 16 * wq + g;
+        const uint32_t kb = sb;
+        // ---- S^T: thread reads dims [32c, 32c+32) of token rows r0 and r0+8
+        const uint4 k00 = lds128(kb + (uint32_t)r0 * 128u + ((uint32_t)((2 * c) ^ g) << 4));
+        const uint4 k01 = lds128(kb + (uint32_t)r0 * 128u + ((uint32_t)((2 * c + 1) ^ g) << 4));
+        const uint4 k10 = lds128(kb + (uint32_t)(r0 + 8) * 128u + ((uint32_t)((2 * c) ^ g) << 4));
+        const uint4 k11 = lds128(kb + (uint32_t)(r0 + 8) * 128u + ((uint32_t)((2 * c + 1) ^ g) << 4));
+        const uint32_t w0[8] = {k00.x, k00.y, k00.z, k00.w, k01.x, k01.y, k01.z, k01.w};
+        const uint32_t w1[8] = {k10.x, k10.y, k10.z, k10.w, k11.x, k11.y, k11.z, k11.w};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            a[0] = e4m3x2_to_f16x2(w0[ks]);
+            a[1] = e4m3x2_to_f16x2(w1[ks]);
+            a[2] = e4m3x2_to_f16x2(w0[ks] >> 16);
+            a[3] = e4m3x2_to_f16x2(w1[ks] >> 16);
+            if (ks & 1)
+                mma_f16(acc1, a, qf[ks][0], qf[ks][1]);
+            else
+                mma_f16(acc0, a, qf[ks][0], qf[ks][1]);
+        }
+        const float ks0 = ksc[r0] * scale_log2, ks1 = ksc[r0 + 8] * scale_log2;
+        s[0] = (acc0[0] + acc1[0]) * ks0;
+        s[1] = (acc0[1] + acc1[1]) * ks0;
+        s[2] = (acc0[2] + acc1[2]) * ks1;
+        s[3] = (acc0[3] + acc1[3]) * ks1;
+        const bool v0 = g < nv, v1 = g + 8 < nv;
+        if (!v0) s[0] = s[1] = kNegInf;
+        if (!v1) s[2] = s[3] = kNegInf;
+        softmax_step(s, m, l, o, p);
+        const float vs0 = v0 ? vsc[r0] * KvCfg<true>::kPScale : 0.f;
+        const float vs1 = v1 ? vsc[r0 + 8] * KvCfg<true>::kPScale : 0.f;
+        const uint32_t pb0 = movmatrix_t(pack_f16x2(v0 ? p[0] * vs0 : 0.f, v0 ? p[1] * vs0 : 0.f));
+        const uint32_t pb1 = movmatrix_t(pack_f16x2(v1 ? p[2] * vs1 : 0.f, v1 ? p[3] * vs1 : 0.f));
+        // ---- O^T += V^T P^T: thread reads the 16-byte column g of token rows
+        // 2c, 2c+1, 2c+8, 2c+9; m-tile i row g is dim 16g+2i, row g+8 is 16g+2i+1
+        const uint32_t vb = sb + 8192u;
+        const int t0 = 16 * wq + 2 * c;
+        const uint4 R0 = lds128(vb + (uint32_t)t0 * 128u + ((uint32_t)(g ^ (2 * c)) << 4));
+        const uint4 R1 = lds128(vb + (uint32_t)(t0 + 1) * 128u + ((uint32_t)(g ^ (2 * c + 1)) << 4));
+        const uint4 R2 = lds128(vb + (uint32_t)(t0 + 8) * 128u + ((uint32_t)(g ^ (2 * c)) << 4));
+        const uint4 R3 = lds128(vb + (uint32_t)(t0 + 9) * 128u + ((uint32_t)(g ^ (2 * c + 1)) << 4));
+        const uint32_t x0[4] = {R0.x, R0.y, R0.z, R0.w}, x1[4] = {R1.x, R1.y, R1.z, R1.w};
+        const uint32_t x2[4] = {R2.x, R2.y, R2.z, R2.w}, x3[4] = {R3.x, R3.y, R3.z, R3.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+            const uint32_t u = prmt(x0[i >> 1], x1[i >> 1], sel);
+            const uint32_t v = prmt(x2[i >> 1], x3[i >> 1], sel);
+            uint32_t a[4];
+            a[0] = e4m3x2_to_f16x2(u);
+            a[1] = e4m3x2_to_f16x2(u >> 16);
+            a[2] = e4m3x2_to_f16x2(v);
+            a[3] = e4m3x2_to_f16x2(v >> 16);
+            mma_f16(o[i], a, pb0, pb1);
+        }
+    }
+    if (nv < 16) fence_proxy_async_smem();  // generic zero-fill before the next TMA write
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <bool FP8, int STAGES, int NG>
+__global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using LY = Layout<FP8, STAGES, NG>;
+    using Cfg = KvCfg<FP8>;
+    constexpr int NCW = LY::kNCW;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + LY::kBars);
+    uint64_t* empty = full + STAGES;
+    uint64_t* qfull = empty + STAGES;
+    uint64_t* qempty = qfull + 2;
+    uint64_t* merge_bar = qempty + 2;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kFlag);
+    volatile int* meta = reinterpret_cast<volatile int*>(smem + LY::kMeta);
+    uint8_t* qbuf = smem + LY::kQ;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 4);  // a stage is consumed by the 4 warps of one group
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], NCW);
+        }
+        mbar_init(merge_bar, NCW * 32);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int list0 = p.cta_off[blockIdx.x];
+
+    if (warp == NCW) {
+        // ============================ producer warp
+        const uint64_t pol = l2_evict_first_policy();
+        uint32_t seq = 0;
+        int qd = 0;
+        bool ok = true;
+        for (int slot = list0; ok; ++slot) {
+            const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
+            const int4 t1 =
+                __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
+            const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
+            if (h < 0) break;
+            if (!desc_ok(p, h, b, c0, c1, t1.x)) {
+                if (lane == 0) atomicOr(p.err, (int)HPC_DEVERR_BAD_DESCRIPTOR);
+                continue;
+            }
+            const int L = __ldg(p.seq_lens + b);
+            const int qs = qd & 1;
+            if (lane == 0) {
+                ok = wait_bounded(&qempty[qs], ((qd >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
+                if (ok) {
+                    mbar_arrive_expect_tx(&qfull[qs], kQSlotBytes);
+                    bulk_load_nohint(qbuf + qs * kQSlotBytes,
+                                     p.q + ((long long)b * p.num_q_heads + (long long)h * kGroup) * kHeadDim,
+                                     kQSlotBytes, &qfull[qs]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++qd;
+            const int32_t* prow = p.page_table + (long long)b * p.pt_stride;
+            for (int cb = c0; cb < c1 && ok; cb += 32) {
+                const int cl = cb + lane;
+                const int pg = cl < c1 ? __ldg(prow + cl) : 0;
+                const int n = min(32, c1 - cb);
+                for (int j = 0; j < n; ++j, ++seq) {
+                    const int page = __shfl_sync(0xffffffffu, pg, j);
+                    const int cc = cb + j;
+                    const int nvalid = min(kChunk, L - kChunk * cc);
+                    const bool page_ok = (unsigned)page < (unsigned)p.num_pages;
+                    const int st = (int)(seq % STAGES);
+                    const uint32_t ph = (seq / STAGES) & 1;
+                    if (lane == 0) {
+                        ok = wait_bounded(&empty[st], ph ^ 1, abort_flag, kWaitLimitNs);
+                        if (ok) {
+                            if (!page_ok) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
+                            if (page_ok && nvalid > 0) {
+                                meta[st] = nvalid;
+                                mbar_arrive_expect_tx(&full[st], Cfg::kTxBytes);
+                                uint8_t* sbuf = smem + (size_t)st * Cfg::kStageBytes;
+                                const int tok = page * kChunk;
+                                if constexpr (FP8) {
+                                    tma_load_3d(sbuf, &tm_k, &full[st], 0, h, tok, pol);
+                                    tma_load_3d(sbuf + 8192, &tm_v, &full[st], 0, h, tok, pol);
+                                    const long long so = ((long long)page * p.num_kv_heads + h) * kChunk;
+                                    bulk_load(sbuf + 16384, p.k_scale + so, 256, &full[st], pol);
+                                    bulk_load(sbuf + 16640, p.v_scale + so, 256, &full[st], pol);
+                                } else {
+                                    tma_load_3d(sbuf, &tm_k, &full[st], 0, h, tok, pol);
+                                    tma_load_3d(sbuf + 8192, &tm_k, &full[st], 64, h, tok, pol);
+                                    tma_load_3d(sbuf + 16384, &tm_v, &full[st], 0, h, tok, pol);
+                                    tma_load_3d(sbuf + 24576, &tm_v, &full[st], 64, h, tok, pol);
+                                }
+                            } else {
+                                meta[st] = 0;
+                                mbar_arrive(&full[st]);
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(p.err, (int)HPC_DEVERR_WAIT_TIMEOUT);
+            // wait (bounded) for the copies this warp may still have in flight
+            const uint32_t first = seq > (uint32_t)STAGES ? seq - STAGES : 0u;
+            for (uint32_t k = first; k < seq; ++k)
+                wait_bounded(&full[k % STAGES], (k / STAGES) & 1, nullptr, kDrainLimitNs);
+            if (qd > 0) wait_bounded(&qfull[(qd - 1) & 1], ((qd - 1) >> 1) & 1, nullptr, kDrainLimitNs);
+        }
+        return;
+    }
+
+    // ================================ consumer warps
+    const int gi = warp >> 2, wq = warp & 3;
+    const int g = lane >> 2, c = lane & 3;
+    float* scratch = reinterpret_cast<float*>(smem + LY::kScratch);
+    float2* ml = reinterpret_cast<float2*>(smem + LY::kML);
+    uint32_t seq = 0, mphase = 0;
+    int qd = 0;
+    for (int slot = list0;; ++slot) {
+        const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
+        const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
+        const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w, s = t1.x;
+        if (h < 0) break;
+        if (!desc_ok(p, h, b, c0, c1, s)) continue;
+        (void)b;
+
+        uint32_t qf[8][2];
+        const int qs = qd & 1;
+        if (!wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
+        load_q_frags<FP8>(smem_u32(qbuf + qs * kQSlotBytes), lane, qf);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qempty[qs]);
+        ++qd;
+
+        {
+            float o[8][4];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f};
+
+            for (int cc = c0; cc < c1; ++cc, ++seq) {
+                if (NG > 1 && (int)(seq % NG) != gi) continue;
+                const int st = (int)(seq % STAGES);
+                if (!wait_bounded(&full[st], (seq / STAGES) & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                const int nv = meta[st] - 16 * wq;
+                if (nv > 0)
+                    chunk_compute<FP8>(smem + (size_t)st * Cfg::kStageBytes, wq, lane, nv < 16 ? nv : 16, qf,
+                                       o, m, l, p.scale_log2);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+
+            // ---- merge the NCW warps' states of this descriptor
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+                l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+            }
+            float* scr = scratch + warp * kGroup * kScratchStride;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if constexpr (FP8) {
+                    const int d = 16 * g + 2 * i;
+                    *reinterpret_cast<float2*>(scr + (2 * c) * kScratchStride + d) = make_float2(o[i][0], o[i][2]);
+                    *reinterpret_cast<float2*>(scr + (2 * c + 1) * kScratchStride + d) =
+                        make_float2(o[i][1], o[i][3]);
+                } else {
+                    const int d = 16 * i + g;
+                    scr[(2 * c) * kScratchStride + d] = o[i][0];
+                    scr[(2 * c + 1) * kScratchStride + d] = o[i][1];
+                    scr[(2 * c) * kScratchStride + d + 8] = o[i][2];
+                    scr[(2 * c + 1) * kScratchStride + d + 8] = o[i][3];
+                }
+            }
+            if (g == 0) {
+                ml[warp * kGroup + 2 * c] = make_float2(m[0], l[0]);
+                ml[warp * kGroup + 2 * c + 1] = make_float2(m[1], l[1]);
+            }
+        }
+        mbar_arrive(merge_bar);
+        if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
+        ++mphase;
+        {
+            const int ct = warp * 32 + lane;
+            for (int idx = ct; idx < kGroup * 32; idx += NCW * 32) {
+                const int qh = idx >> 5, d4 = idx & 31;
+                float M = kNegInf;
+#pragma unroll
+                for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[w * kGroup + qh].x);
+                float lsum = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (M != kNegInf) {
+#pragma unroll
+                    for (int w = 0; w < NCW; ++w) {
+                        const float2 v = ml[w * kGroup + qh];
+                        const float f = fast_exp2(v.x - M);
+                        lsum += v.y * f;
+                        const float4 x = *reinterpret_cast<const float4*>(
+                            scratch + (w * kGroup + qh) * kScratchStride + 4 * d4);
+                        acc.x += f * x.x;
+                        acc.y += f * x.y;
+                        acc.z += f * x.z;
+                        acc.w += f * x.w;
+                    }
+                }
+                const float inv = lsum > 0.f ? 1.f / (lsum * Cfg::kPScale) : 0.f;
+                float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                *reinterpret_cast<float4*>(p.split_o + ((long long)s * kGroup + qh) * kHeadDim + 4 * d4) = r;
+                if (d4 == 0)
+                    p.split_lse[(long long)s * kGroup + qh] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : kNegInf;
+            }
+        }
+        mbar_arrive(merge_bar);
+        if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
+        ++mphase;
+    }
+    return;
+timeout:
+    if (lane == 0) {
+        *abort_flag = 1;
+        atomicOr(p.err, (int)HPC_DEVERR_WAIT_TIMEOUT);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 3-D map over a paged cache [num_pages*64 tokens][Hkv][128]; box = 64 tokens
+// x 1 head x (64 bf16 or 128 e4m3 = 128 bytes), 128-byte swizzle.
+bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int Hkv) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t esz = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv, (cuuint64_t)num_pages * kChunk};
+    cuuint64_t strides[2] = {kHeadDim * esz, (cuuint64_t)Hkv * kHeadDim * esz};
+    cuuint32_t box[3] = {fp8 ? 128u : 64u, 1u, (cuuint32_t)kChunk};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <bool FP8, int STAGES, int NG>
+struct Inst {
+    using LY = Layout<FP8, STAGES, NG>;
+    static const void* fn() { return reinterpret_cast<const void*>(&decode_attn_kernel<FP8, STAGES, NG>); }
+    static cudaError_t prepare() {
+        return cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::kAlloc);
+    }
+    static cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
+                              cudaStream_t s) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        decode_attn_kernel<FP8, STAGES, NG><<<grid, LY::kThreads, LY::kAlloc, s>>>(mk, mv, p);
+        return cudaGetLastError();
+    }
+    static int ctas_per_sm() {
+        if (prepare() != cudaSuccess) return 0;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<FP8, STAGES, NG>,
+                                                          LY::kThreads, LY::kAlloc) != cudaSuccess)
+            return 0;
+        return n;
+    }
+};
+
+// Persistent (load-balanced) instances: deep rings, one CTA per SM.
+using BalancedBf16 = Inst<false, 6, 1>;
+using BalancedFp8 = Inst<true, 10, 2>;
+// Static split-KV instances: one descriptor per CTA, shallow rings so that
+// several CTAs share an SM, as a non-persistent split-KV grid would.
+using StaticBf16 = Inst<false, 2, 1>;
+using StaticFp8 = Inst<true, 4, 1>;
+
+}  // namespace
+
+int attn_default_ctas(int fp8) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    const int per = fp8 ? BalancedFp8::ctas_per_sm() : BalancedBf16::ctas_per_sm();
+    return sms * (per > 0 ? per : 1);
+}
+
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
+    CUtensorMap mk, mv;
+    if (!make_kv_map(&mk, a.k_cache, a.fp8, a.num_pages, a.num_kv_heads) ||
+        !make_kv_map(&mv, a.v_cache, a.fp8, a.num_pages, a.num_kv_heads))
+        return cudaErrorInvalidValue;
+    const PlanLayout L = plan_layout(a.batch, a.num_kv_heads, a.num_ctas);
+    Params p;
+    p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    p.k_scale = a.k_scale;
+    p.v_scale = a.v_scale;
+    p.page_table = a.page_table;
+    p.pt_stride = a.pt_stride;
+    p.seq_lens = a.seq_lens;
+    p.batch = a.batch;
+    p.num_q_heads = a.num_q_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.num_pages = a.num_pages;
+    p.cta_off = a.plan + L.cta_off;
+    p.tasks = a.plan + L.tasks;
+    p.err = const_cast<int32_t*>(a.plan) + kHError;
+    p.split_cap = a.split_cap;
+    p.split_o = a.split_o;
+    p.split_lse = a.split_lse;
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
+    const bool stat = a.mode == 1;
+    if (a.fp8)
+        return stat ? StaticFp8::launch(mk, mv, p, a.num_ctas, s) : BalancedFp8::launch(mk, mv, p, a.num_ctas, s);
+    return stat ? StaticBf16::launch(mk, mv, p, a.num_ctas, s) : BalancedBf16::launch(mk, mv, p, a.num_ctas, s);
+}
+
+}  // namespace hpc

@@ -1,0 +1,84 @@
+// Combine stage (HPC-Ops/SGLang blog, "Scheduling around live KV work", the
+// paragraph on execution: the combine reads the actual split count of every
+// (request, head) and merges the partials under the global softmax
+// normalisation; vLLM x HPC-Ops blog, "解决方案：按步负载均衡的 decode 调度器",
+// the final combine into the BF16 output).
+//
+// One warp per output row (request b, query head qh); lane k owns dims
+// [4k, 4k+4). With n partials (o_i, lse_i) of pair (qh / 8, b):
+//   M = max lse_i, w_i = exp(lse_i - M), out = sum w_i o_i / sum w_i,
+//   out_lse = M + ln sum w_i.
+#include "hpc_internal.cuh"
+
+namespace hpc {
+namespace {
+
+constexpr int kCombineWarps = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    combine_kernel(const int32_t* __restrict__ pair_nsplit, const int32_t* __restrict__ pair_split0,
+                   const float* __restrict__ split_o, const float* __restrict__ split_lse,
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ out_lse, int B, int Hq) {
+    const int lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (row >= (long long)B * Hq) return;
+    const int b = (int)(row / Hq), qh = (int)(row % Hq);
+    const int h = qh / kGroup, j = qh % kGroup;
+    const long long pair = (long long)h * B + b;
+    const int n = pair_nsplit[pair];
+    const long long s0 = pair_split0[pair];
+
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lse = -INFINITY;
+    if (n == 1) {
+        acc = *reinterpret_cast<const float4*>(split_o + (s0 * kGroup + j) * kHeadDim + 4 * lane);
+        lse = split_lse[s0 * kGroup + j];
+    } else if (n > 1) {
+        float M = -INFINITY;
+        for (int i = lane; i < n; i += 32) M = fmaxf(M, split_lse[(s0 + i) * kGroup + j]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (M != -INFINITY) {
+            float wsum = 0.f;
+            for (int i = 0; i < n; ++i) {
+                const long long r = (s0 + i) * kGroup + j;
+                const float w = exp2f((split_lse[r] - M) * kLog2e);
+                const float4 x = *reinterpret_cast<const float4*>(split_o + r * kHeadDim + 4 * lane);
+                wsum += w;
+                acc.x += w * x.x;
+                acc.y += w * x.y;
+                acc.z += w * x.z;
+                acc.w += w * x.w;
+            }
+            const float inv = 1.f / wsum;
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
+            lse = M + log2f(wsum) * kLn2;
+        }
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + row * kHeadDim + 4 * lane) = packed;
+    if (out_lse && lane == 0) out_lse[row] = lse;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o, const float* split_lse,
+                           __nv_bfloat16* out, float* out_lse, int B, int Hq, int Hkv, cudaStream_t s) {
+    const PlanLayout L = plan_layout(B, Hkv, C);
+    const long long rows = (long long)B * Hq;
+    const long long blocks = (rows + kCombineWarps - 1) / kCombineWarps;
+    combine_kernel<<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(plan + L.pair_nsplit, plan + L.pair_split0,
+                                                                  split_o, split_lse, out, out_lse, B, Hq);
+    return cudaGetLastError();
+}
+
+}  // namespace hpc

@@ -1,0 +1,283 @@
+// Task-map planners (one block, integer only).
+//
+// Load-balanced map: HPC-Ops/SGLang blog, "Scheduling around live KV work";
+// vLLM x HPC-Ops blog, "解决方案：按步负载均衡的 decode 调度器" (assign stage).
+// Static map: HPC-Ops/SGLang blog, "Attention: load balancing for mixed-length
+// decode", policy (1), a fixed split count.
+//
+// The planner never walks chunks one by one. For pair p = (h, b) with n_b
+// chunks starting at global chunk g0 = h*N + prefix_b, the CTAs it touches are
+// g0/bucket .. (g0+n_b-1)/bucket; descriptor k of the pair lives in CTA
+// g0/bucket + k and covers [max(g0, cta*bucket), min(g0+n_b, (cta+1)*bucket)).
+// Its split index s is the running descriptor count, and its task row is
+// s + cta (every earlier CTA contributed one terminator row).
+#include "hpc_internal.cuh"
+
+namespace hpc {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanWarps = kPlanThreads / 32;
+
+// Exclusive scan of one value per thread across the block. All threads must
+// call it. Returns the exclusive prefix; *total receives the block sum.
+__device__ long long block_exclusive_scan(long long v, long long* total, long long* warp_sums) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        long long w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    long long prefix = (wid > 0 ? warp_sums[wid - 1] : 0) + x - v;
+    *total = warp_sums[kPlanWarps - 1];
+    __syncthreads();
+    return prefix;
+}
+
+__device__ __forceinline__ void write_row(int32_t* row, int a, int b, int c, int d, int e, int f,
+                                          int g) {
+    reinterpret_cast<int4*>(row)[0] = make_int4(a, b, c, d);
+    reinterpret_cast<int4*>(row)[1] = make_int4(e, f, g, 0);
+}
+
+__device__ __forceinline__ void write_term(int32_t* row) {
+    reinterpret_cast<int4*>(row)[0] = make_int4(-1, -1, -1, -1);
+    reinterpret_cast<int4*>(row)[1] = make_int4(-1, -1, -1, -1);
+}
+
+// Chunk prefix sums pre[0..B] (pre[B] = N) of n_b = ceil(max(L_b, 0) / 64).
+// Returns N, or 0 with every prefix zeroed when Hkv * N overflows int32.
+__device__ long long chunk_prefix(const int32_t* __restrict__ seq_lens, int B, int Hkv, int32_t* pre,
+                                  long long* warp_sums, int* s_err) {
+    const int tid = threadIdx.x;
+    long long running = 0;
+    for (int base = 0; base < B; base += kPlanThreads) {
+        const int b = base + tid;
+        long long n = 0;
+        if (b < B) {
+            long long L = seq_lens[b];
+            if (L < 0) {
+                atomicOr(s_err, (int)HPC_DEVERR_NEGATIVE_LENGTH);
+                L = 0;
+            }
+            n = (L + kChunk - 1) / kChunk;
+        }
+        long long tot;
+        long long ex = block_exclusive_scan(n, &tot, warp_sums);
+        if (b < B) pre[b] = (int32_t)(running + ex);
+        running += tot;
+    }
+    const bool overflow = running * (long long)Hkv > 2147483647LL;
+    __syncthreads();
+    if (overflow) {
+        for (int b = tid; b <= B; b += kPlanThreads) pre[b] = 0;
+        if (tid == 0) atomicOr(s_err, (int)HPC_DEVERR_CHUNK_OVERFLOW);
+        running = 0;
+    } else if (tid == 0) {
+        pre[B] = (int32_t)running;
+    }
+    __syncthreads();
+    return running;
+}
+
+__device__ void write_header(int32_t* buf, long long T, long long bucket, long long used,
+                             long long splits, int C, int B, int Hkv, int m, long long max_tasks,
+                             int mode, long long N, int err) {
+    buf[kHTotalChunks] = (int32_t)T;
+    buf[kHBucket] = (int32_t)bucket;
+    buf[kHUsedCtas] = (int32_t)used;
+    buf[kHTotalSplits] = (int32_t)splits;
+    buf[kHNumCtas] = C;
+    buf[kHBatch] = B;
+    buf[kHNumKvHeads] = Hkv;
+    buf[kHMinChunks] = m;
+    buf[kHMaxTasks] = (int32_t)max_tasks;
+    buf[kHMode] = mode;
+    buf[kHChunksPerHead] = (int32_t)N;
+    buf[kHChunkTokens] = kChunk;
+    buf[kHError] = err;
+    buf[13] = buf[14] = buf[15] = 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+    plan_balanced_kernel(const int32_t* __restrict__ seq_lens, int B, int Hkv, int C, int m,
+                         int32_t* __restrict__ buf) {
+    extern __shared__ int32_t pre[];  // [B + 1]
+    __shared__ long long warp_sums[32];
+    __shared__ int s_err;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+
+    const PlanLayout L = plan_layout(B, Hkv, C);
+    int32_t* cta_off = buf + L.cta_off;
+    int32_t* tasks = buf + L.tasks;
+    int32_t* nsplit = buf + L.pair_nsplit;
+    int32_t* split0 = buf + L.pair_split0;
+
+    const long long N = chunk_prefix(seq_lens, B, Hkv, pre, warp_sums, &s_err);
+    const long long T = N * Hkv;
+    long long bucket = (T + C - 1) / C;
+    if (bucket < m) bucket = m;
+    if (bucket < 1) bucket = 1;
+    const long long used = T ? (T + bucket - 1) / bucket : 0;
+    const long long P = (long long)Hkv * B;
+
+    // split count of every (kv head, request) pair, then its first split index
+    long long running = 0;
+    for (long long base = 0; base < P; base += kPlanThreads) {
+        const long long p = base + tid;
+        long long ns = 0;
+        if (p < P) {
+            const int h = (int)(p / B), b = (int)(p % B);
+            const long long nb = pre[b + 1] - pre[b];
+            const long long g0 = (long long)h * N + pre[b];
+            ns = nb ? (g0 + nb - 1) / bucket - g0 / bucket + 1 : 0;
+        }
+        long long tot;
+        long long ex = block_exclusive_scan(ns, &tot, warp_sums);
+        if (p < P) {
+            nsplit[p] = (int32_t)ns;
+            split0[p] = (int32_t)(running + ex);
+        }
+        running += tot;
+    }
+    const long long total = running;
+    __syncthreads();
+
+    // descriptors, and the first task row of every used CTA
+    for (long long p = tid; p < P; p += kPlanThreads) {
+        const int h = (int)(p / B), b = (int)(p % B);
+        const long long nb = pre[b + 1] - pre[b];
+        if (!nb) continue;
+        const long long g0 = (long long)h * N + pre[b];
+        const long long first = g0 / bucket;
+        const int ns = nsplit[p];
+        const long long s0 = split0[p];
+        for (int k = 0; k < ns; ++k) {
+            const long long cta = first + k;
+            const long long lo = cta * bucket, hi = lo + bucket;
+            const long long cs = g0 > lo ? g0 : lo;
+            const long long ce = (g0 + nb) < hi ? (g0 + nb) : hi;
+            const long long s = s0 + k;
+            const long long slot = s + cta;
+            write_row(tasks + slot * kTaskInts, h, b, (int)(cs - g0), (int)(ce - g0), (int)s, k, ns);
+            if (cs == lo) cta_off[cta] = (int32_t)slot;
+        }
+    }
+    for (long long j = used + tid; j <= C; j += kPlanThreads) cta_off[j] = (int32_t)(total + j);
+    for (long long i = L.cta_off + C + 1 + tid; i < L.tasks; i += kPlanThreads) buf[i] = 0;
+    __syncthreads();
+    for (long long j = tid; j < C; j += kPlanThreads) write_term(tasks + (cta_off[j + 1] - 1) * kTaskInts);
+    for (long long r = total + C + tid; r < L.max_tasks; r += kPlanThreads) write_term(tasks + r * kTaskInts);
+    if (tid == 0)
+        write_header(buf, T, bucket, used, total, C, B, Hkv, m, L.max_tasks, 0, N, s_err);
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+    plan_static_kernel(const int32_t* __restrict__ seq_lens, int B, int Hkv, int S,
+                       int32_t* __restrict__ buf) {
+    extern __shared__ int32_t pre[];  // [B + 1]
+    __shared__ long long warp_sums[32];
+    __shared__ int s_err;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+
+    const long long C = (long long)Hkv * B * S;
+    const PlanLayout L = plan_layout(B, Hkv, C);
+    int32_t* cta_off = buf + L.cta_off;
+    int32_t* tasks = buf + L.tasks;
+    int32_t* nsplit = buf + L.pair_nsplit;
+    int32_t* split0 = buf + L.pair_split0;
+
+    const long long N = chunk_prefix(seq_lens, B, Hkv, pre, warp_sums, &s_err);
+    const long long P = (long long)Hkv * B;
+
+    // non-empty splits of a pair: s*q < n_b  <=>  s < ceil(n_b / q), q = ceil(n_b / S)
+    long long running = 0;
+    for (long long base = 0; base < P; base += kPlanThreads) {
+        const long long p = base + tid;
+        long long ns = 0;
+        if (p < P) {
+            const int b = (int)(p % B);
+            const long long nb = pre[b + 1] - pre[b];
+            const long long q = (nb + S - 1) / S;
+            ns = q ? (nb + q - 1) / q : 0;
+        }
+        long long tot;
+        long long ex = block_exclusive_scan(ns, &tot, warp_sums);
+        if (p < P) {
+            nsplit[p] = (int32_t)ns;
+            split0[p] = (int32_t)(running + ex);
+        }
+        running += tot;
+    }
+    const long long total = running;
+    __syncthreads();
+
+    for (long long j = tid; j < C; j += kPlanThreads) {
+        const long long p = j / S;
+        const int s = (int)(j % S);
+        const int h = (int)(p / B), b = (int)(p % B);
+        const long long nb = pre[b + 1] - pre[b];
+        const long long q = (nb + S - 1) / S;
+        const int ns = nsplit[p];
+        const long long s0 = split0[p];
+        const long long off = s0 + (s < ns ? s : ns) + j;
+        cta_off[j] = (int32_t)off;
+        if (s < ns) {
+            const long long c0 = (long long)s * q;
+            const long long c1 = (c0 + q) < nb ? (c0 + q) : nb;
+            write_row(tasks + off * kTaskInts, h, b, (int)c0, (int)c1, (int)(s0 + s), s, ns);
+            write_term(tasks + (off + 1) * kTaskInts);
+        } else {
+            write_term(tasks + off * kTaskInts);
+        }
+    }
+    if (tid == 0) cta_off[C] = (int32_t)(total + C);
+    for (long long i = L.cta_off + C + 1 + tid; i < L.tasks; i += kPlanThreads) buf[i] = 0;
+    for (long long r = total + C + tid; r < L.max_tasks; r += kPlanThreads) write_term(tasks + r * kTaskInts);
+    if (tid == 0)
+        write_header(buf, N * Hkv, 0, total, total, (int)C, B, Hkv, S, L.max_tasks, 1, N, s_err);
+}
+
+cudaError_t set_smem(const void* fn, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t* seq_lens, int B, int Hkv, int C, int m, int32_t* buf,
+                        cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * ((size_t)B + 1);
+    cudaError_t e = set_smem((const void*)plan_balanced_kernel, smem);
+    if (e != cudaSuccess) return e;
+    plan_balanced_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, B, Hkv, C, m, buf);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan_static(const int32_t* seq_lens, int B, int Hkv, int S, int32_t* buf,
+                               cudaStream_t s) {
+    const size_t smem = sizeof(int32_t) * ((size_t)B + 1);
+    cudaError_t e = set_smem((const void*)plan_static_kernel, smem);
+    if (e != cudaSuccess) return e;
+    plan_static_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, B, Hkv, S, buf);
+    return cudaGetLastError();
+}
+
+}  // namespace hpc

@@ -1,0 +1,119 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the binding and
+compare it with the float64 oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from load_balanced_paged_02_gb300 import binding as hb
+from load_balanced_paged_02_gb300 import workloads as wl
+
+BF16_MAX_ABS, BF16_MEAN_ABS = 2e-2, 2e-3
+FP8_MAX_ABS = 6e-2
+LSE_ABS = 1e-3
+
+
+def run(case, num_ctas=None, min_chunks=2, static_splits=None, plan=None):
+    """plan -> attn -> combine on the case's device. Returns a dict of tensors."""
+    Hkv = case["k_cache"].shape[2]
+    if plan is None:
+        if static_splits:
+            plan = hb.hpc_decode_plan_static(case["seq_lens"], Hkv, static_splits)
+        else:
+            if num_ctas is None:
+                num_ctas = hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"]))
+            plan = hb.hpc_decode_plan(case["seq_lens"], Hkv, num_ctas, min_chunks)
+    so, sl = hb.split_buffers(plan)
+    so.fill_(float("nan"))
+    sl.fill_(float("nan"))
+    hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
+                       case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
+                       num_pages=case["num_pages"])
+    out = torch.full_like(case["q"], float("nan"))
+    lse = torch.full(case["q"].shape[:2], float("nan"), dtype=torch.float32, device=case["q"].device)
+    hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+    torch.cuda.synchronize()
+    return dict(plan=plan, split_o=so, split_lse=sl, out=out, lse=lse)
+
+
+def tolerances(case):
+    fp8 = case["k_cache"].dtype != torch.bfloat16
+    return (FP8_MAX_ABS, None) if fp8 else (BF16_MAX_ABS, BF16_MEAN_ABS)
+
+
+def assert_close(got_o, got_lse, ref_o, ref_lse, case, what=""):
+    """Element-wise output and LSE bounds (max abs, mean abs, LSE abs)."""
+    max_abs, mean_abs = tolerances(case)
+    got_o = np.asarray(got_o, dtype=np.float64).reshape(ref_o.shape)
+    got_lse = np.asarray(got_lse, dtype=np.float64).reshape(ref_lse.shape)
+    assert np.all(np.isfinite(got_o)), f"{what}: non-finite outputs"
+    err = np.abs(got_o - ref_o)
+    assert err.max() <= max_abs, f"{what}: max abs {err.max():.3g} > {max_abs}"
+    if mean_abs is not None:
+        assert err.mean() <= mean_abs, f"{what}: mean abs {err.mean():.3g} > {mean_abs}"
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(fin, np.isfinite(got_lse)), f"{what}: -inf LSE pattern differs"
+    if fin.any():
+        lerr = np.abs(got_lse[fin] - ref_lse[fin]).max()
+        assert lerr <= LSE_ABS, f"{what}: LSE abs {lerr:.3g} > {LSE_ABS}"
+    return err
+
+
+def check_plan_exact(res, case, num_ctas=None, min_chunks=2, static_splits=None):
+    sl = case["seq_lens"].cpu().numpy()
+    Hkv = case["k_cache"].shape[2]
+    if static_splits:
+        ref = oracle.plan_static(sl, Hkv, static_splits)
+    else:
+        ref = oracle.plan(sl, Hkv, res["plan"].num_ctas, min_chunks)
+    got = res["plan"].buf.cpu().numpy()
+    assert got.shape == ref.shape and np.array_equal(got, ref), "task map differs from the oracle"
+    return ref
+
+
+def check_full(case, res, check_splits=True):
+    """Compare every output row (and every split partial) with the oracle."""
+    host = wl.to_numpy_case(case)
+    B, Hq, _ = host["q"].shape
+    ro, rl = oracle.attn_rows(host)
+    assert_close(res["out"].float().cpu().numpy(), res["lse"].cpu().numpy(), ro.reshape(B, Hq, 128),
+                 rl.reshape(B, Hq), case, "output")
+    if check_splits:
+        pb = res["plan"].buf.cpu().numpy()
+        so, sl = oracle.attn_splits(pb, host)
+        n = so.shape[0]
+        assert_close(res["split_o"][:n].cpu().numpy(), res["split_lse"][:n].cpu().numpy(), so, sl,
+                     case, "split partials")
+
+
+def check_sampled(case, res, requests, heads=None):
+    """Compare rows of the given requests (all query heads, or `heads`) with the
+    oracle run on a host copy of just those requests' pages."""
+    host = wl.to_numpy_case(case, requests=requests)
+    Hq = host["q"].shape[1]
+    heads = list(range(Hq)) if heads is None else list(heads)
+    rows = [(i, h) for i in range(len(requests)) for h in heads]
+    ro, rl = oracle.attn_rows(host, rows)
+    out = res["out"].float().cpu().numpy()
+    lse = res["lse"].cpu().numpy()
+    got_o = np.stack([out[requests[i], h] for i, h in rows])
+    got_l = np.array([lse[requests[i], h] for i, h in rows])
+    return assert_close(got_o, got_l, ro, rl, case, f"sampled rows of requests {list(requests)}")
+
+
+def check_split_invariants(case, res):
+    """At any size: combining the GPU partials in float64 with the oracle's
+    combine reproduces the GPU output, and every partial LSE is finite."""
+    pb = res["plan"].buf.cpu().numpy()
+    n = int(pb[3])
+    so = res["split_o"][:n].double().cpu().numpy()
+    sl = res["split_lse"][:n].double().cpu().numpy()
+    assert np.all(np.isfinite(so)) and np.all(np.isfinite(sl))
+    B, Hq, _ = case["q"].shape
+    o, l = oracle.combine(pb, so, sl, B, Hq, case["k_cache"].shape[2])
+    got = res["out"].float().cpu().numpy()
+    # the only difference is the float32 merge and the bf16 rounding of the output
+    assert np.all(np.abs(got - o) <= 2.0 ** -8 * np.abs(o) + 1e-5)
+    fin = np.isfinite(l)
+    assert np.abs(res["lse"].cpu().numpy()[fin] - l[fin]).max() <= 1e-4

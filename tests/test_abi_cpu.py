@@ -1,0 +1,120 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/hpc_decode.h declares, and rejects bad arguments on the host
+before any CUDA work (fake, never-dereferenced pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from load_balanced_paged_02_gb300 import _build
+from load_balanced_paged_02_gb300 import binding as hb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hpc_decode.h")
+FAKE = ctypes.c_void_p(0x10000)      # 256-byte aligned, never dereferenced
+FAKE_ODD = ctypes.c_void_p(0x10004)  # not 16-byte aligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return hb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(hpc_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for required in ("hpc_decode_plan", "hpc_decode_plan_static", "hpc_decode_attn",
+                     "hpc_decode_combine", "hpc_decode_step_host", "hpc_decode_read_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} not exported"
+    assert set(declared_functions()) == set(hb.SIGNATURES), "binding and header disagree"
+
+
+def test_plan_bytes_match_layout(L):
+    for B, H, C in [(1, 1, 1), (4, 1, 16), (64, 8, 152), (16384, 1, 5000), (7, 3, 999)]:
+        assert L.hpc_decode_plan_bytes(B, H, C) == 4 * oracle.layout(B, H, C)["total"]
+        assert L.hpc_decode_split_capacity(B, H, C) == H * B + C - 1
+    assert L.hpc_decode_plan_bytes(0, 1, 1) == 0
+    assert L.hpc_decode_plan_bytes(16385, 1, 1) == 0
+    assert L.hpc_decode_plan_bytes(1, 257, 1) == 0
+    assert L.hpc_decode_plan_bytes(1, 1, 0) == 0
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert L.hpc_status_string(code)
+    assert L.hpc_status_string(99) == b"unknown status"
+
+
+def _attn(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, dt=0, pages=16, pt=FAKE, stride=4, sl=FAKE,
+             B=2, Hq=8, Hkv=1, D=128, P=64, plan=None, so=FAKE, slse=FAKE)
+    a.update(kw)
+    return L.hpc_decode_attn(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["dt"], a["pages"], a["pt"],
+                             a["stride"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], a["plan"],
+                             a["so"], a["slse"], None)
+
+
+def test_attn_rejects_unsupported_shapes(L):
+    assert _attn(L, D=64) == 2
+    assert _attn(L, P=16) == 2
+    assert _attn(L, Hq=16, Hkv=1) == 2
+    assert _attn(L, dt=7) == 2
+
+
+def test_attn_rejects_bad_arguments(L):
+    plan = hb.PlanStruct(FAKE.value, 1 << 20, 2, 1, 4, 2, 0, 10)
+    assert _attn(L, q=None, plan=ctypes.byref(plan)) == 1
+    assert _attn(L, q=FAKE_ODD, plan=ctypes.byref(plan)) == 1
+    assert _attn(L, dt=1, plan=ctypes.byref(plan)) == 1          # e4m3 without scales
+    assert _attn(L, plan=None) == 1
+    wrong = hb.PlanStruct(FAKE.value, 1 << 20, 3, 1, 4, 2, 0, 10)  # batch mismatch
+    assert _attn(L, plan=ctypes.byref(wrong)) == 1
+    small = hb.PlanStruct(FAKE.value, 8, 2, 1, 4, 2, 0, 10)        # buffer too small
+    assert _attn(L, plan=ctypes.byref(small)) == 1
+    assert _attn(L, pages=0, plan=ctypes.byref(plan)) == 1
+
+
+def test_plan_rejects_bad_arguments(L):
+    p = hb.PlanStruct(FAKE.value, 1 << 20, 0, 0, 0, 0, 0, 0)
+    assert L.hpc_decode_plan(None, 4, 1, 16, 2, ctypes.byref(p), None) == 1
+    assert L.hpc_decode_plan(FAKE, 0, 1, 16, 2, ctypes.byref(p), None) == 1
+    assert L.hpc_decode_plan(FAKE, 4, 1, 16, -1, ctypes.byref(p), None) == 1
+    assert L.hpc_decode_plan(FAKE, 4, 1, 0, 2, ctypes.byref(p), None) == 1
+    small = hb.PlanStruct(FAKE.value, 64, 0, 0, 0, 0, 0, 0)
+    assert L.hpc_decode_plan(FAKE, 4, 1, 16, 2, ctypes.byref(small), None) == 3
+    odd = hb.PlanStruct(FAKE_ODD.value, 1 << 20, 0, 0, 0, 0, 0, 0)
+    assert L.hpc_decode_plan(FAKE, 4, 1, 16, 2, ctypes.byref(odd), None) == 1
+    assert L.hpc_decode_plan_static(FAKE, 4, 1, 0, ctypes.byref(p), None) == 1
+    assert L.hpc_decode_plan_static(FAKE, 4, 1, 16, ctypes.byref(small), None) == 3
+
+
+def test_combine_and_step_reject_bad_arguments(L):
+    plan = hb.PlanStruct(FAKE.value, 1 << 20, 2, 1, 4, 2, 0, 10)
+    assert L.hpc_decode_combine(ctypes.byref(plan), FAKE, FAKE, FAKE, None, 2, 8, 1, 64, None) == 2
+    assert L.hpc_decode_combine(ctypes.byref(plan), None, FAKE, FAKE, None, 2, 8, 1, 128, None) == 1
+    assert L.hpc_decode_combine(None, FAKE, FAKE, FAKE, None, 2, 8, 1, 128, None) == 1
+    ws = L.hpc_decode_step_workspace_bytes(2, 8, 1, 4, 4)
+    assert ws > 0 and ws % 256 == 0
+    args = [FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, None, 0, 16, 2, 8, 1, 128, 64, 4, 2, FAKE]
+    assert L.hpc_decode_step_host(*args, ws - 1, FAKE, None, None) == 3
+    assert L.hpc_decode_step_host(*args[:-1], FAKE_ODD, ws, FAKE, None, None) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(hb, "_LIB", None)
+    monkeypatch.setattr(hb._build, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(hb.HpcError):
+        hb.lib()

@@ -1,0 +1,252 @@
+"""CUDA path against the float64 oracle, through the C ABI (GPU only).
+
+Task maps must match byte for byte. Outputs: BF16 KV max abs <= 2e-2 and mean
+abs <= 2e-3; e4m3 KV max abs <= 6e-2; LSE <= 1e-3 abs. Small cases compare
+every output row and every split partial; the full-size workloads compare all
+query heads of sampled requests (the longest, the shortest and seeded others)
+plus size-independent properties of the partials.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import oracle
+from load_balanced_paged_02_gb300 import binding as hb
+from load_balanced_paged_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hb.lib()
+
+
+def case_for(lens, hkv=1, dtype="bf16", seed=0, pool=None, stride=None):
+    w = wl.Workload("t", len(lens), 8 * hkv, hkv, dtype, seed, lens=list(lens), pool_pages=pool)
+    return wl.make_case(w, device=DEV, stride=stride)
+
+
+# ------------------------------------------------------------------ planner
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_plan_bit_exact_workloads(name):
+    w = wl.WORKLOADS[name]
+    lens = torch.from_numpy(wl.draw_lengths(w).astype(np.int32)).to(DEV)
+    C = w.num_ctas or hb.default_num_ctas(hb.KV_FP8_E4M3 if w.kv_dtype == "fp8" else hb.KV_BF16)
+    plan = hb.hpc_decode_plan(lens, w.num_kv_heads, C, w.min_chunks)
+    ref = oracle.plan(lens.cpu().numpy(), w.num_kv_heads, C, w.min_chunks)
+    assert np.array_equal(plan.buf.cpu().numpy(), ref)
+    st = hb.hpc_decode_plan_static(lens, w.num_kv_heads, w.static_splits)
+    ref = oracle.plan_static(lens.cpu().numpy(), w.num_kv_heads, w.static_splits)
+    assert np.array_equal(st.buf.cpu().numpy(), ref)
+
+
+def test_plan_bit_exact_random_and_edges():
+    rng = np.random.default_rng(123)
+    cases = [([0], 1, 1, 0), ([0, 0, 0], 2, 5, 2), ([1], 1, 1, 0), ([64], 3, 7, 0),
+             ([65, 1, 0, 4096], 8, 148, 2), ([10 ** 6], 8, 152, 2), ([37, 128, 300, 1000], 1, 16, 2)]
+    for _ in range(60):
+        B = int(rng.integers(1, 60))
+        cases.append((rng.integers(0, 6000, size=B).tolist(), int(rng.integers(1, 9)),
+                      int(rng.integers(1, 400)), int(rng.integers(0, 6))))
+    # more than 1024 requests / pairs: several scan tiles in the planner
+    cases.append((rng.integers(0, 3000, size=3000).tolist(), 8, 304, 2))
+    cases.append((rng.integers(0, 300, size=HB_MAX_B).tolist(), 1, 1000, 1))
+    for lens, hkv, C, m in cases:
+        sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+        plan = hb.hpc_decode_plan(sl, hkv, C, m)
+        ref = oracle.plan(np.array(lens, dtype=np.int32), hkv, C, m)
+        assert np.array_equal(plan.buf.cpu().numpy(), ref), (len(lens), hkv, C, m)
+        S = int(rng.integers(1, 20))
+        if hkv * len(lens) * S <= 1 << 20:
+            st = hb.hpc_decode_plan_static(sl, hkv, S)
+            assert np.array_equal(st.buf.cpu().numpy(), oracle.plan_static(np.array(lens, np.int32), hkv, S))
+
+
+HB_MAX_B = 16384
+
+
+def test_plan_negative_length_error_bit():
+    sl = torch.tensor([-3, 100, 5], dtype=torch.int32, device=DEV)
+    plan = hb.hpc_decode_plan(sl, 2, 4, 1)
+    ref = oracle.plan(sl.cpu().numpy(), 2, 4, 1)
+    assert np.array_equal(plan.buf.cpu().numpy(), ref)
+    assert hb.hpc_decode_read_error(plan) & 1
+
+
+# ------------------------------------------------------------------ attention, small (every row)
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_tiny_workload_full(dtype):
+    w = wl.WORKLOADS["tiny"]
+    case = case_for(w.lens, 1, dtype, seed=0, pool=64)
+    res = _gpu.run(case, num_ctas=16, min_chunks=2)
+    _gpu.check_plan_exact(res, case, min_chunks=2)
+    _gpu.check_full(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("C,m", [(1, 0), (7, 1), (40, 2), (152, 2), (300, 4)])
+def test_ragged_lengths_full(dtype, C, m):
+    lens = [1, 63, 64, 65, 127, 200, 0, 333, 1000, 4097, 2, 640]
+    case = case_for(lens, 2, dtype, seed=C + m)
+    res = _gpu.run(case, num_ctas=C, min_chunks=m)
+    _gpu.check_plan_exact(res, case, min_chunks=m)
+    _gpu.check_full(case, res)
+    out = res["out"].float().cpu().numpy()
+    assert np.all(out[6] == 0) and np.all(np.isneginf(res["lse"][6].cpu().numpy()))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_static_split_full(dtype):
+    lens = [37, 128, 300, 1000, 5000, 0, 64]
+    case = case_for(lens, 2, dtype, seed=5)
+    res = _gpu.run(case, static_splits=4)
+    _gpu.check_plan_exact(res, case, static_splits=4)
+    _gpu.check_full(case, res)
+
+
+def test_all_lengths_zero():
+    case = case_for([0, 0, 0], 1, seed=6, pool=4)
+    res = _gpu.run(case, num_ctas=8)
+    assert np.all(res["out"].float().cpu().numpy() == 0)
+    assert np.all(np.isneginf(res["lse"].cpu().numpy()))
+
+
+def test_plan_reused_across_layers():
+    """One task map per step serves every layer (different caches, same lengths)."""
+    lens = [100, 3000, 64, 777]
+    a = case_for(lens, 2, seed=7)
+    b = case_for(lens, 2, seed=8)
+    b["page_table"], b["seq_lens"] = a["page_table"], a["seq_lens"]
+    res_a = _gpu.run(a, num_ctas=20)
+    res_b = _gpu.run(b, plan=res_a["plan"])
+    _gpu.check_full(a, res_a)
+    _gpu.check_full(b, res_b)
+
+
+def test_peaky_scores():
+    """Q scaled x8 with a planted key equal to q: the softmax is far from flat,
+    so max tracking and rescaling matter. Checked also by relative norm."""
+    lens = [3000, 130, 64 * 9 + 5]
+    case = case_for(lens, 1, seed=9)
+    q = case["q"].float() * 8.0
+    case["q"] = q.to(torch.bfloat16)
+    pt = case["page_table"].cpu().numpy()
+    for b, L in enumerate(lens):
+        t = (b * 977) % L
+        case["k_cache"][pt[b, t // 64], t % 64, 0] = case["q"][b, 0] / 8.0
+    res = _gpu.run(case, num_ctas=9)
+    _gpu.check_full(case, res)
+    host = wl.to_numpy_case(case)
+    ro, _ = oracle.attn_rows(host)
+    got = res["out"].float().cpu().numpy().reshape(-1, 128)
+    rel = np.linalg.norm(got - ro, axis=1) / np.maximum(np.linalg.norm(ro, axis=1), 1e-30)
+    assert rel.max() < 1e-2
+
+
+def test_invalid_page_id_sets_error_and_skips():
+    lens = [200, 300]
+    case = case_for(lens, 1, seed=10)
+    bad = case["page_table"].clone()
+    bad[1, 2] = case["num_pages"] + 5
+    case_bad = dict(case, page_table=bad)
+    res = _gpu.run(case_bad, num_ctas=4)
+    assert hb.hpc_decode_read_error(res["plan"]) & 4
+    # request 0 is untouched by the bad page of request 1
+    host = wl.to_numpy_case(case)
+    ro, rl = oracle.attn_rows(host, [(0, h) for h in range(8)])
+    _gpu.assert_close(res["out"][0].float().cpu().numpy(), res["lse"][0].cpu().numpy(), ro, rl, case)
+
+
+def test_garbage_beyond_live_length_is_ignored():
+    """NaN bits in the unused slots of a request's last page must not leak."""
+    lens = [70, 129]
+    case = case_for(lens, 1, seed=11)
+    pt = case["page_table"].cpu().numpy()
+    for b, L in enumerate(lens):
+        last = pt[b, (L - 1) // 64]
+        case["k_cache"][last, L % 64:] = float("nan")
+        case["v_cache"][last, L % 64:] = float("nan")
+    res = _gpu.run(case, num_ctas=3)
+    _gpu.check_full(case, res, check_splits=False)
+
+
+def test_garbage_beyond_live_length_is_ignored_fp8():
+    lens = [70, 129]
+    case = case_for(lens, 1, "fp8", seed=12)
+    pt = case["page_table"].cpu().numpy()
+    for b, L in enumerate(lens):
+        last = pt[b, (L - 1) // 64]
+        case["k_cache"].view(torch.uint8)[last, L % 64:] = 0x7F
+        case["v_cache"].view(torch.uint8)[last, L % 64:] = 0x7F
+        case["k_scale"][last, :, L % 64:] = float("inf")
+        case["v_scale"][last, :, L % 64:] = float("nan")
+    res = _gpu.run(case, num_ctas=3)
+    _gpu.check_full(case, res, check_splits=False)
+
+
+def test_step_host_matches_device_path():
+    lens = [500, 64, 1300, 7]
+    case = case_for(lens, 2, seed=13)
+    res = _gpu.run(case, num_ctas=10)
+    B, Hq, D = case["q"].shape
+    ws_bytes = hb.step_workspace_bytes(B, Hq, 2, case["page_table"].shape[1], 10)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    h_q = case["q"].cpu().pin_memory()
+    h_sl = case["seq_lens"].cpu().pin_memory()
+    h_pt = case["page_table"].cpu().pin_memory()
+    h_out = torch.empty_like(h_q).pin_memory()
+    h_lse = torch.empty((B, Hq), dtype=torch.float32).pin_memory()
+    hb.hpc_decode_step_host(h_q, h_sl, h_pt, case["k_cache"], case["v_cache"], ws, h_out, h_lse,
+                            num_ctas=10, num_pages=case["num_pages"])
+    torch.cuda.synchronize()
+    assert torch.equal(h_out, res["out"].cpu())
+    assert torch.equal(h_lse, res["lse"].cpu())
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+def _sample_requests(lens, k, seed):
+    lens = np.asarray(lens)
+    order = np.argsort(lens)
+    pick = {int(order[-1]), int(order[0])}
+    rng = np.random.default_rng(seed)
+    while len(pick) < min(k, len(lens)):
+        pick.add(int(rng.integers(0, len(lens))))
+    return sorted(pick)
+
+
+def test_uniform_workload_full():
+    w = wl.WORKLOADS["uniform"]
+    case = wl.make_case(w, device=DEV)
+    res = _gpu.run(case, num_ctas=w.num_ctas, min_chunks=w.min_chunks)
+    _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
+    _gpu.check_full(case, res, check_splits=False)
+    _gpu.check_split_invariants(case, res)
+
+
+@pytest.mark.parametrize("name", ["mixed", "skew", "fp8"])
+def test_full_size_workload_sampled(name):
+    w = wl.WORKLOADS[name]
+    case = wl.make_case(w, device=DEV)
+    C = hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"]))
+    res = _gpu.run(case, num_ctas=C, min_chunks=w.min_chunks)
+    _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
+    lens = case["seq_lens"].cpu().numpy()
+    _gpu.check_sampled(case, res, _sample_requests(lens, 5, seed=w.seed))
+    _gpu.check_split_invariants(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
+    # the static split-KV schedule of the same kernel gives the same answer
+    st = _gpu.run(case, static_splits=w.static_splits)
+    _gpu.check_plan_exact(st, case, static_splits=w.static_splits)
+    _gpu.check_sampled(case, st, _sample_requests(lens, 3, seed=w.seed + 1))
+    diff = (st["out"].float() - res["out"].float()).abs().max().item()
+    assert diff <= 2 * _gpu.tolerances(case)[0]
