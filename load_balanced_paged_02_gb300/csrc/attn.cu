@@ -69,7 +69,8 @@ struct Layout {
     static constexpr size_t kScratch = kQ + 2 * kQSlotBytes;
     static constexpr size_t kML = kScratch + (size_t)kNCW * kGroup * kScratchStride * 4;
     static constexpr size_t kMeta = kML + (size_t)kNCW * kGroup * 8;
-    static constexpr size_t kBars = (kMeta + STAGES * 4 + 7) / 8 * 8;
+    static constexpr size_t kSink = kMeta + STAGES * 4;  // one word per consumer warp
+    static constexpr size_t kBars = (kSink + kNCW * 4 + 7) / 8 * 8;
     static constexpr int kNumBars = 2 * STAGES + 5;
     static constexpr size_t kFlag = kBars + kNumBars * 8;
     static constexpr size_t kTotal = kFlag + 16;
@@ -431,6 +432,7 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
     const int g = lane >> 2, c = lane & 3;
     float* scratch = reinterpret_cast<float*>(smem + LY::kScratch);
     float2* ml = reinterpret_cast<float2*>(smem + LY::kML);
+    volatile uint32_t* q_sink = reinterpret_cast<volatile uint32_t*>(smem + LY::kSink);
     uint32_t seq = 0, mphase = 0;
     int qd = 0;
     for (int slot = list0;; ++slot) {
@@ -445,8 +447,19 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
         const int qs = qd & 1;
         if (!wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
         load_q_frags<FP8>(smem_u32(qbuf + qs * kQSlotBytes), lane, qf);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&qempty[qs]);
+        {
+            // The slot may be refilled by TMA as soon as it is released, so the
+            // release must wait until the fragment loads have returned: fold
+            // every fragment word into a value that a store consumes first.
+            uint32_t x = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x ^= qf[i][0] ^ qf[i][1];
+            __syncwarp();
+            if (lane == 0) {
+                q_sink[warp] = x;
+                mbar_arrive(&qempty[qs]);
+            }
+        }
         ++qd;
 
         {

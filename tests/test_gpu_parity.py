@@ -105,6 +105,20 @@ def test_ragged_lengths_full(dtype, C, m):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("seed", [1, 2, 3, 4, 5])
+def test_single_cta_many_descriptors(dtype, seed):
+    """One or two CTAs drain every descriptor: the producer runs far ahead of
+    the consumers, and short descriptors follow long ones, so the Q slots and
+    the stage ring turn over while the previous contents are still in use."""
+    lens = [1, 63, 64, 65, 127, 200, 0, 333, 1000, 4097, 2, 640, 1, 1, 70, 3]
+    case = case_for(lens, 2, dtype, seed=seed)
+    for C in (1, 2):
+        res = _gpu.run(case, num_ctas=C, min_chunks=0)
+        _gpu.check_plan_exact(res, case, min_chunks=0)
+        _gpu.check_full(case, res)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_static_split_full(dtype):
     lens = [37, 128, 300, 1000, 5000, 0, 64]
     case = case_for(lens, 2, dtype, seed=5)
