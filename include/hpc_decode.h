@@ -226,6 +226,37 @@ hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens,
                                 void* d_workspace, size_t workspace_bytes, void* h_out,
                                 float* h_out_lse, void* stream);
 
+/*
+ * One decode step (plan -> attention -> combine) that allocates nothing. The
+ * pages describe no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc where they run the step, for example an engine
+ * whose memory pool takes all device memory at start-up and forbids
+ * allocations outside it, or plugin code that is handed only input and output
+ * pointers and has no allocator to reach. The caller passes the inputs (as
+ * for hpc_decode_attn) and the outputs (as for hpc_decode_combine); the task
+ * map and the split buffers live in one fixed 8 MiB device array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.
+ *   - Limit: the task map for (batch, num_kv_heads, num_ctas) plus
+ *     hpc_decode_split_capacity rows of 4128 bytes (each part rounded up to
+ *     256 bytes) must fit in 8 MiB, about 2000 split rows; larger sizes return
+ *     HPC_ERR_WORKSPACE_TOO_SMALL before any work is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the array: calls whose work overlaps on
+ *     the GPU (other streams, no ordering between them) race on it. Nothing in
+ *     the array needs to start at zero; each call rewrites what it reads.
+ *   - The device error word lives in that array and is not reported.
+ * Errors: as hpc_decode_plan, hpc_decode_attn and hpc_decode_combine.
+ */
+hpc_status hpc_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale, int kv_dtype,
+                              int num_pages, const int32_t* page_table, int page_table_stride,
+                              const int32_t* seq_lens, int batch, int num_q_heads,
+                              int num_kv_heads, int head_dim, int page_size, int num_ctas,
+                              int min_chunks_per_cta, void* out, float* out_lse, void* stream);
+
 /* Synchronises the device, then reads the task map's error word into
  * *device_error_word. Returns HPC_ERR_DEVICE_CHECK when it is non-zero.
  * For tests and diagnostics, not for the hot loop. */

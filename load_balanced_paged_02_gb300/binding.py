@@ -55,6 +55,8 @@ SIGNATURES = {
     "hpc_decode_step_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "hpc_decode_step_host": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                   _i, _i, _vp, _sz, _vp, _vp, _vp]),
+    "hpc_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                _i, _vp, _vp, _vp]),
     "hpc_decode_read_error": (_i, [_P, ctypes.POINTER(_i)]),
     "hpc_status_string": (ctypes.c_char_p, [_i]),
 }
