@@ -40,7 +40,7 @@ UNIT = "GB/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed")
@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-static", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches only")
     return ap.parse_args()
 
 
@@ -94,7 +95,7 @@ def step_bytes(lens, w, n_splits):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -102,7 +103,11 @@ class ClockSampler:
         self.index = index
         self.proc = None
 
+    def mark(self, which):
+        setattr(self, which, time.time())
+
     def __enter__(self):
+        self.t_begin = self.t_end = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
@@ -126,24 +131,33 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
+        """Median SM clock and active throttle reasons over the samples taken
+        between mark('t_begin') and mark('t_end') (all samples if too few)."""
+        import datetime
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
         for line in getattr(self, "lines", []):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                parsed.append((ts, float(f[2]), float(f[3]), f[6:10]))
             except ValueError:
                 continue
-            for name, v in zip(names, f[5:9]):
+        inside = [p for p in parsed if self.t_begin and self.t_end and self.t_begin <= p[0] <= self.t_end]
+        use = inside if len(inside) >= 3 else parsed
+        for _, cur, mxv, flags in use:
+            sm.append(cur)
+            mx = mxv
+            for name, v in zip(names, flags):
                 if v.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "timed region" if use is inside else "whole run"}
 
 
 def measured_peaks():
@@ -220,7 +234,7 @@ def run_reference(args):
     import oracle
     from load_balanced_paged_02_gb300 import workloads as wl
     oracle.build()
-    w = wl.WORKLOADS[args.workload]
+    w = wl.by_name(args.workload)
     case = wl.make_case(w, device="cpu")
     lens = case["seq_lens"].numpy()
     byt = step_bytes(lens, w, 0)
@@ -256,7 +270,7 @@ def run_ours(args):
     _build.build()
     hb.lib()
 
-    w = rank_workload(wl.WORKLOADS[args.workload], rank)
+    w = rank_workload(wl.by_name(args.workload), rank)
     case = wl.make_case(w, device=dev)
     kvd = hb.kv_dtype_of(case["k_cache"])
     C = hb.default_num_ctas(kvd)
@@ -297,20 +311,46 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
 
+    # The whole step captured once as a CUDA graph (how a serving engine
+    # replays decode steps); replays re-run plan, attention and combine.
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
+    t_start, t_stop, g_start, g_stop = (torch.cuda.Event(enable_timing=True) for _ in range(4))
     with ClockSampler(local) as clk:
+        clk.mark("t_begin")
+        # eager launches, with events around every kernel (per-kernel times)
         t_start.record(stream)
         for k in range(args.steps):
             step(evs[k])
         t_stop.record(stream)
+        # graph replays of the same step (the step time reported as the value)
+        if graph is not None:
+            g_start.record(stream)
+            for k in range(args.steps):
+                graph.replay()
+            g_stop.record(stream)
         torch.cuda.synchronize()
-    total_ms = t_start.elapsed_time(t_stop)
+        clk.mark("t_end")
+    eager_ms = t_start.elapsed_time(t_stop) / args.steps
+    graph_ms = g_start.elapsed_time(g_stop) / args.steps if graph is not None else None
     plan_us = 1e3 * float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
     attn_us = 1e3 * float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     comb_us = 1e3 * float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
-    ms_step = max_over_ranks(total_ms / args.steps, dist, dev)
+    ms_step = max_over_ranks(graph_ms if graph_ms is not None else eager_ms, dist, dev)
     if dist is not None:
         dist.barrier()
 
@@ -330,13 +370,15 @@ def run_ours(args):
             "config": {"workload": w.name, "detail": w.note, "num_ctas": C, "min_chunks": w.min_chunks,
                        "live_tokens": int(lens.sum()), "splits": n_splits,
                        "bytes_per_step": byt, "l2": "inputs larger than L2 (no flush)",
+                       "step": "cuda graph replay" if graph is not None else "eager launches",
                        "us_per_step": {"plan": plan_us, "attn": attn_us, "combine": comb_us,
-                                       "total": ms_step * 1e3}},
+                                       "eager_total": eager_ms * 1e3,
+                                       "graph_total": graph_ms * 1e3 if graph_ms is not None else None}},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
                          "traffic": recorded_traffic(w.name, "bf16" if kvd == hb.KV_BF16 else "e4m3"),
                          "kernel": "decode_attn_kernel", "algorithmic_bytes_per_launch": byt["attn"]},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (6 if graph is not None else 3) * args.steps,
             "clocks": clocks,
         }
 
@@ -355,10 +397,18 @@ def run_ours(args):
         for _ in range(3):
             sstep()
         torch.cuda.synchronize()
+        run = sstep
+        if graph is not None:
+            sgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(sgraph):
+                sstep()
+            sgraph.replay()
+            run = sgraph.replay
+        torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(n_static):
-            sstep()
+            run()
         b.record(stream)
         torch.cuda.synchronize()
         sms = a.elapsed_time(b) / n_static

@@ -33,6 +33,7 @@
 // flight, and the CTA returns.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "hpc_internal.cuh"
@@ -170,12 +171,16 @@ __device__ __forceinline__ void softmax_step(float (&s)[4], float (&m)[2], float
     p[3] = fast_exp2(s[3] - mu1);
     l[0] = l[0] * al0 + p[0] + p[2];
     l[1] = l[1] * al1 + p[1] + p[3];
+    // Once a long sequence's running max settles, alpha is 1 for every lane;
+    // skip the rescale of O then (warp-uniform branch).
+    if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        o[i][0] *= al0;
-        o[i][1] *= al1;
-        o[i][2] *= al0;
-        o[i][3] *= al1;
+        for (int i = 0; i < 8; ++i) {
+            o[i][0] *= al0;
+            o[i][1] *= al1;
+            o[i][2] *= al0;
+            o[i][3] *= al1;
+        }
     }
 }
 
@@ -255,10 +260,8 @@ __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, 
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t a[4];
-            a[0] = e4m3x2_to_f16x2(w0[ks]);
-            a[1] = e4m3x2_to_f16x2(w1[ks]);
-            a[2] = e4m3x2_to_f16x2(w0[ks] >> 16);
-            a[3] = e4m3x2_to_f16x2(w1[ks] >> 16);
+            e4m3x4_to_f16x2x2(w0[ks], a[0], a[2]);
+            e4m3x4_to_f16x2x2(w1[ks], a[1], a[3]);
             if (ks & 1)
                 mma_f16(acc1, a, qf[ks][0], qf[ks][1]);
             else
@@ -293,10 +296,8 @@ __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, 
             const uint32_t u = prmt(x0[i >> 1], x1[i >> 1], sel);
             const uint32_t v = prmt(x2[i >> 1], x3[i >> 1], sel);
             uint32_t a[4];
-            a[0] = e4m3x2_to_f16x2(u);
-            a[1] = e4m3x2_to_f16x2(u >> 16);
-            a[2] = e4m3x2_to_f16x2(v);
-            a[3] = e4m3x2_to_f16x2(v >> 16);
+            e4m3x4_to_f16x2x2(u, a[0], a[1]);
+            e4m3x4_to_f16x2x2(v, a[2], a[3]);
             mma_f16(o[i], a, pb0, pb1);
         }
     }
@@ -589,8 +590,18 @@ template <bool FP8, int STAGES, int NG>
 struct Inst {
     using LY = Layout<FP8, STAGES, NG>;
     static const void* fn() { return reinterpret_cast<const void*>(&decode_attn_kernel<FP8, STAGES, NG>); }
+    // The shared-memory opt-in is set once per device (the launch path then
+    // makes no extra runtime calls, which keeps it cheap and capturable).
     static cudaError_t prepare() {
-        return cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::kAlloc);
+        static std::atomic<unsigned long long> done{0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const unsigned long long bit = 1ull << (dev & 63);
+        if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+        e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LY::kAlloc);
+        if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
     }
     static cudaError_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int grid,
                               cudaStream_t s) {

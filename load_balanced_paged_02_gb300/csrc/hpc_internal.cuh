@@ -237,11 +237,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Two e4m3 codes (low byte = first element) -> f16x2 (low half = first), exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu),
-                                               __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Four e4m3 codes (bytes 0..3 of w) -> two f16x2, exact (every e4m3 value is
+// an f16 value): lo = {b0, b1}, hi = {b2, b3}, lower byte to lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

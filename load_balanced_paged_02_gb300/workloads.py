@@ -88,6 +88,18 @@ def table3_workload(mix: str, num_q_heads: int = 8, num_kv_heads: int = 1, seed:
                     "fp8", seed, lens=list(lens), note=f"decode-latency table mix {mix}, e4m3 KV")
 
 
+def by_name(name: str) -> Workload:
+    """A workload by name: one of WORKLOADS, or "t3:<mix>" / "t3:<mix>:<Hq>/<Hkv>"
+    for a length mix of the decode-latency table (default 8 query / 1 KV head)."""
+    if name in WORKLOADS:
+        return WORKLOADS[name]
+    parts = name.split(":")
+    if parts[0] == "t3" and len(parts) in (2, 3) and parts[1] in TABLE3_MIXES:
+        hq, hkv = (8, 1) if len(parts) == 2 else (int(x) for x in parts[2].split("/"))
+        return table3_workload(parts[1], hq, hkv)
+    raise KeyError(f"unknown workload {name!r}")
+
+
 def draw_lengths(w: Workload) -> np.ndarray:
     if w.lens is not None:
         return np.asarray(w.lens, dtype=np.int64)
