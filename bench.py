@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default="mixed")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="total oracle time of the --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-static", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -193,34 +195,50 @@ def recorded_traffic(workload, dtype):
 
 # ---------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(case, w, seconds):
-    """Time the float64 oracle on a bounded sample of requests and scale the
-    rate to the whole batch. Returns (seconds per full step, cores, sample text)."""
+def oracle_sample(case, w, seconds, seed=99):
+    """Time the float64 oracle on a bounded sample of the workload and scale its
+    rate to the whole batch. Rows (request, query head) are taken request by
+    request in a seeded order (cycling over the batch if time allows) until
+    about `seconds` of oracle time is spent. Returns (seconds per full step,
+    threads used, text describing the sample)."""
     import oracle
     from load_balanced_paged_02_gb300 import workloads as wl
-    lens = case["seq_lens"].cpu().numpy().astype(np.int64)
-    total_tok = float(np.maximum(lens, 0).sum())
-    order = np.random.default_rng(99).permutation(len(lens))
-    # grow the sample until it takes about `seconds` of oracle time
-    t_used, tok_done, reqs = 0.0, 0.0, []
-    i = 0
-    per_tok = None
-    while i < len(order) and t_used < seconds:
-        b = int(order[i])
-        i += 1
-        if per_tok is not None and t_used + per_tok * lens[b] > 1.5 * seconds and reqs:
-            continue
-        host = wl.to_numpy_case(case, requests=[b])
+    lens = np.maximum(case["seq_lens"].cpu().numpy().astype(np.int64), 0)
+    total = float(lens.sum()) * w.num_q_heads
+    order = [int(b) for b in np.random.default_rng(seed).permutation(len(lens)) if lens[b] > 0]
+    Hq = w.num_q_heads
+    spent, done, rows_done, k = 0.0, 0.0, 0, 0
+    hosts = {}
+    if total <= 4e6:
+        # a small batch: whole-batch oracle calls, repeated within the budget
+        host = wl.to_numpy_case(case)
+        while spent < seconds or done == 0:
+            t0 = time.perf_counter()
+            oracle.attn_rows(host)
+            spent += time.perf_counter() - t0
+            done += total
+            rows_done += len(lens) * Hq
+        order = []
+    while spent < seconds and order:
+        b = order[k % len(order)]
+        k += 1
+        if b not in hosts:
+            hosts[b] = wl.to_numpy_case(case, requests=[b])
+        # whole request if it fits the remaining budget, else a prefix of its heads
+        per_row = spent / done if done else None
+        nh = Hq
+        if per_row is not None:
+            nh = int(max(1, min(Hq, (seconds - spent) / max(per_row * lens[b], 1e-12))))
+        rows = [(0, h) for h in range(nh)]
         t0 = time.perf_counter()
-        oracle.attn_rows(host)
-        dt = time.perf_counter() - t0
-        t_used += dt
-        tok_done += lens[b]
-        reqs.append(b)
-        per_tok = t_used / max(tok_done, 1.0)
-    full = per_tok * total_tok
-    text = (f"{len(reqs)} of {len(lens)} requests ({int(tok_done)} of {int(total_tok)} tokens, "
-            f"all {w.num_q_heads} query heads), {t_used:.1f} s of oracle time, scaled by token count")
+        oracle.attn_rows(hosts[b], rows)
+        spent += time.perf_counter() - t0
+        done += float(lens[b]) * nh
+        rows_done += nh
+    full = spent * total / max(done, 1.0)
+    text = (f"{rows_done} (request, query head) rows covering {int(done)} token-head pairs "
+            f"({done / total:.2f} x the batch's {int(total)}), {spent:.1f} s of oracle time, "
+            f"rate scaled to one whole batch")
     return full, oracle.num_threads(), text
 
 
@@ -238,10 +256,12 @@ def run_reference(args):
     case = wl.make_case(w, device="cpu")
     lens = case["seq_lens"].numpy()
     byt = step_bytes(lens, w, 0)
+    # every step is a bounded sample; the whole run stays within --ref-seconds
+    per_step = max(0.02, args.ref_seconds / max(args.steps + args.warmup, 1))
     times = []
     sample = None
     for k in range(args.warmup + args.steps):
-        full, cores, sample = oracle_sample(case, w, max(1.0, args.cpu_seconds / max(args.steps, 1)))
+        full, cores, sample = oracle_sample(case, w, per_step, seed=99 + k)
         if k >= args.warmup:
             times.append(full)
     t = float(np.mean(times))

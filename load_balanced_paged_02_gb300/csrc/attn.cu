@@ -65,6 +65,11 @@ struct KvCfg<true> {
 
 template <bool FP8, int STAGES, int NG>
 struct Layout {
+    // Chunk k goes to group k % NG and to stage k % STAGES. With STAGES a
+    // multiple of NG every stage always belongs to the same group, so a group
+    // never waits on a stage lap that another group has not finished (which
+    // would alias the mbarrier phase parity).
+    static_assert(STAGES % NG == 0, "stage ring must be a multiple of the consumer groups");
     static constexpr int kNCW = NG * 4;
     static constexpr size_t kQ = (size_t)STAGES * KvCfg<FP8>::kStageBytes;
     static constexpr size_t kScratch = kQ + 2 * kQSlotBytes;
@@ -339,6 +344,10 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // Everything above overlaps the planner's tail; the task map, lengths and
+    // Q may come from earlier kernels, so wait for them here.
+    grid_dependency_wait();
+    grid_launch_dependents();
     __syncthreads();
 
     const int list0 = p.cta_off[blockIdx.x];
@@ -394,11 +403,13 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
                                 uint8_t* sbuf = smem + (size_t)st * Cfg::kStageBytes;
                                 const int tok = page * kChunk;
                                 if constexpr (FP8) {
-                                    tma_load_3d(sbuf, &tm_k, &full[st], 0, h, tok, pol);
-                                    tma_load_3d(sbuf + 8192, &tm_v, &full[st], 0, h, tok, pol);
+                                    // the small scale rows first, so that they are not the
+                                    // last bytes of the stage to land
                                     const long long so = ((long long)page * p.num_kv_heads + h) * kChunk;
                                     bulk_load(sbuf + 16384, p.k_scale + so, 256, &full[st], pol);
                                     bulk_load(sbuf + 16640, p.v_scale + so, 256, &full[st], pol);
+                                    tma_load_3d(sbuf, &tm_k, &full[st], 0, h, tok, pol);
+                                    tma_load_3d(sbuf + 8192, &tm_v, &full[st], 0, h, tok, pol);
                                 } else {
                                     tma_load_3d(sbuf, &tm_k, &full[st], 0, h, tok, pol);
                                     tma_load_3d(sbuf + 8192, &tm_k, &full[st], 64, h, tok, pol);
@@ -607,8 +618,8 @@ struct Inst {
                               cudaStream_t s) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        decode_attn_kernel<FP8, STAGES, NG><<<grid, LY::kThreads, LY::kAlloc, s>>>(mk, mv, p);
-        return cudaGetLastError();
+        return launch_pdl(decode_attn_kernel<FP8, STAGES, NG>, dim3(grid), dim3(LY::kThreads), LY::kAlloc, s,
+                          mk, mv, p);
     }
     static int ctas_per_sm() {
         if (prepare() != cudaSuccess) return 0;
@@ -620,9 +631,12 @@ struct Inst {
     }
 };
 
-// Persistent (load-balanced) instances: deep rings, one CTA per SM.
-using BalancedBf16 = Inst<false, 6, 1>;
-using BalancedFp8 = Inst<true, 10, 2>;
+// Persistent (load-balanced) instances, one CTA per SM. Two consumer groups
+// work on alternate chunks; measured on GB300 (mixed-length batches) these
+// ring depths were the best that fit in shared memory: bf16 4 x 32 KB
+// stages, e4m3 8 x 17 KB stages.
+using BalancedBf16 = Inst<false, 4, 2>;
+using BalancedFp8 = Inst<true, 8, 2>;
 // Static split-KV instances: one descriptor per CTA, shallow rings so that
 // several CTAs share an SM, as a non-persistent split-KV grid would.
 using StaticBf16 = Inst<false, 2, 1>;

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     __shared__ int s_err;
     const int tid = threadIdx.x;
     if (tid == 0) s_err = 0;
+    grid_dependency_wait();   // seq_lens may come from the previous kernel
+    grid_launch_dependents();
     __syncthreads();
 
     const PlanLayout L = plan_layout(B, Hkv, C);
@@ -195,6 +197,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     __shared__ int s_err;
     const int tid = threadIdx.x;
     if (tid == 0) s_err = 0;
+    grid_dependency_wait();   // seq_lens may come from the previous kernel
+    grid_launch_dependents();
     __syncthreads();
 
     const long long C = (long long)Hkv * B * S;
@@ -267,8 +271,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int Hkv, int C, int m, i
     const size_t smem = sizeof(int32_t) * ((size_t)B + 1);
     cudaError_t e = set_smem((const void*)plan_balanced_kernel, smem);
     if (e != cudaSuccess) return e;
-    plan_balanced_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, B, Hkv, C, m, buf);
-    return cudaGetLastError();
+    return launch_pdl(plan_balanced_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, B, Hkv, C, m, buf);
 }
 
 cudaError_t launch_plan_static(const int32_t* seq_lens, int B, int Hkv, int S, int32_t* buf,
@@ -276,8 +279,7 @@ cudaError_t launch_plan_static(const int32_t* seq_lens, int B, int Hkv, int S, i
     const size_t smem = sizeof(int32_t) * ((size_t)B + 1);
     cudaError_t e = set_smem((const void*)plan_static_kernel, smem);
     if (e != cudaSuccess) return e;
-    plan_static_kernel<<<1, kPlanThreads, smem, s>>>(seq_lens, B, Hkv, S, buf);
-    return cudaGetLastError();
+    return launch_pdl(plan_static_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, B, Hkv, S, buf);
 }
 
 }  // namespace hpc
