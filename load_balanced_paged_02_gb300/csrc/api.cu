@@ -132,6 +132,7 @@ hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cac
     if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) return HPC_ERR_INVALID_ARG;
     if (num_pages < 1 || (long long)num_pages * kChunk > 2147483647LL || page_table_stride < 1)
         return HPC_ERR_INVALID_ARG;
+    if (fp8 && (long long)num_pages * num_kv_heads > 2147483647LL) return HPC_ERR_INVALID_ARG;
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     AttnArgs a;
     a.q = q;

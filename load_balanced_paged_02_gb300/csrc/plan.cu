@@ -138,16 +138,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     const long long used = T ? (T + bucket - 1) / bucket : 0;
     const long long P = (long long)Hkv * B;
 
+    // Chunk indices stay below T <= INT32_MAX (checked in chunk_prefix), so the
+    // per-pair divisions run in 32 bits; products that can pass 2^31 stay 64-bit.
+    const unsigned ubucket = (unsigned)bucket;
+    const unsigned uB = (unsigned)B;
+
     // split count of every (kv head, request) pair, then its first split index
     long long running = 0;
     for (long long base = 0; base < P; base += kPlanThreads) {
         const long long p = base + tid;
         long long ns = 0;
         if (p < P) {
-            const int h = (int)(p / B), b = (int)(p % B);
-            const long long nb = pre[b + 1] - pre[b];
-            const long long g0 = (long long)h * N + pre[b];
-            ns = nb ? (g0 + nb - 1) / bucket - g0 / bucket + 1 : 0;
+            const unsigned up = (unsigned)p;
+            const unsigned h = up / uB, b = up - h * uB;
+            const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
+            const unsigned g0 = h * (unsigned)N + (unsigned)pre[b];
+            ns = nb ? (long long)((g0 + nb - 1) / ubucket - g0 / ubucket + 1) : 0;
         }
         long long tot;
         long long ex = block_exclusive_scan(ns, &tot, warp_sums);
@@ -162,11 +168,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 
     // descriptors, and the first task row of every used CTA
     for (long long p = tid; p < P; p += kPlanThreads) {
-        const int h = (int)(p / B), b = (int)(p % B);
+        const unsigned up = (unsigned)p;
+        const int h = (int)(up / uB), b = (int)(up - (unsigned)h * uB);
         const long long nb = pre[b + 1] - pre[b];
         if (!nb) continue;
         const long long g0 = (long long)h * N + pre[b];
-        const long long first = g0 / bucket;
+        const long long first = (unsigned)g0 / ubucket;
         const int ns = nsplit[p];
         const long long s0 = split0[p];
         for (int k = 0; k < ns; ++k) {
@@ -217,10 +224,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
         const long long p = base + tid;
         long long ns = 0;
         if (p < P) {
-            const int b = (int)(p % B);
-            const long long nb = pre[b + 1] - pre[b];
-            const long long q = (nb + S - 1) / S;
-            ns = q ? (nb + q - 1) / q : 0;
+            const unsigned b = (unsigned)p % (unsigned)B;
+            const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
+            const unsigned q = (nb + (unsigned)S - 1) / (unsigned)S;
+            ns = q ? (long long)((nb + q - 1) / q) : 0;
         }
         long long tot;
         long long ex = block_exclusive_scan(ns, &tot, warp_sums);
@@ -233,12 +240,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     const long long total = running;
     __syncthreads();
 
+    const unsigned uS = (unsigned)S, uB = (unsigned)B;
     for (long long j = tid; j < C; j += kPlanThreads) {
-        const long long p = j / S;
-        const int s = (int)(j % S);
-        const int h = (int)(p / B), b = (int)(p % B);
+        const unsigned uj = (unsigned)j;  // C <= HPC_MAX_CTAS < 2^31
+        const unsigned up = uj / uS;
+        const int s = (int)(uj - up * uS);
+        const int h = (int)(up / uB), b = (int)(up - (unsigned)h * uB);
+        const long long p = up;
         const long long nb = pre[b + 1] - pre[b];
-        const long long q = (nb + S - 1) / S;
+        const long long q = ((unsigned)nb + uS - 1) / uS;
         const int ns = nsplit[p];
         const long long s0 = split0[p];
         const long long off = s0 + (s < ns ? s : ns) + j;

@@ -226,6 +226,73 @@ def test_step_host_matches_device_path():
     assert torch.equal(h_lse, res["lse"].cpu())
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_cuda_graph_replay_recomputes_from_device_inputs(dtype):
+    """The step (plan -> attn -> combine, chained with programmatic dependent
+    launch) captures into one CUDA graph; each replay re-plans from the lengths
+    in device memory, so new lengths and new Q give new, correct outputs."""
+    lens_a = [100, 3000, 64, 777, 0]
+    lens_b = [2000, 5, 640, 3100, 129]
+    cap = [max(x, y) for x, y in zip(lens_a, lens_b)]
+    case = case_for(cap, 2, dtype, seed=21)
+    Hkv = 2
+    case["seq_lens"].copy_(torch.tensor(lens_a, dtype=torch.int32))
+    plan = hb.hpc_decode_plan(case["seq_lens"], Hkv, 24, 2)
+    so, sl = hb.split_buffers(plan)
+    out = torch.empty_like(case["q"])
+    lse = torch.empty(case["q"].shape[:2], dtype=torch.float32, device=DEV)
+
+    def step():
+        hb.hpc_decode_plan(case["seq_lens"], Hkv, 24, 2, plan=plan)
+        hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
+                           case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
+                           num_pages=case["num_pages"])
+        hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(5)
+    for lens in (lens_a, lens_b, lens_a):
+        case["seq_lens"].copy_(torch.tensor(lens, dtype=torch.int32))
+        case["q"].copy_(torch.randn(case["q"].shape, generator=gen, device=DEV).to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        res = dict(plan=plan, split_o=so, split_lse=sl, out=out, lse=lse)
+        _gpu.check_plan_exact(res, case, min_chunks=2)
+        _gpu.check_full(case, res)
+
+
+def test_many_steps_chained_without_sync():
+    """Back-to-back steps on one stream with no host synchronisation between
+    them: each kernel waits for its predecessor's output before reading it."""
+    lens = [1000, 64, 4097, 300]
+    case = case_for(lens, 2, seed=22)
+    plan = hb.hpc_decode_plan(case["seq_lens"], 2, 16, 2)
+    so, sl = hb.split_buffers(plan)
+    outs = []
+    for k in range(6):
+        hb.hpc_decode_plan(case["seq_lens"], 2, 16, 2, plan=plan)
+        hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
+                           case["seq_lens"], plan, so, sl, num_pages=case["num_pages"])
+        o = torch.empty_like(case["q"])
+        l = torch.empty(case["q"].shape[:2], dtype=torch.float32, device=DEV)
+        hb.hpc_decode_combine(plan, so, sl, o, l, 2)
+        outs.append((o, l))
+    torch.cuda.synchronize()
+    res = dict(plan=plan, split_o=so, split_lse=sl, out=outs[-1][0], lse=outs[-1][1])
+    _gpu.check_full(case, res)
+    for o, l in outs:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 def _sample_requests(lens, k, seed):
