@@ -18,6 +18,8 @@ Recipe (stated once here and in the design notes):
     128-vector x gets scale = amax|x| / 448 (1 when amax is 0) and codes
     e4m3(x / scale) by round-to-nearest-even; the scale is stored as float32 in
     [page][kv_head][slot] order.
+  * An e4m3 Q (q_dtype "fp8") is quantised the same way per (request, query
+    head), with its scale in a float32 [B, Hq] array.
   * Q/K/V of a large batch are drawn on the GPU; the oracle reads a host copy
     of the same bytes.
 """
@@ -50,6 +52,7 @@ class Workload:
     num_ctas: int | None = None       # None: device default
     min_chunks: int = 2
     static_splits: int = 16
+    q_dtype: str = "bf16"  # "bf16", or "fp8": e4m3 codes with one float32 scale per (request, head)
     note: str = ""
     extra: dict = field(default_factory=dict)
 
@@ -70,6 +73,9 @@ WORKLOADS = {
                      note="batch 32: 1 x 131072 + 31 x 1024 tokens, 64 Q / 8 KV heads, bf16"),
     "fp8": Workload("fp8", 64, 64, 8, "fp8", 4, loguniform=(512, 262144), total_cap=FOUR_M,
                     note="batch 64, L log-uniform in [512, 262144] capped at 4M tokens, e4m3 KV"),
+    "fp8q": Workload("fp8q", 64, 64, 8, "fp8", 4, loguniform=(512, 262144), total_cap=FOUR_M,
+                     q_dtype="fp8",
+                     note="the fp8 batch with e4m3 Q and a per-(request, head) Q scale"),
 }
 
 TABLE3_MIXES = {
@@ -164,7 +170,8 @@ def _fill_cache_e4m3(num_pages, Hkv, gen, device, block_pages=2048):
 def make_case(w: Workload, device="cpu", lens=None, pool_pages=None, stride=None) -> dict:
     """Draw one decode batch. Tensors live on ``device``.
 
-    Returns a dict with q (bf16 [B,Hq,128]), k_cache / v_cache (bf16 or
+    Returns a dict with q (bf16 [B,Hq,128], or float8_e4m3fn with q_scale float32
+    [B,Hq] when the workload's q_dtype is "fp8"), k_cache / v_cache (bf16 or
     float8_e4m3fn [pages,64,Hkv,128]), k_scale / v_scale (float32
     [pages,Hkv,64] or None), page_table (int32 [B,stride]), seq_lens (int32 [B]),
     num_pages, and the workload.
@@ -174,7 +181,16 @@ def make_case(w: Workload, device="cpu", lens=None, pool_pages=None, stride=None
                                        w.seed, stride)
     gen = torch.Generator(device=device)
     gen.manual_seed(int(w.seed) * 1000003 + 17)
-    q = _bf16_normal((len(L), w.num_q_heads, HEAD_DIM), gen, device)
+    q_scale = None
+    if w.q_dtype == "fp8":
+        x = torch.randn((len(L), w.num_q_heads, HEAD_DIM), generator=gen, device=device,
+                        dtype=torch.float32)
+        amax = x.abs().amax(dim=-1, keepdim=True)
+        s = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+        q = (x / s).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+        q_scale = s.squeeze(-1).contiguous()
+    else:
+        q = _bf16_normal((len(L), w.num_q_heads, HEAD_DIM), gen, device)
     if w.kv_dtype == "fp8":
         k, ks = _fill_cache_e4m3(num_pages, w.num_kv_heads, gen, device)
         v, vs = _fill_cache_e4m3(num_pages, w.num_kv_heads, gen, device)
@@ -182,7 +198,7 @@ def make_case(w: Workload, device="cpu", lens=None, pool_pages=None, stride=None
         k = _fill_cache_bf16(num_pages, w.num_kv_heads, gen, device)
         v = _fill_cache_bf16(num_pages, w.num_kv_heads, gen, device)
         ks = vs = None
-    return dict(workload=w, q=q, k_cache=k, v_cache=v, k_scale=ks, v_scale=vs,
+    return dict(workload=w, q=q, q_scale=q_scale, k_cache=k, v_cache=v, k_scale=ks, v_scale=vs,
                 page_table=torch.from_numpy(table).to(device),
                 seq_lens=torch.from_numpy(L.astype(np.int32)).to(device),
                 num_pages=num_pages)
@@ -215,6 +231,8 @@ def to_numpy_case(case: dict, requests=None) -> dict:
             off += nb
         pt, sl = new_pt, sl[req]
         q = q.index_select(0, torch.from_numpy(req).to(q.device))
+        if case.get("q_scale") is not None:
+            qs_sel = case["q_scale"].index_select(0, torch.from_numpy(req).to(q.device))
 
     def bits(t):
         t = t.detach().cpu().contiguous()
@@ -226,6 +244,9 @@ def to_numpy_case(case: dict, requests=None) -> dict:
 
     out = dict(q=bits(q), k_cache=bits(k), v_cache=bits(v), page_table=np.ascontiguousarray(pt),
                seq_lens=np.ascontiguousarray(sl.astype(np.int32)))
+    if case.get("q_scale") is not None:
+        qs = qs_sel if requests is not None else case["q_scale"]
+        out["q_scale"] = qs.detach().cpu().numpy()
     if ks is not None:
         out["k_scale"] = ks.detach().cpu().numpy()
         out["v_scale"] = vs.detach().cpu().numpy()

@@ -81,7 +81,7 @@ def load_library(path: str):
     L.oracle_set_num_threads.argtypes = [ci]
     L.oracle_plan.argtypes = [i32p, ci, ci, ci, ci, i32p, ctypes.c_longlong]
     L.oracle_plan_static.argtypes = [i32p, ci, ci, ci, i32p, ctypes.c_longlong]
-    kv = [vp, vp, vp, vp, vp, ci, ci, i32p, ci, i32p, ci, ci, ci]
+    kv = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, i32p, ci, ci, ci]
     L.oracle_attn_rows.argtypes = kv + [ci, i32p, f64p, f64p]
     L.oracle_attn_splits.argtypes = [i32p] + kv + [f64p, f64p]
     L.oracle_combine.argtypes = [i32p, f64p, f64p, ci, ci, ci, f64p, f64p]
@@ -181,13 +181,18 @@ def _kv_args(case):
     if fp8:
         ks = np.ascontiguousarray(case["k_scale"], dtype=np.float32)
         vs = np.ascontiguousarray(case["v_scale"], dtype=np.float32)
-    q = np.ascontiguousarray(case["q"], dtype=np.uint16)
+    qs = None
+    if case.get("q_scale") is not None:
+        q = np.ascontiguousarray(case["q"], dtype=np.uint8)
+        qs = np.ascontiguousarray(case["q_scale"], dtype=np.float32)
+    else:
+        q = np.ascontiguousarray(case["q"], dtype=np.uint16)
     pt = np.ascontiguousarray(case["page_table"], dtype=np.int32)
     sl = np.ascontiguousarray(case["seq_lens"], dtype=np.int32)
     B, Hq, _ = q.shape
     Hkv = kc.shape[2]
-    keep = (q, kc, vc, ks, vs, pt, sl)
-    args = [_vp(q), _vp(kc), _vp(vc), _vp(ks), _vp(vs), int(fp8), int(kc.shape[0]),
+    keep = (q, qs, kc, vc, ks, vs, pt, sl)
+    args = [_vp(q), _vp(qs), _vp(kc), _vp(vc), _vp(ks), _vp(vs), int(fp8), int(kc.shape[0]),
             _p(pt, ctypes.c_int32), int(pt.shape[1]), _p(sl, ctypes.c_int32), B, Hq, Hkv]
     return args, keep, B, Hq, Hkv
 
@@ -195,7 +200,8 @@ def _kv_args(case):
 def attn_rows(case: dict, rows=None):
     """Full-sequence attention (float64) for the given (b, qh) rows, or all rows.
 
-    ``case`` holds numpy arrays: q (uint16 bf16 bits [B,Hq,128]), k_cache and
+    ``case`` holds numpy arrays: q (uint16 bf16 bits [B,Hq,128], or uint8 e4m3
+    codes with q_scale float32 [B,Hq]), k_cache and
     v_cache (uint16 bf16 bits or uint8 e4m3 codes, [pages,64,Hkv,128]),
     k_scale/v_scale (float32 [pages,Hkv,64], e4m3 only), page_table
     (int32 [B, stride]) and seq_lens (int32 [B]).

@@ -337,7 +337,8 @@ int oracle_plan_static(const int32_t* seq_lens, int B, int Hkv, int S, int32_t* 
 /* ---------------------------------------------------------------- attention */
 
 typedef struct {
-    const uint16_t* q; /* bf16 bits [B][Hq][128] */
+    const void* q;     /* bf16 bits, or e4m3 codes when q_scale is set: [B][Hq][128] */
+    const float* q_scale; /* e4m3 query only: [B][Hq] */
     const void* kc;    /* [P][64][Hkv][128] bf16 bits or e4m3 bytes */
     const void* vc;
     const float* ks; /* e4m3 only: [P][Hkv][64] */
@@ -373,8 +374,17 @@ static int or_attend(const or_kv* kv, int b, int qh, long long t0, long long t1,
         return 0;
     }
     double qv[OR_HEAD_DIM];
-    const uint16_t* qrow = kv->q + ((long long)b * kv->Hq + qh) * OR_HEAD_DIM;
-    for (int dd = 0; dd < OR_HEAD_DIM; ++dd) qv[dd] = oracle_bf16_to_f64(qrow[dd]);
+    const long long qoff = ((long long)b * kv->Hq + qh) * OR_HEAD_DIM;
+    if (kv->q_scale) {
+        /* e4m3 query with one scale per (request, query head), the form the fused
+         * attention prologue hands to the attention kernel */
+        const uint8_t* qrow = (const uint8_t*)kv->q + qoff;
+        const double qs = kv->q_scale[(long long)b * kv->Hq + qh];
+        for (int dd = 0; dd < OR_HEAD_DIM; ++dd) qv[dd] = oracle_e4m3_to_f64(qrow[dd]) * qs;
+    } else {
+        const uint16_t* qrow = (const uint16_t*)kv->q + qoff;
+        for (int dd = 0; dd < OR_HEAD_DIM; ++dd) qv[dd] = oracle_bf16_to_f64(qrow[dd]);
+    }
     long long n = t1 - t0;
     double* s = (double*)malloc(sizeof(double) * (size_t)n);
     if (!s) return -3;
@@ -421,12 +431,13 @@ static int or_check_kv(const or_kv* kv) {
 
 /* Full-sequence attention for selected rows. rows holds nrows (b, qh) pairs;
  * rows == NULL means every row in (b, qh) order (nrows must be B * Hq).
+ * q is bf16 bits, or e4m3 codes scaled by q_scale[b][qh] when q_scale != NULL.
  * Outputs: out_o [nrows][128], out_lse [nrows]. */
-int oracle_attn_rows(const uint16_t* q, const void* kc, const void* vc, const float* ks,
-                     const float* vs, int kv_fp8, int num_pages, const int32_t* pt,
+int oracle_attn_rows(const void* q, const float* q_scale, const void* kc, const void* vc,
+                     const float* ks, const float* vs, int kv_fp8, int num_pages, const int32_t* pt,
                      int pt_stride, const int32_t* seq_lens, int B, int Hq, int Hkv, int nrows,
                      const int32_t* rows, double* out_o, double* out_lse) {
-    or_kv kv = {q, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv};
+    or_kv kv = {q, q_scale, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv};
     if (or_check_kv(&kv)) return -1;
     if (!rows && nrows != B * Hq) return -1;
     int bad = 0;
@@ -448,11 +459,11 @@ int oracle_attn_rows(const uint16_t* q, const void* kc, const void* vc, const fl
  * oracle_plan_static: for descriptor s = (h, b, c0, c1) and each j < G the
  * attention of row (b, h*G + j) over tokens [64*c0, min(64*c1, L_b)).
  * Outputs: split_o [total_splits][G][128], split_lse [total_splits][G]. */
-int oracle_attn_splits(const int32_t* plan, const uint16_t* q, const void* kc, const void* vc,
-                       const float* ks, const float* vs, int kv_fp8, int num_pages,
+int oracle_attn_splits(const int32_t* plan, const void* q, const float* q_scale, const void* kc,
+                       const void* vc, const float* ks, const float* vs, int kv_fp8, int num_pages,
                        const int32_t* pt, int pt_stride, const int32_t* seq_lens, int B, int Hq,
                        int Hkv, double* split_o, double* split_lse) {
-    or_kv kv = {q, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv};
+    or_kv kv = {q, q_scale, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv};
     if (or_check_kv(&kv)) return -1;
     if (plan[OR_H_BATCH] != B || plan[OR_H_NUM_KV_HEADS] != Hkv) return -1;
     int G = Hq / Hkv;

@@ -230,8 +230,9 @@ def check_static_random(seed=1, trials=30):
 
 # ------------------------------------------------------------------ attention
 
-def small_case(lens, hkv=1, hq=8, dtype="bf16", seed=0, pool=None):
-    w = wl.Workload("pin", len(lens), hq, hkv, dtype, seed, lens=list(lens), pool_pages=pool)
+def small_case(lens, hkv=1, hq=8, dtype="bf16", seed=0, pool=None, q_dtype="bf16"):
+    w = wl.Workload("pin", len(lens), hq, hkv, dtype, seed, lens=list(lens), pool_pages=pool,
+                    q_dtype=q_dtype)
     case = wl.make_case(w, device="cpu")
     return wl.to_numpy_case(case)
 
@@ -267,7 +268,11 @@ def check_attn_vs_sdpa(case, tol=1e-12):
     Hkv = case["k_cache"].shape[2]
     G = Hq // Hkv
     o, lse = oracle.attn_rows(case)
-    q64 = torch.from_numpy(case["q"].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    if case.get("q_scale") is not None:
+        q64 = (torch.from_numpy(case["q"]).view(torch.float8_e4m3fn).to(torch.float64)
+               * torch.from_numpy(case["q_scale"]).to(torch.float64)[..., None])
+    else:
+        q64 = torch.from_numpy(case["q"].view(np.int16)).view(torch.bfloat16).to(torch.float64)
     for b in range(B):
         if case["seq_lens"][b] <= 0:
             continue

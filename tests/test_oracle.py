@@ -63,6 +63,20 @@ def test_attn_matches_torch_sdpa(dtype):
     pins.check_attn_vs_sdpa(case)
 
 
+def test_attn_with_e4m3_query_matches_torch_sdpa():
+    """e4m3 Q with a scale per (request, query head), e4m3 KV."""
+    case = pins.small_case([1, 63, 64, 65, 200, 333], hkv=2, hq=16, dtype="fp8", seed=15,
+                           q_dtype="fp8")
+    assert case["q"].dtype == np.uint8 and case["q_scale"].shape == (6, 16)
+    pins.check_attn_vs_sdpa(case)
+
+
+def test_combine_of_splits_with_e4m3_query():
+    case = pins.small_case([37, 128, 300, 1000, 0, 5], hkv=2, hq=16, dtype="fp8", seed=16,
+                           q_dtype="fp8")
+    pins.check_combine_equals_full(case, 7, 2)
+
+
 def test_attn_closed_forms():
     pins.check_attn_closed_forms()
 

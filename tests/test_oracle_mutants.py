@@ -40,6 +40,7 @@ MUTANTS = {
     "tail_token_dropped": ("if (t1 > len) t1 = len;", "if (t1 > len) t1 = len - 1;"),
     "split_rank_off_by_one": ("t[5] = (int32_t)(i - split0[p]);", "t[5] = (int32_t)(i - split0[p] + 1);"),
     "combine_weights_unnormalised": ("for (int dd = 0; dd < OR_HEAD_DIM; ++dd) o[dd] /= wsum;", ""),
+    "query_scale_dropped": ("qv[dd] = oracle_e4m3_to_f64(qrow[dd]) * qs;", "qv[dd] = oracle_e4m3_to_f64(qrow[dd]);"),
 }
 
 
@@ -47,6 +48,7 @@ def _all_pins():
     case_bf = pins.small_case([1, 63, 64, 65, 200, 333], hkv=2, hq=16, dtype="bf16", seed=11)
     case_f8 = pins.small_case([1, 65, 333], hkv=2, hq=16, dtype="fp8", seed=11)
     case_cb = pins.small_case([37, 128, 300, 1000, 0, 5], hkv=2, hq=16, seed=12)
+    case_q8 = pins.small_case([1, 65, 333], hkv=2, hq=16, dtype="fp8", seed=15, q_dtype="fp8")
     return [
         pins.check_e4m3_closed_forms,
         pins.check_golden_dynamic,
@@ -55,6 +57,7 @@ def _all_pins():
         pins.check_attn_closed_forms,
         lambda: pins.check_attn_vs_sdpa(case_bf),
         lambda: pins.check_attn_vs_sdpa(case_f8),
+        lambda: pins.check_attn_vs_sdpa(case_q8),
         lambda: pins.check_combine_equals_full(case_cb, 7, 2),
         pins.check_empty_request,
         lambda: pins.check_split_ranges(pins.small_case([37, 128, 300, 1000], seed=13), 16, 2),
