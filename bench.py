@@ -85,11 +85,12 @@ def rank_workload(w, rank):
 
 
 def step_bytes(lens, w, n_splits):
-    """Algorithmic bytes of one step: live K+V (+e4m3 scales), Q, and the split
-    partials (8 x (128 + 1) float32 per split, written once and read once)."""
+    """Algorithmic bytes of one step: live K+V (+e4m3 scales), Q (+ its scales),
+    and the split partials (8 x (128 + 1) float32 per split, written once and
+    read once)."""
     from load_balanced_paged_02_gb300 import workloads as wl
     kv = wl.kv_bytes(lens, w.num_kv_heads, w.kv_dtype)
-    q = len(lens) * w.num_q_heads * 128 * 2
+    q = len(lens) * w.num_q_heads * ((128 + 4) if w.q_dtype == "fp8" else 256)
     part = n_splits * 8 * 129 * 4
     pages = int(wl.chunk_counts(lens).sum()) * 4
     return dict(kv=kv, q=q, partials_rw=2 * part, metric=kv + q + 2 * part,
@@ -301,7 +302,7 @@ def run_ours(args):
     plan = hb.Plan(w.batch, Hkv, C, dev)
     hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
     so, sl = hb.split_buffers(plan)
-    out = torch.empty_like(case["q"])
+    out = torch.empty(case["q"].shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(case["q"].shape[:2], dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
     n_splits = int(plan.buf[3].item())
@@ -315,7 +316,7 @@ def run_ours(args):
             ev[1].record(stream)
         hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                            case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
-                           num_pages=case["num_pages"])
+                           num_pages=case["num_pages"], q_scale=case["q_scale"])
         if ev is not None:
             ev[2].record(stream)
         hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
@@ -350,7 +351,7 @@ def run_ours(args):
         with torch.cuda.graph(layer_graph):
             hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                                case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
-                               num_pages=case["num_pages"])
+                               num_pages=case["num_pages"], q_scale=case["q_scale"])
             hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
         for _ in range(3):
             graph.replay()
@@ -404,7 +405,8 @@ def run_ours(args):
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if kvd == hb.KV_BF16 else "e4m3",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if kvd == hb.KV_BF16 else ("e4m3 (q and kv)" if w.q_dtype == "fp8" else "e4m3 kv, bf16 q"),
             "data": "synthetic",
             "config": {"workload": w.name, "detail": w.note, "num_ctas": C, "min_chunks": w.min_chunks,
                        "live_tokens": int(lens.sum()), "splits": n_splits,
@@ -432,7 +434,7 @@ def run_ours(args):
             hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits, plan=splan)
             hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                                case["seq_lens"], splan, sso, ssl, case["k_scale"], case["v_scale"],
-                               num_pages=case["num_pages"])
+                               num_pages=case["num_pages"], q_scale=case["q_scale"])
             hb.hpc_decode_combine(splan, sso, ssl, out, lse, Hkv)
         for _ in range(3):
             sstep()
@@ -458,8 +460,10 @@ def run_ours(args):
                                      "speedup_of_balanced": sms / ms_step}
         del sso, ssl, splan
 
-    # ---- end to end through the C ABI with host buffers
-    if not args.no_e2e:
+    # ---- end to end through the C ABI with host buffers (bf16 query path)
+    if not args.no_e2e and case["q_scale"] is not None and rank == 0:
+        result["e2e"] = {"unavailable": "hpc_decode_step_host takes a bf16 query"}
+    if not args.no_e2e and case["q_scale"] is None:
         B, Hq, D = case["q"].shape
         h_q = case["q"].cpu().pin_memory()
         h_sl = case["seq_lens"].cpu().pin_memory()

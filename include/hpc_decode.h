@@ -187,6 +187,24 @@ hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cac
                            float* split_lse, void* stream);
 
 /*
+ * Persistent decode attention with an e4m3 query ([SGL] "A fused attention
+ * prologue": the prologue emits Q in FP8 with one scale per token and head
+ * and passes both to the attention kernel, which does not requantise). Same
+ * task map, cache, outputs and errors as hpc_decode_attn with
+ * kv_dtype = HPC_KV_FP8_E4M3; the query is q8[b][qh][d] * q_scale[b][qh].
+ *   q8        device e4m3 codes [batch][num_q_heads][128], 16-byte aligned
+ *   q_scale   device float32 [batch][num_q_heads], 16-byte aligned, not NULL
+ * QK^T runs on e4m3 operands directly (K and Q codes, float32 accumulation);
+ * the scores are then multiplied by the K and Q scales.
+ */
+hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              int num_pages, const int32_t* page_table, int page_table_stride,
+                              const int32_t* seq_lens, int batch, int num_q_heads,
+                              int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
+                              float* split_o, float* split_lse, void* stream);
+
+/*
  * Combine ([SGL] the paragraph on execution; [VLLM] combine stage). For every
  * (request b, query head qh) with h = qh / 8, j = qh % 8 and the pair's
  * n = pair_nsplit[h*batch+b] partials starting at s0 = pair_split0[...]:

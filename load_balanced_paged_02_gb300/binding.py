@@ -51,6 +51,8 @@ SIGNATURES = {
     "hpc_decode_plan_static": (_i, [_vp, _i, _i, _i, _P, _vp]),
     "hpc_decode_attn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _P,
                              _vp, _vp, _vp]),
+    "hpc_decode_attn_q8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _P,
+                                _vp, _vp, _vp]),
     "hpc_decode_combine": (_i, [_P, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "hpc_decode_step_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "hpc_decode_step_host": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -194,8 +196,10 @@ def split_buffers(plan: Plan, device=None):
 
 
 def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split_o, split_lse,
-                    k_scale=None, v_scale=None, num_pages: int | None = None, stream=None):
-    """Persistent attention over the task map; writes split_o / split_lse."""
+                    k_scale=None, v_scale=None, num_pages: int | None = None, stream=None,
+                    q_scale=None):
+    """Persistent attention over the task map; writes split_o / split_lse.
+    A float8_e4m3fn q with its q_scale [B, Hq] goes to hpc_decode_attn_q8."""
     kvd = kv_dtype_of(k_cache)
     B, Hq, D = q.shape
     Hkv = k_cache.shape[2]
@@ -207,9 +211,18 @@ def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split
     _cuda_i32(seq_lens, "seq_lens")
     if split_o.shape[0] < plan.split_capacity or split_lse.shape[0] < plan.split_capacity:
         raise HpcError("split buffers", detail=f"need {plan.split_capacity} rows")
+    npages = int(num_pages if num_pages is not None else k_cache.shape[0])
+    if q.dtype in (torch.float8_e4m3fn, torch.uint8):
+        if q_scale is None:
+            raise HpcError("hpc_decode_attn_q8", detail="an e4m3 q needs q_scale")
+        rc = lib().hpc_decode_attn_q8(
+            _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), npages,
+            _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D,
+            int(k_cache.shape[1]), plan.ref(), _ptr(split_o), _ptr(split_lse), _stream(stream))
+        _check("hpc_decode_attn_q8", rc)
+        return
     rc = lib().hpc_decode_attn(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd,
-        int(num_pages if num_pages is not None else k_cache.shape[0]), _ptr(page_table),
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd, npages, _ptr(page_table),
         int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D, int(k_cache.shape[1]), plan.ref(),
         _ptr(split_o), _ptr(split_lse), _stream(stream))
     _check("hpc_decode_attn", rc)
@@ -227,7 +240,7 @@ def hpc_decode_combine(plan: Plan, split_o, split_lse, out, out_lse=None, num_kv
 
 def decode(q, k_cache, v_cache, page_table, seq_lens, k_scale=None, v_scale=None,
            num_ctas: int | None = None, min_chunks_per_cta: int = 2, static_splits: int | None = None,
-           stream=None):
+           stream=None, q_scale=None):
     """plan -> attn -> combine with freshly allocated buffers. Returns (out, lse, plan)."""
     Hkv = k_cache.shape[2]
     if static_splits:
@@ -238,8 +251,8 @@ def decode(q, k_cache, v_cache, page_table, seq_lens, k_scale=None, v_scale=None
         plan = hpc_decode_plan(seq_lens, Hkv, num_ctas, min_chunks_per_cta, stream=stream)
     so, sl = split_buffers(plan)
     hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan, so, sl, k_scale, v_scale,
-                    stream=stream)
-    out = torch.empty_like(q)
+                    stream=stream, q_scale=q_scale)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
     hpc_decode_combine(plan, so, sl, out, lse, Hkv, stream=stream)
     return out, lse, plan

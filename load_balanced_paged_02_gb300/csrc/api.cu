@@ -115,11 +115,16 @@ hpc_status hpc_decode_plan_static(const int32_t* d_seq_lens, int batch, int num_
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
 
-hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
-                           const float* v_scale, int kv_dtype, int num_pages, const int32_t* page_table,
-                           int page_table_stride, const int32_t* seq_lens, int batch, int num_q_heads,
-                           int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
-                           float* split_o, float* split_lse, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by hpc_decode_attn (bf16 Q) and hpc_decode_attn_q8 (e4m3 Q + scales).
+hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache, const void* v_cache,
+                       const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
+                       const int32_t* page_table, int page_table_stride, const int32_t* seq_lens, int batch,
+                       int num_q_heads, int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
+                       float* split_o, float* split_lse, void* stream) {
     hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
     if (st != HPC_OK) return st;
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
@@ -133,9 +138,11 @@ hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cac
     if (num_pages < 1 || (long long)num_pages * kChunk > 2147483647LL || page_table_stride < 1)
         return HPC_ERR_INVALID_ARG;
     if (fp8 && (long long)num_pages * num_kv_heads > 2147483647LL) return HPC_ERR_INVALID_ARG;
+    if (q_scale && (!fp8 || !aligned(q_scale, 16))) return fp8 ? HPC_ERR_INVALID_ARG : HPC_ERR_UNSUPPORTED;
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     AttnArgs a;
     a.q = q;
+    a.q_scale = q_scale;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
     a.k_scale = fp8 ? k_scale : nullptr;
@@ -157,6 +164,31 @@ hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cac
     cudaError_t e = launch_attn(a, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return HPC_ERR_INVALID_ARG;
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, int kv_dtype, int num_pages, const int32_t* page_table,
+                           int page_table_stride, const int32_t* seq_lens, int batch, int num_q_heads,
+                           int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
+                           float* split_o, float* split_lse, void* stream) {
+    return attn_common(q, nullptr, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
+                       page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
+                       split_o, split_lse, stream);
+}
+
+hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale, int num_pages,
+                              const int32_t* page_table, int page_table_stride, const int32_t* seq_lens,
+                              int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                              const hpc_plan* plan, float* split_o, float* split_lse, void* stream) {
+    if (!q_scale) return HPC_ERR_INVALID_ARG;
+    return attn_common(q8, q_scale, k_cache, v_cache, k_scale, v_scale, HPC_KV_FP8_E4M3, num_pages, page_table,
+                       page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
+                       split_o, split_lse, stream);
 }
 
 hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse, void* out,

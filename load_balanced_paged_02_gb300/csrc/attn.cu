@@ -88,6 +88,8 @@ struct Layout {
 
 struct Params {
     const __nv_bfloat16* q;
+    const uint8_t* q8;      // e4m3 query codes (QF8 instances)
+    const float* q_scale;   // one float32 scale per (request, query head) (QF8 instances)
     const float* k_scale;
     const float* v_scale;
     const int32_t* page_table;
@@ -123,9 +125,26 @@ __device__ __forceinline__ bool desc_ok(const Params& p, int h, int b, int c0, i
 
 // ------------------------------------------------------------------ consumer math
 
-template <bool FP8>
+template <bool FP8, bool QF8>
 __device__ __forceinline__ void load_q_frags(uint32_t qbase, int lane, uint32_t (&qf)[8][2]) {
-    if constexpr (!FP8) {
+    if constexpr (QF8) {
+        // e4m3 Q codes, rows of 128 bytes: thread (g, c) takes bytes [32c, 32c+32)
+        // of query g; k-step ks (32 dims) uses words 2ks and 2ks+1 of that slice,
+        // matching the K words the same thread reads (see chunk_compute).
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t base = qbase + (uint32_t)g * 128u + (uint32_t)c * 32u;
+        const uint4 v0 = lds128(base), v1 = lds128(base + 16u);
+        qf[0][0] = v0.x;
+        qf[0][1] = v0.y;
+        qf[1][0] = v0.z;
+        qf[1][1] = v0.w;
+        qf[2][0] = v1.x;
+        qf[2][1] = v1.y;
+        qf[3][0] = v1.z;
+        qf[3][1] = v1.w;
+#pragma unroll
+        for (int i = 4; i < 8; ++i) qf[i][0] = qf[i][1] = 0u;
+    } else if constexpr (!FP8) {
         // Q^T B-fragments: rows are the 8 query heads, 16-byte columns are dims.
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
@@ -210,10 +229,11 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int wq, int nv, int 
     __syncwarp();
 }
 
-template <bool FP8>
+template <bool FP8, bool QF8>
 __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, int nv,
-                                              const uint32_t (&qf)[8][2], float (&o)[8][4],
-                                              float (&m)[2], float (&l)[2], float scale_log2) {
+                                              const uint32_t (&qf)[8][2], const float (&qsc)[2],
+                                              float (&o)[8][4], float (&m)[2], float (&l)[2],
+                                              float scale_log2) {
     const int g = lane >> 2, c = lane & 3;
     const uint32_t sb = smem_u32(stage);
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -264,21 +284,35 @@ __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, 
         const uint4 k11 = lds128(kb + (uint32_t)(r0 + 8) * 128u + ((uint32_t)((2 * c + 1) ^ g) << 4));
         const uint32_t w0[8] = {k00.x, k00.y, k00.z, k00.w, k01.x, k01.y, k01.z, k01.w};
         const uint32_t w1[8] = {k10.x, k10.y, k10.z, k10.w, k11.x, k11.y, k11.z, k11.w};
+        if constexpr (QF8) {
+            // e4m3 x e4m3 straight from shared memory: 4 k-steps of 32 dims, the
+            // codes of K and Q in the same permuted order, no widening
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4];
-            e4m3x4_to_f16x2x2(w0[ks], a[0], a[2]);
-            e4m3x4_to_f16x2x2(w1[ks], a[1], a[3]);
-            if (ks & 1)
-                mma_f16(acc1, a, qf[ks][0], qf[ks][1]);
-            else
-                mma_f16(acc0, a, qf[ks][0], qf[ks][1]);
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t a[4] = {w0[2 * ks], w1[2 * ks], w0[2 * ks + 1], w1[2 * ks + 1]};
+                if (ks & 1)
+                    mma_e4m3(acc1, a, qf[ks][0], qf[ks][1]);
+                else
+                    mma_e4m3(acc0, a, qf[ks][0], qf[ks][1]);
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a[4];
+                e4m3x4_to_f16x2x2(w0[ks], a[0], a[2]);
+                e4m3x4_to_f16x2x2(w1[ks], a[1], a[3]);
+                if (ks & 1)
+                    mma_f16(acc1, a, qf[ks][0], qf[ks][1]);
+                else
+                    mma_f16(acc0, a, qf[ks][0], qf[ks][1]);
+            }
         }
         const float ks0 = ksc[r0] * scale_log2, ks1 = ksc[r0 + 8] * scale_log2;
-        s[0] = (acc0[0] + acc1[0]) * ks0;
-        s[1] = (acc0[1] + acc1[1]) * ks0;
-        s[2] = (acc0[2] + acc1[2]) * ks1;
-        s[3] = (acc0[3] + acc1[3]) * ks1;
+        // score columns 2c and 2c+1 are query heads 2c, 2c+1 (their Q scales)
+        s[0] = (acc0[0] + acc1[0]) * ks0 * qsc[0];
+        s[1] = (acc0[1] + acc1[1]) * ks0 * qsc[1];
+        s[2] = (acc0[2] + acc1[2]) * ks1 * qsc[0];
+        s[3] = (acc0[3] + acc1[3]) * ks1 * qsc[1];
         const bool v0 = g < nv, v1 = g + 8 < nv;
         if (!v0) s[0] = s[1] = kNegInf;
         if (!v1) s[2] = s[3] = kNegInf;
@@ -313,11 +347,12 @@ __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, 
 
 // ------------------------------------------------------------------ kernel
 
-template <bool FP8, int STAGES, int NG>
+template <bool FP8, bool QF8, int STAGES, int NG>
 __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
                        const Params p) {
+    static_assert(FP8 || !QF8, "an e4m3 query needs the e4m3 cache");
     using LY = Layout<FP8, STAGES, NG>;
     using Cfg = KvCfg<FP8>;
     constexpr int NCW = LY::kNCW;
@@ -376,10 +411,19 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
             if (lane == 0) {
                 ok = wait_bounded(&qempty[qs], ((qd >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
                 if (ok) {
-                    mbar_arrive_expect_tx(&qfull[qs], kQSlotBytes);
-                    bulk_load_nohint(qbuf + qs * kQSlotBytes,
-                                     p.q + ((long long)b * p.num_q_heads + (long long)h * kGroup) * kHeadDim,
-                                     kQSlotBytes, &qfull[qs]);
+                    const long long qrow = (long long)b * p.num_q_heads + (long long)h * kGroup;
+                    if constexpr (QF8) {
+                        // 8 rows of 128 e4m3 codes, then their 8 scales
+                        mbar_arrive_expect_tx(&qfull[qs], kGroup * kHeadDim + kGroup * 4);
+                        bulk_load_nohint(qbuf + qs * kQSlotBytes, p.q8 + qrow * kHeadDim, kGroup * kHeadDim,
+                                         &qfull[qs]);
+                        bulk_load_nohint(qbuf + qs * kQSlotBytes + kGroup * kHeadDim, p.q_scale + qrow,
+                                         kGroup * 4, &qfull[qs]);
+                    } else {
+                        mbar_arrive_expect_tx(&qfull[qs], kQSlotBytes);
+                        bulk_load_nohint(qbuf + qs * kQSlotBytes, p.q + qrow * kHeadDim, kQSlotBytes,
+                                         &qfull[qs]);
+                    }
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -463,12 +507,18 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
         uint32_t qf[8][2];
         const int qs = qd & 1;
         if (!wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
-        load_q_frags<FP8>(smem_u32(qbuf + qs * kQSlotBytes), lane, qf);
+        load_q_frags<FP8, QF8>(smem_u32(qbuf + qs * kQSlotBytes), lane, qf);
+        float qsc[2] = {1.f, 1.f};
+        if constexpr (QF8) {
+            const float* qs_smem = reinterpret_cast<const float*>(qbuf + qs * kQSlotBytes + kGroup * kHeadDim);
+            qsc[0] = qs_smem[2 * c];
+            qsc[1] = qs_smem[2 * c + 1];
+        }
         {
             // The slot may be refilled by TMA as soon as it is released, so the
             // release must wait until the fragment loads have returned: fold
             // every fragment word into a value that a store consumes first.
-            uint32_t x = 0;
+            uint32_t x = __float_as_uint(qsc[0]) ^ __float_as_uint(qsc[1]);
 #pragma unroll
             for (int i = 0; i < 8; ++i) x ^= qf[i][0] ^ qf[i][1];
             __syncwarp();
@@ -491,8 +541,8 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
                 if (!wait_bounded(&full[st], (seq / STAGES) & 1, abort_flag, kWaitLimitNs)) goto timeout;
                 const int nv = meta[st] - 16 * wq;
                 if (nv > 0)
-                    chunk_compute<FP8>(smem + (size_t)st * Cfg::kStageBytes, wq, lane, nv < 16 ? nv : 16, qf,
-                                       o, m, l, p.scale_log2);
+                    chunk_compute<FP8, QF8>(smem + (size_t)st * Cfg::kStageBytes, wq, lane, nv < 16 ? nv : 16,
+                                            qf, qsc, o, m, l, p.scale_log2);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
             }
@@ -617,10 +667,10 @@ bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int
     return r == CUDA_SUCCESS;
 }
 
-template <bool FP8, int STAGES, int NG>
+template <bool FP8, bool QF8, int STAGES, int NG>
 struct Inst {
     using LY = Layout<FP8, STAGES, NG>;
-    static const void* fn() { return reinterpret_cast<const void*>(&decode_attn_kernel<FP8, STAGES, NG>); }
+    static const void* fn() { return reinterpret_cast<const void*>(&decode_attn_kernel<FP8, QF8, STAGES, NG>); }
     // The shared-memory opt-in is set once per device (the launch path then
     // makes no extra runtime calls, which keeps it cheap and capturable).
     static cudaError_t prepare() {
@@ -637,13 +687,13 @@ struct Inst {
     static cudaError_t launch(const CUtensorMap* maps, const Params& p, int grid, cudaStream_t s) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        return launch_pdl(decode_attn_kernel<FP8, STAGES, NG>, dim3(grid), dim3(LY::kThreads), LY::kAlloc, s,
+        return launch_pdl(decode_attn_kernel<FP8, QF8, STAGES, NG>, dim3(grid), dim3(LY::kThreads), LY::kAlloc, s,
                           maps[0], maps[1], maps[2], maps[3], p);
     }
     static int ctas_per_sm() {
         if (prepare() != cudaSuccess) return 0;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<FP8, STAGES, NG>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_attn_kernel<FP8, QF8, STAGES, NG>,
                                                           LY::kThreads, LY::kAlloc) != cudaSuccess)
             return 0;
         return n;
@@ -654,12 +704,14 @@ struct Inst {
 // work on alternate chunks; measured on GB300 (mixed-length batches) these
 // ring depths were the best that fit in shared memory: bf16 4 x 32 KB
 // stages, e4m3 8 x 17 KB stages.
-using BalancedBf16 = Inst<false, 4, 2>;
-using BalancedFp8 = Inst<true, 8, 2>;
+using BalancedBf16 = Inst<false, false, 4, 2>;
+using BalancedFp8 = Inst<true, false, 8, 2>;
+using BalancedFp8Q = Inst<true, true, 8, 2>;
 // Static split-KV instances: one descriptor per CTA, shallow rings so that
 // several CTAs share an SM, as a non-persistent split-KV grid would.
-using StaticBf16 = Inst<false, 2, 1>;
-using StaticFp8 = Inst<true, 4, 1>;
+using StaticBf16 = Inst<false, false, 2, 1>;
+using StaticFp8 = Inst<true, false, 4, 1>;
+using StaticFp8Q = Inst<true, true, 4, 1>;
 
 }  // namespace
 
@@ -683,6 +735,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     const PlanLayout L = plan_layout(a.batch, a.num_kv_heads, a.num_ctas);
     Params p;
     p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+    p.q8 = reinterpret_cast<const uint8_t*>(a.q);
+    p.q_scale = a.q_scale;
     p.k_scale = a.k_scale;
     p.v_scale = a.v_scale;
     p.page_table = a.page_table;
@@ -700,6 +754,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     p.split_lse = a.split_lse;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
     const bool stat = a.mode == 1;
+    if (a.fp8 && a.q_scale)
+        return stat ? StaticFp8Q::launch(maps, p, a.num_ctas, s) : BalancedFp8Q::launch(maps, p, a.num_ctas, s);
     if (a.fp8)
         return stat ? StaticFp8::launch(maps, p, a.num_ctas, s) : BalancedFp8::launch(maps, p, a.num_ctas, s);
     return stat ? StaticBf16::launch(maps, p, a.num_ctas, s) : BalancedBf16::launch(maps, p, a.num_ctas, s);

@@ -95,14 +95,22 @@ def table3_workload(mix: str, num_q_heads: int = 8, num_kv_heads: int = 1, seed:
 
 
 def by_name(name: str) -> Workload:
-    """A workload by name: one of WORKLOADS, or "t3:<mix>" / "t3:<mix>:<Hq>/<Hkv>"
-    for a length mix of the decode-latency table (default 8 query / 1 KV head)."""
+    """A workload by name: one of WORKLOADS, or "t3:<mix>[:<Hq>/<Hkv>][:q8]" for a
+    length mix of the decode-latency table (default 8 query / 1 KV head; ":q8"
+    gives it an e4m3 query with per-head scales)."""
     if name in WORKLOADS:
         return WORKLOADS[name]
     parts = name.split(":")
+    q8 = parts[-1] == "q8"
+    if q8:
+        parts = parts[:-1]
     if parts[0] == "t3" and len(parts) in (2, 3) and parts[1] in TABLE3_MIXES:
         hq, hkv = (8, 1) if len(parts) == 2 else (int(x) for x in parts[2].split("/"))
-        return table3_workload(parts[1], hq, hkv)
+        w = table3_workload(parts[1], hq, hkv)
+        if q8:
+            w.q_dtype = "fp8"
+            w.name += ":q8"
+        return w
     raise KeyError(f"unknown workload {name!r}")
 
 

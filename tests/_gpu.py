@@ -29,8 +29,8 @@ def run(case, num_ctas=None, min_chunks=2, static_splits=None, plan=None):
     sl.fill_(float("nan"))
     hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                        case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
-                       num_pages=case["num_pages"])
-    out = torch.full_like(case["q"], float("nan"))
+                       num_pages=case["num_pages"], q_scale=case.get("q_scale"))
+    out = torch.full(case["q"].shape, float("nan"), dtype=torch.bfloat16, device=case["q"].device)
     lse = torch.full(case["q"].shape[:2], float("nan"), dtype=torch.float32, device=case["q"].device)
     hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
     torch.cuda.synchronize()

@@ -87,6 +87,22 @@ def test_attn_rejects_bad_arguments(L):
     assert _attn(L, pages=0, plan=ctypes.byref(plan)) == 1
 
 
+def test_attn_q8_rejects_bad_arguments(L):
+    plan = hb.PlanStruct(FAKE.value, 1 << 20, 2, 1, 4, 2, 0, 10)
+    args = dict(q8=FAKE, qs=FAKE, k=FAKE, v=FAKE, ks=FAKE, vs=FAKE, pages=16, pt=FAKE, stride=4, sl=FAKE,
+                B=2, Hq=8, Hkv=1, D=128, P=64, plan=ctypes.byref(plan), so=FAKE, slse=FAKE)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.hpc_decode_attn_q8(a["q8"], a["qs"], a["k"], a["v"], a["ks"], a["vs"], a["pages"], a["pt"],
+                                    a["stride"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
+                                    a["plan"], a["so"], a["slse"], None)
+    assert call(qs=None) == 1
+    assert call(qs=FAKE_ODD) == 1
+    assert call(ks=None) == 1
+    assert call(D=64) == 2
+
+
 def test_plan_rejects_bad_arguments(L):
     p = hb.PlanStruct(FAKE.value, 1 << 20, 0, 0, 0, 0, 0, 0)
     assert L.hpc_decode_plan(None, 4, 1, 16, 2, ctypes.byref(p), None) == 1

@@ -27,8 +27,9 @@ def _lib():
     hb.lib()
 
 
-def case_for(lens, hkv=1, dtype="bf16", seed=0, pool=None, stride=None):
-    w = wl.Workload("t", len(lens), 8 * hkv, hkv, dtype, seed, lens=list(lens), pool_pages=pool)
+def case_for(lens, hkv=1, dtype="bf16", seed=0, pool=None, stride=None, q_dtype="bf16"):
+    w = wl.Workload("t", len(lens), 8 * hkv, hkv, dtype, seed, lens=list(lens), pool_pages=pool,
+                    q_dtype=q_dtype)
     return wl.make_case(w, device=DEV, stride=stride)
 
 
@@ -102,6 +103,29 @@ def test_ragged_lengths_full(dtype, C, m):
     _gpu.check_full(case, res)
     out = res["out"].float().cpu().numpy()
     assert np.all(out[6] == 0) and np.all(np.isneginf(res["lse"][6].cpu().numpy()))
+
+
+@pytest.mark.parametrize("C,m", [(1, 0), (7, 1), (152, 2), (300, 4)])
+def test_e4m3_query_ragged_full(C, m):
+    """e4m3 Q with per-(request, head) scales on the e4m3 cache: QK^T on e4m3
+    operands, every row and every split against the oracle."""
+    lens = [1, 63, 64, 65, 127, 200, 0, 333, 1000, 4097, 2, 640]
+    case = case_for(lens, 2, "fp8", seed=C + m + 50, q_dtype="fp8")
+    assert case["q"].dtype == torch.float8_e4m3fn
+    res = _gpu.run(case, num_ctas=C, min_chunks=m)
+    _gpu.check_plan_exact(res, case, min_chunks=m)
+    _gpu.check_full(case, res)
+
+
+def test_e4m3_query_static_and_peaky():
+    lens = [37, 128, 300, 1000, 5000, 0, 64]
+    case = case_for(lens, 2, "fp8", seed=57, q_dtype="fp8")
+    res = _gpu.run(case, static_splits=4)
+    _gpu.check_full(case, res)
+    # a peaky query: scale x16 on one head of each request
+    case["q_scale"][:, 3] *= 16.0
+    res = _gpu.run(case, num_ctas=9)
+    _gpu.check_full(case, res)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
@@ -314,7 +338,7 @@ def test_uniform_workload_full():
     _gpu.check_split_invariants(case, res)
 
 
-@pytest.mark.parametrize("name", ["mixed", "skew", "fp8"])
+@pytest.mark.parametrize("name", ["mixed", "skew", "fp8", "fp8q"])
 def test_full_size_workload_sampled(name):
     w = wl.WORKLOADS[name]
     case = wl.make_case(w, device=DEV)
