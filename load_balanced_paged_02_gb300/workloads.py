@@ -266,3 +266,51 @@ def kv_bytes(lens, num_kv_heads: int, kv_dtype: str) -> int:
     tok = int(np.maximum(np.asarray(lens, dtype=np.int64), 0).sum())
     per = 2 * HEAD_DIM * (1 if kv_dtype == "fp8" else 2) + (8 if kv_dtype == "fp8" else 0)
     return tok * num_kv_heads * per
+
+
+# ---------------------------------------------------------------- prologue inputs
+
+def rope_table(max_pos: int, base: float = 10000.0) -> np.ndarray:
+    """Rotary table float32 [max_pos, 128]: cos(p * base^(-2i/128)) for i < 64,
+    then the matching sines (the model's precomputed rotary cache)."""
+    i = np.arange(HEAD_DIM // 2, dtype=np.float64)
+    inv_freq = base ** (-2.0 * i / HEAD_DIM)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def make_prologue_case(positions, num_q_heads, num_kv_heads, seed, device="cpu", max_pos=None,
+                       slots=None, eps=1e-6):
+    """Inputs of the fused prologue for tokens at the given positions: the QKV
+    projection output (bf16 [T, Hq + 2*Hkv, 128], N(0,1)), per-dim RMSNorm
+    weights (float32, 1 + 0.1 N(0,1)), the rotary table and the KV slots
+    (int32 page*64 + offset, or -1 to skip)."""
+    positions = np.asarray(positions, dtype=np.int32)
+    T = len(positions)
+    max_pos = int(positions.max()) + 1 if max_pos is None and T else (max_pos or 1)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed) * 7919 + 3)
+    H3 = num_q_heads + 2 * num_kv_heads
+    qkv = torch.randn((T, H3, HEAD_DIM), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    rng = np.random.default_rng(seed + 11)
+    qw = (1.0 + 0.1 * rng.standard_normal(HEAD_DIM)).astype(np.float32)
+    kw = (1.0 + 0.1 * rng.standard_normal(HEAD_DIM)).astype(np.float32)
+    if slots is None:
+        slots = np.arange(T, dtype=np.int32)
+    return dict(qkv=qkv, positions=torch.from_numpy(positions).to(device),
+                cos_sin=torch.from_numpy(rope_table(max_pos)).to(device),
+                q_weight=torch.from_numpy(qw).to(device), k_weight=torch.from_numpy(kw).to(device),
+                slots=torch.from_numpy(np.asarray(slots, dtype=np.int32)).to(device), eps=eps,
+                num_q_heads=num_q_heads, num_kv_heads=num_kv_heads)
+
+
+def decode_slots(case: dict) -> np.ndarray:
+    """Slot of each request's newest token (position L_b - 1) in a decode case."""
+    pt = case["page_table"].cpu().numpy()
+    L = case["seq_lens"].cpu().numpy().astype(np.int64)
+    out = np.full(len(L), -1, dtype=np.int32)
+    for b, n in enumerate(L):
+        if n > 0:
+            p = n - 1
+            out[b] = pt[b, p // PAGE] * PAGE + p % PAGE
+    return out

@@ -85,8 +85,11 @@ def load_library(path: str):
     L.oracle_attn_rows.argtypes = kv + [ci, i32p, f64p, f64p]
     L.oracle_attn_splits.argtypes = [i32p] + kv + [f64p, f64p]
     L.oracle_combine.argtypes = [i32p, f64p, f64p, ci, ci, ci, f64p, f64p]
+    L.oracle_rope_norm.argtypes = [ctypes.POINTER(ctypes.c_uint16), i32p, ctypes.POINTER(ctypes.c_float), ci,
+                                   ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
+                                   ctypes.c_double, ci, ci, ci, f64p, f64p, f64p]
     for f in ("oracle_plan", "oracle_plan_static", "oracle_attn_rows", "oracle_attn_splits",
-              "oracle_combine"):
+              "oracle_combine", "oracle_rope_norm"):
         getattr(L, f).restype = ci
     return L
 
@@ -257,3 +260,25 @@ def combine(plan_buf, split_o, split_lse, batch: int, num_q_heads: int, num_kv_h
     if rc:
         raise ValueError(f"oracle_combine failed ({rc})")
     return o, lse
+
+
+def rope_norm(qkv_bits, positions, cos_sin, q_weight, k_weight, eps, num_q_heads, num_kv_heads):
+    """Fused prologue in float64: RMS QK-norm then rotary embedding on Q and K,
+    V passed through. qkv_bits: uint16 bf16 bits [T, Hq + 2*Hkv, 128].
+    Returns (q [T,Hq,128], k [T,Hkv,128], v [T,Hkv,128]) float64, before rounding."""
+    x = np.ascontiguousarray(qkv_bits, dtype=np.uint16)
+    T = x.shape[0]
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    qw = np.ascontiguousarray(q_weight, dtype=np.float32)
+    kw = np.ascontiguousarray(k_weight, dtype=np.float32)
+    q = np.zeros((T, num_q_heads, HEAD_DIM))
+    k = np.zeros((T, num_kv_heads, HEAD_DIM))
+    v = np.zeros((T, num_kv_heads, HEAD_DIM))
+    rc = _load().oracle_rope_norm(_p(x, ctypes.c_uint16), _p(pos, ctypes.c_int32), _p(cs, ctypes.c_float),
+                                  cs.shape[0], _p(qw, ctypes.c_float), _p(kw, ctypes.c_float), float(eps), T,
+                                  num_q_heads, num_kv_heads, _p(q, ctypes.c_double), _p(k, ctypes.c_double),
+                                  _p(v, ctypes.c_double))
+    if rc:
+        raise ValueError(f"oracle_rope_norm failed ({rc})")
+    return q, k, v

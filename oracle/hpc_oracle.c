@@ -529,3 +529,59 @@ int oracle_combine(const int32_t* plan, const double* split_o, const double* spl
         }
     return 0;
 }
+
+/* ---------------------------------------------------------------- prologue */
+
+/* Fused attention prologue ([SGL] "A fused attention prologue"; [VLLM]
+ * "融合的注意力前奏", HpcRopeNorm): from the fused QKV projection output,
+ * RMS QK-norm, then rotary position embedding, for every query and key head;
+ * value heads pass through. Returns the float64 values before any output
+ * rounding or quantisation (the tests check the CUDA outputs against them).
+ *   qkv      bf16 bits [T][Hq + 2*Hkv][128], heads in the order Q, K, V
+ *   pos      int32 [T], position of each token (row of cos_sin)
+ *   cos_sin  float32 [max_pos][128]: cos(theta_i) for i < 64, then sin(theta_i)
+ *   qw, kw   float32 [128] RMSNorm weights shared by all query / key heads
+ *   q_out    [T][Hq][128], k_out / v_out [T][Hkv][128]
+ * RMSNorm: y_d = x_d / sqrt(mean_d x_d^2 + eps) * w_d.
+ * Rotation (pairs (i, i+64), i < 64): y_i = x_i c_i - x_{i+64} s_i,
+ * y_{i+64} = x_{i+64} c_i + x_i s_i. */
+int oracle_rope_norm(const uint16_t* qkv, const int32_t* pos, const float* cos_sin, int max_pos,
+                     const float* qw, const float* kw, double eps, int T, int Hq, int Hkv,
+                     double* q_out, double* k_out, double* v_out) {
+    if (T < 0 || Hq < 1 || Hkv < 1 || max_pos < 1) return -1;
+    const int H3 = Hq + 2 * Hkv;
+    const int half = OR_HEAD_DIM / 2;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (long long r = 0; r < (long long)T * H3; ++r) {
+        const int t = (int)(r / H3), j = (int)(r % H3);
+        const uint16_t* src = qkv + r * OR_HEAD_DIM;
+        double x[OR_HEAD_DIM];
+        for (int d = 0; d < OR_HEAD_DIM; ++d) x[d] = oracle_bf16_to_f64(src[d]);
+        double* dst;
+        if (j >= Hq + Hkv) {
+            dst = v_out + ((long long)t * Hkv + (j - Hq - Hkv)) * OR_HEAD_DIM;
+            for (int d = 0; d < OR_HEAD_DIM; ++d) dst[d] = x[d];
+            continue;
+        }
+        const float* w = j < Hq ? qw : kw;
+        dst = j < Hq ? q_out + ((long long)t * Hq + j) * OR_HEAD_DIM
+                     : k_out + ((long long)t * Hkv + (j - Hq)) * OR_HEAD_DIM;
+        double ss = 0.0;
+        for (int d = 0; d < OR_HEAD_DIM; ++d) ss += x[d] * x[d];
+        const double inv = 1.0 / sqrt(ss / OR_HEAD_DIM + eps);
+        for (int d = 0; d < OR_HEAD_DIM; ++d) x[d] = x[d] * inv * (double)w[d];
+        const int p = pos[t];
+        if (p < 0 || p >= max_pos) {
+            bad |= 1;
+            continue;
+        }
+        const float* cs = cos_sin + (long long)p * OR_HEAD_DIM;
+        for (int i = 0; i < half; ++i) {
+            const double c = cs[i], sn = cs[half + i];
+            dst[i] = x[i] * c - x[i + half] * sn;
+            dst[i + half] = x[i + half] * c + x[i] * sn;
+        }
+    }
+    return bad ? -4 : 0;
+}

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import _pins as pins
+import _pins_prologue as pp
 import oracle
 
 MUTANTS = {
@@ -41,6 +42,13 @@ MUTANTS = {
     "split_rank_off_by_one": ("t[5] = (int32_t)(i - split0[p]);", "t[5] = (int32_t)(i - split0[p] + 1);"),
     "combine_weights_unnormalised": ("for (int dd = 0; dd < OR_HEAD_DIM; ++dd) o[dd] /= wsum;", ""),
     "query_scale_dropped": ("qv[dd] = oracle_e4m3_to_f64(qrow[dd]) * qs;", "qv[dd] = oracle_e4m3_to_f64(qrow[dd]);"),
+    "rope_sign": ("dst[i] = x[i] * c - x[i + half] * sn;", "dst[i] = x[i] * c + x[i + half] * sn;"),
+    "rope_adjacent_pairs": ("dst[i + half] = x[i + half] * c + x[i] * sn;",
+                            "dst[i + half] = x[i + half] * c + x[(i + 1) % half] * sn;"),
+    "norm_without_eps": ("1.0 / sqrt(ss / OR_HEAD_DIM + eps)", "1.0 / sqrt(ss / OR_HEAD_DIM)"),
+    "norm_weight_dropped": ("x[d] = x[d] * inv * (double)w[d];", "x[d] = x[d] * inv;"),
+    "norm_sum_not_mean": ("1.0 / sqrt(ss / OR_HEAD_DIM + eps)", "1.0 / sqrt(ss + eps)"),
+    "k_uses_q_weight": ("const float* w = j < Hq ? qw : kw;", "const float* w = qw;"),
 }
 
 
@@ -62,6 +70,9 @@ def _all_pins():
         pins.check_empty_request,
         lambda: pins.check_split_ranges(pins.small_case([37, 128, 300, 1000], seed=13), 16, 2),
         pins.check_e4m3_all_codes,
+        pp.check_norm_at_position_zero,
+        pp.check_rotation_keeps_pair_norms,
+        pp.check_relative_position,
         pins.check_plan_bruteforce_tiny,
     ]
 
