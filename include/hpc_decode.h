@@ -81,6 +81,7 @@ typedef enum hpc_kv_dtype { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
 #define HPC_DEVERR_PAGE_OUT_OF_RANGE 4u  /* a page id outside [0, num_pages): chunk skipped */
 #define HPC_DEVERR_WAIT_TIMEOUT 8u       /* a bounded wait inside the kernel ran out */
 #define HPC_DEVERR_BAD_DESCRIPTOR 16u    /* a task descriptor outside the call's shapes */
+#define HPC_DEVERR_BAD_POSITION 32u      /* prologue: a position outside [0, max_pos): not rotated */
 
 /* Limits checked on the host. */
 #define HPC_MAX_BATCH 16384
@@ -217,6 +218,43 @@ hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* 
 hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse,
                               void* out, float* out_lse, int batch, int num_q_heads,
                               int num_kv_heads, int head_dim, void* stream);
+
+/*
+ * Fused attention prologue, HpcRopeNorm ([SGL] "A fused attention prologue";
+ * [VLLM] "融合的注意力前奏"). For every token t and head of the fused QKV
+ * projection output:
+ *   query and key heads: RMS QK-norm, y = x / sqrt(mean(x^2) + eps) * w
+ *     (w = q_weight or k_weight, shared by all heads), then rotary embedding
+ *     on pairs (i, i+64): y_i' = y_i c_i - y_{i+64} s_i,
+ *     y_{i+64}' = y_{i+64} c_i + y_i s_i, with (c, s) = row positions[t] of
+ *     cos_sin;
+ *   value heads: unchanged.
+ * Queries go to q_out: bf16, or (q_scale_out != NULL) e4m3 codes with one
+ * float32 scale per (token, query head), the input of hpc_decode_attn_q8.
+ * Keys and values go straight into the cache at slot_mapping[t] =
+ * page * 64 + offset (negative: not written): bf16, or e4m3 with one scale
+ * per (token, KV head) in k_scale / v_scale ([num_pages][num_kv_heads][64]).
+ * e4m3 scales are amax / 448 over the head's 128 values (1 if all are 0);
+ * codes are round-to-nearest-even of x / scale, saturated.
+ *   qkv          device bf16 [num_tokens][num_q_heads + 2*num_kv_heads][128],
+ *                heads in the order Q, K, V; 16-byte aligned
+ *   positions    device int32 [num_tokens]
+ *   cos_sin      device float32 [max_pos][128]: 64 cosines then 64 sines
+ *   q_weight,    device float32 [128], 16-byte aligned
+ *   k_weight
+ *   q_out        device bf16 or e4m3 [num_tokens][num_q_heads][128]
+ *   d_error_word device int32 or NULL: HPC_DEVERR_BAD_POSITION (row left
+ *                unrotated), HPC_DEVERR_PAGE_OUT_OF_RANGE (slot skipped)
+ * Errors: HPC_ERR_INVALID_ARG, HPC_ERR_UNSUPPORTED (head_dim != 128,
+ * page_size != 64), HPC_ERR_CUDA. num_tokens == 0 enqueues nothing.
+ */
+hpc_status hpc_rope_norm(const void* qkv, const int32_t* positions, const float* cos_sin, int max_pos,
+                         const float* q_weight, const float* k_weight, float eps,
+                         const int32_t* slot_mapping, int num_tokens, int num_q_heads,
+                         int num_kv_heads, int head_dim, int page_size, void* q_out,
+                         float* q_scale_out, void* k_cache, void* v_cache, float* k_scale,
+                         float* v_scale, int kv_dtype, int num_pages, int* d_error_word,
+                         void* stream);
 
 /*
  * Workspace bytes for hpc_decode_step_host: device copies of q, seq_lens and

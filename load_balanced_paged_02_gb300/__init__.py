@@ -14,7 +14,7 @@ _BINDING_NAMES = {
     "KV_BF16", "KV_FP8_E4M3", "HpcError", "Plan", "build", "default_num_ctas",
     "hpc_decode_attn", "hpc_decode_combine", "hpc_decode_plan", "hpc_decode_plan_static",
     "hpc_decode_read_error", "hpc_decode_step_host", "lib", "split_buffers", "decode",
-    "sm_count",
+    "sm_count", "hpc_rope_norm",
 }
 
 

@@ -54,6 +54,8 @@ SIGNATURES = {
     "hpc_decode_attn_q8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _P,
                                 _vp, _vp, _vp]),
     "hpc_decode_combine": (_i, [_P, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "hpc_rope_norm": (_i, [_vp, _vp, _vp, _i, _vp, _vp, ctypes.c_float, _vp, _i, _i, _i, _i, _i, _vp, _vp,
+                           _vp, _vp, _vp, _vp, _i, _i, _vp, _vp]),
     "hpc_decode_step_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "hpc_decode_step_host": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                   _i, _i, _vp, _sz, _vp, _vp, _vp]),
@@ -288,3 +290,19 @@ def hpc_decode_step_host(h_q, h_seq_lens, h_page_table, k_cache, v_cache, worksp
         int(k_cache.shape[1]), num_ctas, min_chunks_per_cta, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(h_out), _ptr(h_out_lse), _stream(stream))
     _check("hpc_decode_step_host", rc)
+
+
+def hpc_rope_norm(qkv, positions, cos_sin, q_weight, k_weight, slot_mapping, q_out, k_cache, v_cache,
+                  q_scale=None, k_scale=None, v_scale=None, eps: float = 1e-6, num_kv_heads=None,
+                  num_pages=None, error_word=None, stream=None):
+    """Fused prologue: QK-norm + rotary embedding on Q and K, K/V into the cache
+    slots, Q to q_out (bf16, or e4m3 codes with q_scale [T, Hq])."""
+    T, H3, D = qkv.shape
+    Hkv = num_kv_heads if num_kv_heads is not None else k_cache.shape[2]
+    Hq = H3 - 2 * Hkv
+    rc = lib().hpc_rope_norm(
+        _ptr(qkv), _ptr(positions), _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(q_weight), _ptr(k_weight),
+        float(eps), _ptr(slot_mapping), T, Hq, Hkv, D, int(k_cache.shape[1]), _ptr(q_out), _ptr(q_scale),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype_of(k_cache),
+        int(num_pages if num_pages is not None else k_cache.shape[0]), _ptr(error_word), _stream(stream))
+    _check("hpc_rope_norm", rc)

@@ -204,6 +204,50 @@ hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const 
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
 
+hpc_status hpc_rope_norm(const void* qkv, const int32_t* positions, const float* cos_sin, int max_pos,
+                         const float* q_weight, const float* k_weight, float eps, const int32_t* slot_mapping,
+                         int num_tokens, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                         void* q_out, float* q_scale_out, void* k_cache, void* v_cache, float* k_scale,
+                         float* v_scale, int kv_dtype, int num_pages, int* d_error_word, void* stream) {
+    if (head_dim != kHeadDim || page_size != kChunk) return HPC_ERR_UNSUPPORTED;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_kv_heads > HPC_MAX_KV_HEADS ||
+        num_q_heads > 4096 || max_pos < 1 || num_pages < 1 || !(eps >= 0.f))
+        return HPC_ERR_INVALID_ARG;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    if (!qkv || !positions || !cos_sin || !q_weight || !k_weight || !slot_mapping || !q_out || !k_cache ||
+        !v_cache)
+        return HPC_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return HPC_ERR_INVALID_ARG;
+    if (!aligned(qkv, 16) || !aligned(cos_sin, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) ||
+        !aligned(q_out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return HPC_ERR_INVALID_ARG;
+    if ((long long)num_pages * kChunk * num_kv_heads > (1LL << 40)) return HPC_ERR_INVALID_ARG;
+    if (num_tokens == 0) return HPC_OK;
+    RopeNormArgs a;
+    a.qkv = qkv;
+    a.positions = positions;
+    a.cos_sin = cos_sin;
+    a.max_pos = max_pos;
+    a.q_weight = q_weight;
+    a.k_weight = k_weight;
+    a.eps = eps;
+    a.slots = slot_mapping;
+    a.num_tokens = num_tokens;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.q_out = q_out;
+    a.q_scale = q_scale_out;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.k_scale = fp8 ? k_scale : nullptr;
+    a.v_scale = fp8 ? v_scale : nullptr;
+    a.num_pages = num_pages;
+    a.kv_fp8 = fp8;
+    a.err = d_error_word;
+    return launch_rope_norm(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
 size_t hpc_decode_step_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int page_table_stride,
                                        int num_ctas) {
     if (!sizes_ok(batch, num_kv_heads, num_ctas) || page_table_stride < 1 || num_q_heads < 1) return 0;

@@ -84,6 +84,28 @@ struct AttnArgs {
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 int attn_default_ctas(int fp8);
 
+struct RopeNormArgs {
+    const void* qkv;
+    const int32_t* positions;
+    const float* cos_sin;
+    int max_pos;
+    const float* q_weight;
+    const float* k_weight;
+    float eps;
+    const int32_t* slots;
+    int num_tokens, num_q_heads, num_kv_heads;
+    void* q_out;
+    float* q_scale;
+    void* k_cache;
+    void* v_cache;
+    float* k_scale;
+    float* v_scale;
+    int num_pages;
+    int kv_fp8;
+    int* err;
+};
+cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s);
+
 cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o,
                            const float* split_lse, __nv_bfloat16* out, float* out_lse, int B,
                            int Hq, int Hkv, cudaStream_t s);

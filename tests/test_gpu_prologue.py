@@ -1,0 +1,169 @@
+"""Fused attention prologue (HpcRopeNorm) against the float64 oracle (GPU only).
+
+bf16 outputs: within one bf16 rounding of the oracle value (plus float32
+arithmetic). e4m3 outputs are integers decided by floating point, so they are
+checked for validity: the scale is amax/448 of the oracle's row (relative
+1e-4), and each code is a nearest e4m3 value of oracle/scale (at most half a
+grid step away, with float32 slack); almost all codes equal the oracle's own
+rounding. The chained decode test runs prologue -> attention on both sides:
+the oracle side only uses the oracle's own prologue output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import oracle
+from load_balanced_paged_02_gb300 import binding as hb
+from load_balanced_paged_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hb.lib()
+
+
+def _bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _oracle(pc):
+    return oracle.rope_norm(_bits(pc["qkv"]), pc["positions"].cpu().numpy(), pc["cos_sin"].cpu().numpy(),
+                            pc["q_weight"].cpu().numpy(), pc["k_weight"].cpu().numpy(), pc["eps"],
+                            pc["num_q_heads"], pc["num_kv_heads"])
+
+
+def _e4m3_grid_step(v):
+    a = np.abs(v)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -9)))
+    return 2.0 ** (np.maximum(e, -6) - 3)
+
+
+def check_e4m3_rows(codes_u8, scales, ref, what):
+    """codes [..., 128] uint8, scales [...] float32, ref [..., 128] float64."""
+    ref_scale = np.abs(ref).max(axis=-1) / 448.0
+    ref_scale[ref_scale == 0] = 1.0
+    assert np.allclose(scales, ref_scale, rtol=1e-4, atol=0), f"{what}: scales"
+    val = torch.from_numpy(codes_u8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    v = ref / scales.astype(np.float64)[..., None]
+    slack = 2e-5 * np.abs(v) + 1e-6
+    assert np.all(np.abs(val - v) <= 0.5 * _e4m3_grid_step(v) + slack), f"{what}: code not a nearest value"
+    own = torch.from_numpy(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.mean(own != val) < 1e-3, f"{what}: too many codes differ from the oracle's rounding"
+
+
+def run_prologue(pc, q_fp8, kv_fp8, num_pages, err=None):
+    T = pc["qkv"].shape[0]
+    Hq, Hkv = pc["num_q_heads"], pc["num_kv_heads"]
+    kv_dt = torch.float8_e4m3fn if kv_fp8 else torch.bfloat16
+    k = torch.full((num_pages, 64, Hkv, 128), 3.0, device=DEV).to(kv_dt)
+    v = torch.full((num_pages, 64, Hkv, 128), 3.0, device=DEV).to(kv_dt)
+    ks = torch.full((num_pages, Hkv, 64), -7.0, device=DEV) if kv_fp8 else None
+    vs = torch.full((num_pages, Hkv, 64), -7.0, device=DEV) if kv_fp8 else None
+    q = torch.empty((T, Hq, 128), dtype=torch.float8_e4m3fn if q_fp8 else torch.bfloat16, device=DEV)
+    qs = torch.empty((T, Hq), dtype=torch.float32, device=DEV) if q_fp8 else None
+    hb.hpc_rope_norm(pc["qkv"], pc["positions"], pc["cos_sin"], pc["q_weight"], pc["k_weight"], pc["slots"],
+                     q, k, v, q_scale=qs, k_scale=ks, v_scale=vs, eps=pc["eps"], num_kv_heads=Hkv,
+                     error_word=err)
+    torch.cuda.synchronize()
+    return q, qs, k, v, ks, vs
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (64, 8)])
+def test_bf16_outputs_and_slots(Hq, Hkv):
+    T = 37
+    rng = np.random.default_rng(0)
+    pos = rng.integers(0, 8000, size=T).astype(np.int32)
+    slots = rng.permutation(10 * 64)[:T].astype(np.int32)
+    slots[5] = -1  # a padding token: nothing written
+    pc = wl.make_prologue_case(pos, Hq, Hkv, seed=1, device=DEV, max_pos=8192, slots=slots)
+    q, _, k, v, _, _ = run_prologue(pc, False, False, num_pages=10)
+    rq, rk, rv = _oracle(pc)
+    tol = lambda r: 2.0 ** -8 * np.abs(r) + 2e-5  # noqa: E731
+    assert np.all(np.abs(q.float().cpu().numpy() - rq) <= tol(rq))
+    kc, vc = k.float().cpu().numpy(), v.float().cpu().numpy()
+    written = np.zeros((10 * 64,), dtype=bool)
+    for t, sl in enumerate(slots):
+        if sl < 0:
+            continue
+        written[sl] = True
+        assert np.all(np.abs(kc[sl // 64, sl % 64] - rk[t]) <= tol(rk[t]))
+        assert np.array_equal(vc[sl // 64, sl % 64], rv[t].astype(np.float32))
+    untouched = kc.reshape(640, Hkv, 128)[~written]
+    assert np.all(untouched == 3.0) and np.all(vc.reshape(640, Hkv, 128)[~written] == 3.0)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (64, 8)])
+def test_e4m3_outputs(Hq, Hkv):
+    T = 29
+    rng = np.random.default_rng(1)
+    pos = rng.integers(0, 8000, size=T).astype(np.int32)
+    slots = rng.permutation(6 * 64)[:T].astype(np.int32)
+    pc = wl.make_prologue_case(pos, Hq, Hkv, seed=2, device=DEV, max_pos=8192, slots=slots)
+    q, qs, k, v, ks, vs = run_prologue(pc, True, True, num_pages=6)
+    rq, rk, rv = _oracle(pc)
+    check_e4m3_rows(q.view(torch.uint8).cpu().numpy(), qs.cpu().numpy(), rq, "q")
+    kc, vc = k.view(torch.uint8).cpu().numpy(), v.view(torch.uint8).cpu().numpy()
+    ksc, vsc = ks.cpu().numpy(), vs.cpu().numpy()
+    for t, sl in enumerate(slots):
+        pg, off = sl // 64, sl % 64
+        check_e4m3_rows(kc[pg, off], ksc[pg, :, off], rk[t], f"k token {t}")
+        check_e4m3_rows(vc[pg, off], vsc[pg, :, off], rv[t], f"v token {t}")
+
+
+def test_bad_position_sets_error_bit():
+    pc = wl.make_prologue_case([3, 9000, 5], 8, 1, seed=3, device=DEV, max_pos=16)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, _, _, _, _, _ = run_prologue(pc, False, False, num_pages=2, err=err)
+    assert int(err.item()) & 32
+    good = _oracle(dict(pc, positions=torch.tensor([3, 0, 5], dtype=torch.int32)))[0]
+    # rows of valid positions are exact; the bad row is normalised but not rotated
+    assert np.allclose(q[[0, 2]].float().cpu().numpy(), good[[0, 2]], rtol=2 ** -8, atol=2e-5)
+    assert np.allclose(q[1].float().cpu().numpy(), good[1], rtol=2 ** -8, atol=2e-5)
+
+
+def test_decode_chain_prologue_then_e4m3_attention():
+    """One decode step: the prologue writes each request's newest K/V into the
+    e4m3 cache and emits the e4m3 query; attention then reads both. The oracle
+    runs its own prologue, rounds it the same way (torch e4m3 conversion),
+    writes a host copy of the cache, and runs its attention."""
+    lens = [1, 70, 640, 3000, 64, 129]
+    w = wl.Workload("chain", len(lens), 64, 8, "fp8", 31, lens=lens)
+    case = wl.make_case(w, device=DEV)
+    slots = wl.decode_slots(case)
+    pos = np.asarray(lens, dtype=np.int32) - 1
+    pc = wl.make_prologue_case(pos, 64, 8, seed=32, device=DEV, max_pos=4096, slots=slots)
+    q8 = torch.empty((len(lens), 64, 128), dtype=torch.float8_e4m3fn, device=DEV)
+    qs = torch.empty((len(lens), 64), dtype=torch.float32, device=DEV)
+    host = wl.to_numpy_case(case)  # cache before the prologue writes (oracle side)
+    hb.hpc_rope_norm(pc["qkv"], pc["positions"], pc["cos_sin"], pc["q_weight"], pc["k_weight"], pc["slots"],
+                     q8, case["k_cache"], case["v_cache"], q_scale=qs, k_scale=case["k_scale"],
+                     v_scale=case["v_scale"], eps=pc["eps"], num_kv_heads=8)
+    gpu_case = dict(case, q=q8, q_scale=qs)
+    res = _gpu.run(gpu_case, num_ctas=40)
+
+    rq, rk, rv = _oracle(pc)
+
+    def quant(x):
+        s = np.abs(x).max(axis=-1) / 448.0
+        s[s == 0] = 1.0
+        c = torch.from_numpy(x / s[..., None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        return c, s.astype(np.float32)
+
+    qc, qsc = quant(rq)
+    kc, ksc = quant(rk)
+    vc, vsc = quant(rv)
+    for b, sl in enumerate(slots):
+        pg, off = sl // 64, sl % 64
+        host["k_cache"][pg, off], host["v_cache"][pg, off] = kc[b], vc[b]
+        host["k_scale"][pg, :, off], host["v_scale"][pg, :, off] = ksc[b], vsc[b]
+    host["q"], host["q_scale"] = qc, qsc
+    ro, rl = oracle.attn_rows(host)
+    B, Hq = len(lens), 64
+    _gpu.assert_close(res["out"].float().cpu().numpy(), res["lse"].cpu().numpy(), ro.reshape(B, Hq, 128),
+                      rl.reshape(B, Hq), case, "prologue -> attention")
