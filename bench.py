@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-static", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches only")
+    ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue timing")
     return ap.parse_args()
 
 
@@ -241,6 +242,57 @@ def oracle_sample(case, w, seconds, seed=99):
             f"({done / total:.2f} x the batch's {int(total)}), {spent:.1f} s of oracle time, "
             f"rate scaled to one whole batch")
     return full, oracle.num_threads(), text
+
+
+def prologue_timing(w, dev, n_rep=200):
+    """The fused prologue (hpc_rope_norm) for this workload's head shape: one
+    decode step (one token per request) and a prefill-sized pass of 8192
+    tokens, each replayed from a CUDA graph. Output dtypes follow the
+    workload: e4m3 cache -> e4m3 K/V and e4m3 Q."""
+    import torch
+    from load_balanced_paged_02_gb300 import binding as hb
+    from load_balanced_paged_02_gb300 import workloads as wl
+    fp8 = w.kv_dtype == "fp8"
+    out = {}
+    peak, _ = measured_peaks()
+    for label, T in (("decode", w.batch), ("prefill_8192", 8192)):
+        pos = np.arange(T, dtype=np.int32) % 4096
+        pc = wl.make_prologue_case(pos, w.num_q_heads, w.num_kv_heads, seed=77, device=dev, max_pos=4096,
+                                   slots=np.arange(T, dtype=np.int32))
+        pages = (T + 63) // 64
+        kv_dt = torch.float8_e4m3fn if fp8 else torch.bfloat16
+        k = torch.zeros((pages, 64, w.num_kv_heads, 128), dtype=kv_dt, device=dev)
+        v = torch.zeros_like(k)
+        ks = torch.zeros((pages, w.num_kv_heads, 64), dtype=torch.float32, device=dev) if fp8 else None
+        vs = torch.zeros_like(ks) if fp8 else None
+        q = torch.empty((T, w.num_q_heads, 128), dtype=kv_dt, device=dev)
+        qs = torch.empty((T, w.num_q_heads), dtype=torch.float32, device=dev) if fp8 else None
+
+        def call():
+            hb.hpc_rope_norm(pc["qkv"], pc["positions"], pc["cos_sin"], pc["q_weight"], pc["k_weight"],
+                             pc["slots"], q, k, v, q_scale=qs, k_scale=ks, v_scale=vs, eps=pc["eps"],
+                             num_kv_heads=w.num_kv_heads)
+        call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n_rep):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / n_rep
+        e = 1 if fp8 else 2
+        per_row_out = 128 * e + (4 if fp8 else 0)
+        byt = (T * (w.num_q_heads + 2 * w.num_kv_heads) * 256 + T * (512 + 8)
+               + T * (w.num_q_heads + 2 * w.num_kv_heads) * per_row_out)
+        gbs = byt / (us * 1e-6) / 1e9
+        out[label] = {"tokens": T, "us": us, "bytes": byt, "GB/s": gbs, "frac": gbs / peak}
+    return out
 
 
 # ---------------------------------------------------------------- arms
@@ -493,6 +545,10 @@ def run_ours(args):
                              "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                              "api": "hpc_decode_step_host (pinned host q/seq_lens/page_table in, "
                                     "out/lse back; KV cache resident in HBM)"}
+
+    # ---- the fused prologue that feeds this path (NEXT-1), for context
+    if rank == 0 and not args.no_prologue:
+        result["prologue"] = prologue_timing(w, dev)
 
     # ---- CPU oracle baseline (rank 0 only, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -337,6 +337,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
         cfg.numAttrs = 0;
         e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
     }
+    // a refused launch is reported through the return value; leave no error
+    // pending for the caller's next runtime call
+    if (e != cudaSuccess) (void)cudaGetLastError();
     return e;
 }
 

@@ -6,15 +6,22 @@
 // straight into their page slots of the cache (bf16, or e4m3 with one scale
 // per token and head). One pass over the QKV output; no intermediate tensors.
 //
-// One warp per (token, head) row; lane l owns dims [4l, 4l+4). The RMS sum and
-// the e4m3 absolute maximum are warp reductions; the rotation partner of dim d
-// (d +- 64) lives in lane l ^ 16.
+// One block per token. A half-warp owns one (token, head) row, lane k of the
+// half owning dims [8k, 8k+8) (16-byte loads and stores); a warp covers two
+// rows per round and the block's 8 warps cover 16 rows per round, every round
+// loaded before any is processed. The token's position, slot, rotary row and
+// the norm weights are loaded once per block. Reductions (norm sum, e4m3
+// absolute max) take four xor-shuffle steps inside the half-warp, and the
+// rotation partner of dim d (d +- 64) lives in lane ^ 8. Row kinds (query,
+// key, value) are per-lane predicates, so all lanes run every shuffle.
 #include "hpc_internal.cuh"
 
 namespace hpc {
 namespace {
 
-constexpr int kRowsPerBlock = 8;
+constexpr int kWarpsPerBlock = 8;
+constexpr int kRowsPerRound = 2 * kWarpsPerBlock;  // one row per half-warp
+constexpr int kMaxRounds = 4;                        // rounds loaded before any is processed
 constexpr float kE4m3Max = 448.f;
 
 struct PrologueParams {
@@ -36,116 +43,162 @@ struct PrologueParams {
     int num_pages;
     int kv_fp8;
     int* err;  // nullable
+    int rounds_per_block;  // rounds of 16 rows each block of a token takes (gridDim.y splits a token)
 };
 
-__device__ __forceinline__ float warp_sum(float v) {
+__device__ __forceinline__ float half_sum(float v) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
+__device__ __forceinline__ float half_max(float v) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    for (int off = 8; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
     return v;
 }
 
-// Four floats -> e4m3 with a per-row scale = amax / 448 (1 when the row is 0);
-// codes are round-to-nearest-even of x / scale, saturated. Returns the four
-// codes (dim 4l in the low byte) and writes the scale.
-__device__ __forceinline__ uint32_t quantise_row(const float (&y)[4], float& scale_out) {
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3]))));
-    const float scale = amax > 0.f ? amax / kE4m3Max : 1.f;
-    const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(y[0] / scale, y[1] / scale), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi =
-        __nv_cvt_float2_to_fp8x2(make_float2(y[2] / scale, y[3] / scale), __NV_SATFINITE, __NV_E4M3);
-    scale_out = scale;
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+__device__ __forceinline__ void unpack8(const uint4& r, float (&y)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        y[2 * k] = f.x;
+        y[2 * k + 1] = f.y;
+    }
 }
 
-__device__ __forceinline__ uint2 pack_bf16x4(const float (&y)[4]) {
-    uint2 r;
-    r.x = pack_bf16x2(y[0], y[1]);
-    r.y = pack_bf16x2(y[2], y[3]);
-    return r;
-}
-
-__global__ void __launch_bounds__(kRowsPerBlock * 32) rope_norm_kernel(const PrologueParams p) {
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) rope_norm_kernel(const PrologueParams p) {
     grid_dependency_wait();  // the QKV projection may still be finishing
     grid_launch_dependents();
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hl = lane & 15;                 // lane within the half-warp
+    const int half = lane >> 4;               // which of the warp's two rows
     const int H3 = p.Hq + 2 * p.Hkv;
-    const long long r = (long long)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (r >= (long long)p.T * H3) return;
-    const int t = (int)(r / H3), j = (int)(r % H3);
-
-    const uint2 raw = *reinterpret_cast<const uint2*>(p.qkv + r * kHeadDim + 4 * lane);
-    const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-    const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-    float y[4] = {x01.x, x01.y, x23.x, x23.y};
-
-    if (j < p.Hq + p.Hkv) {
-        // RMS QK-norm
-        const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
-        const float inv = rsqrtf(ss * (1.f / kHeadDim) + p.eps);
-        const float4 w = *reinterpret_cast<const float4*>((j < p.Hq ? p.qw : p.kw) + 4 * lane);
-        y[0] *= inv * w.x;
-        y[1] *= inv * w.y;
-        y[2] *= inv * w.z;
-        y[3] *= inv * w.w;
-        // rotary embedding on pairs (i, i + 64)
-        const int pos = p.pos[t];
-        if (pos >= 0 && pos < p.max_pos) {
-            const int i0 = (4 * lane) & 63;
-            const float* cs = p.cos_sin + (long long)pos * kHeadDim;
-            const float4 c = *reinterpret_cast<const float4*>(cs + i0);
-            const float4 s = *reinterpret_cast<const float4*>(cs + 64 + i0);
-            const float cv[4] = {c.x, c.y, c.z, c.w}, sv[4] = {s.x, s.y, s.z, s.w};
-            const float sign = lane < 16 ? -1.f : 1.f;
-            float partner[4];
+    const int t = blockIdx.x;
+    // the first rounds' rows load first: they do not depend on the position
+    const __nv_bfloat16* src = p.qkv + (size_t)t * H3 * kHeadDim + 8 * hl;
+    const int all_rounds = (H3 + kRowsPerRound - 1) / kRowsPerRound;
+    const int first = blockIdx.y * p.rounds_per_block;
+    const int rounds = min(all_rounds, first + p.rounds_per_block);
+    uint4 raw[kMaxRounds];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) partner[k] = __shfl_xor_sync(0xffffffffu, y[k], 16);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) y[k] = y[k] * cv[k] + sign * partner[k] * sv[k];
-        } else if (lane == 0 && p.err) {
-            atomicOr(p.err, (int)HPC_DEVERR_BAD_POSITION);
-        }
+    for (int r = 0; r < kMaxRounds; ++r) {
+        const int j = (first + r) * kRowsPerRound + 2 * warp + half;
+        raw[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (first + r < rounds && j < H3) raw[r] = *reinterpret_cast<const uint4*>(src + (size_t)j * kHeadDim);
     }
-
-    if (j < p.Hq) {
-        const long long qrow = (long long)t * p.Hq + j;
-        if (p.q_scale) {
-            float scale;
-            const uint32_t codes = quantise_row(y, scale);
-            *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.q_out) + qrow * kHeadDim + 4 * lane) = codes;
-            if (lane == 0) p.q_scale[qrow] = scale;
-        } else {
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.q_out) + qrow * kHeadDim + 4 * lane) =
-                pack_bf16x4(y);
-        }
-        return;
-    }
-
-    // K or V: into the token's page slot
+    const int pos = p.pos[t];
     const int slot = p.slots[t];
-    if (slot < 0) return;  // padding token: nothing to write
-    const int page = slot / kChunk, off = slot % kChunk;
-    if (page >= p.num_pages) {
-        if (lane == 0 && p.err) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
-        return;
+    const bool rotate = pos >= 0 && pos < p.max_pos;
+    const bool slot_ok = slot >= 0 && slot / kChunk < p.num_pages;
+    if (threadIdx.x == 0 && blockIdx.y == 0 && p.err) {
+        if (!rotate) atomicOr(p.err, (int)HPC_DEVERR_BAD_POSITION);
+        if (slot >= 0 && !slot_ok) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
     }
-    const bool is_k = j < p.Hq + p.Hkv;
-    const int h = is_k ? j - p.Hq : j - p.Hq - p.Hkv;
-    const long long elem = (((long long)page * kChunk + off) * p.Hkv + h) * kHeadDim + 4 * lane;
-    void* cache = is_k ? p.k_cache : p.v_cache;
-    if (p.kv_fp8) {
-        float scale;
-        const uint32_t codes = quantise_row(y, scale);
-        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(cache) + elem) = codes;
-        if (lane == 0) (is_k ? p.k_scale : p.v_scale)[((long long)page * p.Hkv + h) * kChunk + off] = scale;
-    } else {
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(cache) + elem) = pack_bf16x4(y);
+    // per-lane constants: rotation cos/sin, norm weights for dims [8*hl, 8*hl+8)
+    float c[8], sn[8], qw[8], kw[8];
+    {
+        const int i0 = (8 * hl) & 63;
+        const float* cs = p.cos_sin + (long long)(rotate ? pos : 0) * kHeadDim;
+        const float4 c0 = *reinterpret_cast<const float4*>(cs + i0), c1 = *reinterpret_cast<const float4*>(cs + i0 + 4);
+        const float4 s0 = *reinterpret_cast<const float4*>(cs + 64 + i0);
+        const float4 s1 = *reinterpret_cast<const float4*>(cs + 64 + i0 + 4);
+        const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const float4 q0 = *reinterpret_cast<const float4*>(p.qw + 8 * hl), q1 = *reinterpret_cast<const float4*>(p.qw + 8 * hl + 4);
+        const float4 k0 = *reinterpret_cast<const float4*>(p.kw + 8 * hl), k1 = *reinterpret_cast<const float4*>(p.kw + 8 * hl + 4);
+        const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        const float sign = hl < 8 ? -1.f : 1.f;  // first half of the dims: x_i c - x_{i+64} s
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            c[k] = rotate ? cc[k] : 1.f;
+            sn[k] = rotate ? sign * ss[k] : 0.f;
+            qw[k] = qq[k];
+            kw[k] = kk[k];
+        }
+    }
+    for (int r0 = first; r0 < rounds; r0 += kMaxRounds) {
+        if (r0 != first) {
+#pragma unroll
+            for (int r = 0; r < kMaxRounds; ++r) {
+                const int j = (r0 + r) * kRowsPerRound + 2 * warp + half;
+                raw[r] = make_uint4(0u, 0u, 0u, 0u);
+                if (r0 + r < rounds && j < H3) raw[r] = *reinterpret_cast<const uint4*>(src + (size_t)j * kHeadDim);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kMaxRounds; ++r) {
+            if (r0 + r >= rounds) break;  // uniform across the block
+            const int j = (r0 + r) * kRowsPerRound + 2 * warp + half;
+            const bool valid = j < H3;
+            const bool is_q = j < p.Hq, is_qk = j < p.Hq + p.Hkv;
+            float y[8];
+            unpack8(raw[r], y);
+            // RMS QK-norm (computed for every row, applied to query and key rows)
+            float s2 = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) s2 += y[k] * y[k];
+            s2 = half_sum(s2);
+            const float inv = is_qk ? rsqrtf(s2 * (1.f / kHeadDim) + p.eps) : 1.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y[k] *= is_qk ? inv * (is_q ? qw[k] : kw[k]) : 1.f;
+            // rotary embedding on pairs (i, i + 64)
+            float pr[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, y[k], 8);
+            if (is_qk) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) y[k] = y[k] * c[k] + pr[k] * sn[k];
+            }
+            // output format of this row
+            const bool fp8_row = is_q ? (p.q_scale != nullptr) : (p.kv_fp8 != 0);
+            float am = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(y[k]));
+            am = half_max(am);
+            if (!valid || (!is_q && !slot_ok)) continue;
+            size_t dst_elem;
+            void* dst;
+            float* scale_dst = nullptr;
+            if (is_q) {
+                const size_t qrow = (size_t)t * p.Hq + j;
+                dst_elem = qrow * kHeadDim + 8 * hl;
+                dst = p.q_out;
+                scale_dst = p.q_scale ? p.q_scale + qrow : nullptr;
+            } else {
+                const int h = is_qk ? j - p.Hq : j - p.Hq - p.Hkv;
+                const int page = slot / kChunk, off = slot % kChunk;
+                dst_elem = (((size_t)page * kChunk + off) * p.Hkv + h) * kHeadDim + 8 * hl;
+                dst = is_qk ? p.k_cache : p.v_cache;
+                if (p.kv_fp8) scale_dst = (is_qk ? p.k_scale : p.v_scale) + ((size_t)page * p.Hkv + h) * kChunk + off;
+            }
+            if (fp8_row) {
+                // x / scale with a correctly rounded division: bf16 inputs often land
+                // exactly on e4m3 rounding midpoints, where a reciprocal's last-bit
+                // error would break the tie the other way
+                const float scale = am > 0.f ? am / kE4m3Max : 1.f;
+                uint32_t codes[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                        make_float2(y[4 * k] / scale, y[4 * k + 1] / scale), __NV_SATFINITE, __NV_E4M3);
+                    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                        make_float2(y[4 * k + 2] / scale, y[4 * k + 3] / scale), __NV_SATFINITE, __NV_E4M3);
+                    codes[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                }
+                *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + dst_elem) = make_uint2(codes[0], codes[1]);
+                if (hl == 0) *scale_dst = scale;
+            } else {
+                uint4 packed;
+                packed.x = pack_bf16x2(y[0], y[1]);
+                packed.y = pack_bf16x2(y[2], y[3]);
+                packed.z = pack_bf16x2(y[4], y[5]);
+                packed.w = pack_bf16x2(y[6], y[7]);
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + dst_elem) = packed;
+            }
+        }
     }
 }
 
@@ -173,10 +226,13 @@ cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s) {
     p.num_pages = a.num_pages;
     p.kv_fp8 = a.kv_fp8;
     p.err = a.err;
-    const long long rows = (long long)a.num_tokens * (a.num_q_heads + 2 * a.num_kv_heads);
-    if (rows == 0) return cudaSuccess;
-    const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-    return launch_pdl(rope_norm_kernel, dim3((unsigned)blocks), dim3(kRowsPerBlock * 32), 0, s, p);
+    if (a.num_tokens == 0) return cudaSuccess;
+    // Few tokens (decode): one round of 16 rows per block, so that a token's
+    // rows spread over several blocks; many tokens (prefill): a block per token.
+    const int rounds = (a.num_q_heads + 2 * a.num_kv_heads + kRowsPerRound - 1) / kRowsPerRound;
+    p.rounds_per_block = (long long)a.num_tokens * rounds < 8LL * 152 ? 1 : rounds;
+    const unsigned splits = (unsigned)((rounds + p.rounds_per_block - 1) / p.rounds_per_block);
+    return launch_pdl(rope_norm_kernel, dim3((unsigned)a.num_tokens, splits), dim3(kWarpsPerBlock * 32), 0, s, p);
 }
 
 }  // namespace hpc

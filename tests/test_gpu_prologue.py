@@ -51,8 +51,13 @@ def check_e4m3_rows(codes_u8, scales, ref, what):
     assert np.allclose(scales, ref_scale, rtol=1e-4, atol=0), f"{what}: scales"
     val = torch.from_numpy(codes_u8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
     v = ref / scales.astype(np.float64)[..., None]
-    slack = 2e-5 * np.abs(v) + 1e-6
-    assert np.all(np.abs(val - v) <= 0.5 * _e4m3_grid_step(v) + slack), f"{what}: code not a nearest value"
+    # float32 norm/rotation error is relative to the row's magnitude (about 4 ulp
+    # of the row max = 448 in code units), not to each element
+    slack = 2e-5 * np.abs(v) + 4 * 2.0 ** -23 * 448
+    excess = np.abs(val - v) - (0.5 * _e4m3_grid_step(v) + slack)
+    bad = excess > 0
+    assert not bad.any(), (f"{what}: {int(bad.sum())} codes not a nearest value; worst excess "
+                           f"{excess.max():.3g} at v={v[np.unravel_index(excess.argmax(), v.shape)]:.6g}")
     own = torch.from_numpy(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
     assert np.mean(own != val) < 1e-3, f"{what}: too many codes differ from the oracle's rounding"
 
@@ -114,6 +119,24 @@ def test_e4m3_outputs(Hq, Hkv):
         pg, off = sl // 64, sl % 64
         check_e4m3_rows(kc[pg, off], ksc[pg, :, off], rk[t], f"k token {t}")
         check_e4m3_rows(vc[pg, off], vsc[pg, :, off], rv[t], f"v token {t}")
+
+
+def test_many_rows_path_matches_oracle():
+    """Enough rows that each warp takes eight of them (prefill-sized call)."""
+    T = 1000  # 1000 x 80 rows
+    rng = np.random.default_rng(9)
+    pos = rng.integers(0, 4000, size=T).astype(np.int32)
+    pc = wl.make_prologue_case(pos, 64, 8, seed=9, device=DEV, max_pos=4096,
+                               slots=np.arange(T, dtype=np.int32))
+    q, qs, k, v, ks, vs = run_prologue(pc, True, True, num_pages=16)
+    rq, rk, rv = _oracle(pc)
+    check_e4m3_rows(q.view(torch.uint8).cpu().numpy(), qs.cpu().numpy(), rq, "q")
+    kc = k.view(torch.uint8).cpu().numpy().reshape(1024, 8, 128)[:T]
+    vc = v.view(torch.uint8).cpu().numpy().reshape(1024, 8, 128)[:T]
+    ksc = ks.cpu().numpy().transpose(0, 2, 1).reshape(1024, 8)[:T]
+    vsc = vs.cpu().numpy().transpose(0, 2, 1).reshape(1024, 8)[:T]
+    check_e4m3_rows(kc, ksc, rk, "k")
+    check_e4m3_rows(vc, vsc, rv, "v")
 
 
 def test_bad_position_sets_error_bit():
