@@ -53,6 +53,7 @@ class Workload:
     min_chunks: int = 2
     static_splits: int = 16
     q_dtype: str = "bf16"  # "bf16", or "fp8": e4m3 codes with one float32 scale per (request, head)
+    q_len: int = 1         # new tokens per request (> 1: speculative verification rows)
     note: str = ""
     extra: dict = field(default_factory=dict)
 
@@ -179,7 +180,8 @@ def make_case(w: Workload, device="cpu", lens=None, pool_pages=None, stride=None
     """Draw one decode batch. Tensors live on ``device``.
 
     Returns a dict with q (bf16 [B,Hq,128], or float8_e4m3fn with q_scale float32
-    [B,Hq] when the workload's q_dtype is "fp8"), k_cache / v_cache (bf16 or
+    [B,Hq] when the workload's q_dtype is "fp8"; [B,q_len,Hq,128] and
+    [B,q_len,Hq] when the workload has q_len > 1), k_cache / v_cache (bf16 or
     float8_e4m3fn [pages,64,Hkv,128]), k_scale / v_scale (float32
     [pages,Hkv,64] or None), page_table (int32 [B,stride]), seq_lens (int32 [B]),
     num_pages, and the workload.
@@ -190,15 +192,15 @@ def make_case(w: Workload, device="cpu", lens=None, pool_pages=None, stride=None
     gen = torch.Generator(device=device)
     gen.manual_seed(int(w.seed) * 1000003 + 17)
     q_scale = None
+    qshape = (len(L), w.num_q_heads, HEAD_DIM) if w.q_len == 1 else (len(L), w.q_len, w.num_q_heads, HEAD_DIM)
     if w.q_dtype == "fp8":
-        x = torch.randn((len(L), w.num_q_heads, HEAD_DIM), generator=gen, device=device,
-                        dtype=torch.float32)
+        x = torch.randn(qshape, generator=gen, device=device, dtype=torch.float32)
         amax = x.abs().amax(dim=-1, keepdim=True)
         s = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
         q = (x / s).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
         q_scale = s.squeeze(-1).contiguous()
     else:
-        q = _bf16_normal((len(L), w.num_q_heads, HEAD_DIM), gen, device)
+        q = _bf16_normal(qshape, gen, device)
     if w.kv_dtype == "fp8":
         k, ks = _fill_cache_e4m3(num_pages, w.num_kv_heads, gen, device)
         v, vs = _fill_cache_e4m3(num_pages, w.num_kv_heads, gen, device)

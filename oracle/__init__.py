@@ -81,10 +81,10 @@ def load_library(path: str):
     L.oracle_set_num_threads.argtypes = [ci]
     L.oracle_plan.argtypes = [i32p, ci, ci, ci, ci, i32p, ctypes.c_longlong]
     L.oracle_plan_static.argtypes = [i32p, ci, ci, ci, i32p, ctypes.c_longlong]
-    kv = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, i32p, ci, ci, ci]
+    kv = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, i32p, ci, ci, ci, ci]
     L.oracle_attn_rows.argtypes = kv + [ci, i32p, f64p, f64p]
     L.oracle_attn_splits.argtypes = [i32p] + kv + [f64p, f64p]
-    L.oracle_combine.argtypes = [i32p, f64p, f64p, ci, ci, ci, f64p, f64p]
+    L.oracle_combine.argtypes = [i32p, f64p, f64p, ci, ci, ci, ci, f64p, f64p]
     L.oracle_rope_norm.argtypes = [ctypes.POINTER(ctypes.c_uint16), i32p, ctypes.POINTER(ctypes.c_float), ci,
                                    ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                                    ctypes.c_double, ci, ci, ci, f64p, f64p, f64p]
@@ -192,27 +192,32 @@ def _kv_args(case):
         q = np.ascontiguousarray(case["q"], dtype=np.uint16)
     pt = np.ascontiguousarray(case["page_table"], dtype=np.int32)
     sl = np.ascontiguousarray(case["seq_lens"], dtype=np.int32)
-    B, Hq, _ = q.shape
+    # q is [B, Hq, 128] (one new token per request) or [B, q_len, Hq, 128]
+    B, Hq = q.shape[0], q.shape[-2]
+    q_len = q.shape[1] if q.ndim == 4 else 1
     Hkv = kc.shape[2]
     keep = (q, qs, kc, vc, ks, vs, pt, sl)
     args = [_vp(q), _vp(qs), _vp(kc), _vp(vc), _vp(ks), _vp(vs), int(fp8), int(kc.shape[0]),
-            _p(pt, ctypes.c_int32), int(pt.shape[1]), _p(sl, ctypes.c_int32), B, Hq, Hkv]
-    return args, keep, B, Hq, Hkv
+            _p(pt, ctypes.c_int32), int(pt.shape[1]), _p(sl, ctypes.c_int32), B, Hq, Hkv, q_len]
+    return args, keep, B, Hq, Hkv, q_len
 
 
 def attn_rows(case: dict, rows=None):
-    """Full-sequence attention (float64) for the given (b, qh) rows, or all rows.
+    """Full-sequence attention (float64) for the given (b, r) rows, or all rows.
 
     ``case`` holds numpy arrays: q (uint16 bf16 bits [B,Hq,128], or uint8 e4m3
-    codes with q_scale float32 [B,Hq]), k_cache and
+    codes with q_scale float32 [B,Hq]; with several new tokens per request
+    [B,q_len,Hq,128] and [B,q_len,Hq]), k_cache and
     v_cache (uint16 bf16 bits or uint8 e4m3 codes, [pages,64,Hkv,128]),
     k_scale/v_scale (float32 [pages,Hkv,64], e4m3 only), page_table
-    (int32 [B, stride]) and seq_lens (int32 [B]).
-    Returns (o [n,128] float64, lse [n] float64).
+    (int32 [B, stride]) and seq_lens (int32 [B], counting the new tokens).
+    A row is (b, qi * Hq + qh); new token qi attends causally to tokens
+    [0, L_b - q_len + qi]. Returns (o [n,128] float64, lse [n] float64), all
+    rows in (b, qi, qh) order when ``rows`` is None.
     """
-    args, keep, B, Hq, Hkv = _kv_args(case)
+    args, keep, B, Hq, Hkv, q_len = _kv_args(case)
     if rows is None:
-        n, rp = B * Hq, None
+        n, rp = B * q_len * Hq, None
     else:
         r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
         n, rp = r.shape[0], _p(r, ctypes.c_int32)
@@ -228,37 +233,45 @@ def attn_rows(case: dict, rows=None):
 def attn_splits(plan_buf, case: dict):
     """Per-descriptor partial outputs and LSE of a task map (float64).
 
-    Returns (split_o [total_splits, G, 128], split_lse [total_splits, G]).
+    Returns (split_o [total_splits, G, 128], split_lse [total_splits, G]); with
+    a 4-D q, (split_o [total_splits, q_len, G, 128], split_lse [total_splits, q_len, G]).
     """
     pb = np.ascontiguousarray(plan_buf, dtype=np.int32)
-    args, keep, B, Hq, Hkv = _kv_args(case)
+    args, keep, B, Hq, Hkv, q_len = _kv_args(case)
     G = Hq // Hkv
     S = max(int(pb[3]), 1)
-    so = np.zeros((S, G, HEAD_DIM), dtype=np.float64)
-    sl = np.zeros((S, G), dtype=np.float64)
+    so = np.zeros((S, q_len, G, HEAD_DIM), dtype=np.float64)
+    sl = np.zeros((S, q_len, G), dtype=np.float64)
     rc = _load().oracle_attn_splits(_p(pb, ctypes.c_int32), *args, _p(so, ctypes.c_double),
                                     _p(sl, ctypes.c_double))
     if rc:
         raise ValueError(f"oracle_attn_splits failed ({rc})")
+    if np.asarray(case["q"]).ndim == 3:
+        so, sl = so[:, 0], sl[:, 0]
     return so[: int(pb[3])], sl[: int(pb[3])]
 
 
-def combine(plan_buf, split_o, split_lse, batch: int, num_q_heads: int, num_kv_heads: int):
-    """Merge partials into [B, Hq, 128] outputs and [B, Hq] LSE (float64)."""
+def combine(plan_buf, split_o, split_lse, batch: int, num_q_heads: int, num_kv_heads: int,
+            q_len: int | None = None):
+    """Merge partials into [B, Hq, 128] outputs and [B, Hq] LSE (float64);
+    with ``q_len`` given, into [B, q_len, Hq, 128] and [B, q_len, Hq]."""
     pb = np.ascontiguousarray(plan_buf, dtype=np.int32)
     G = num_q_heads // num_kv_heads
-    so = np.ascontiguousarray(split_o, dtype=np.float64).reshape(-1, G, HEAD_DIM)
-    sl = np.ascontiguousarray(split_lse, dtype=np.float64).reshape(-1, G)
+    n = 1 if q_len is None else int(q_len)
+    so = np.ascontiguousarray(split_o, dtype=np.float64).reshape(-1, n, G, HEAD_DIM)
+    sl = np.ascontiguousarray(split_lse, dtype=np.float64).reshape(-1, n, G)
     if so.shape[0] == 0:
-        so = np.zeros((1, G, HEAD_DIM))
-        sl = np.zeros((1, G))
-    o = np.zeros((batch, num_q_heads, HEAD_DIM), dtype=np.float64)
-    lse = np.zeros((batch, num_q_heads), dtype=np.float64)
+        so = np.zeros((1, n, G, HEAD_DIM))
+        sl = np.zeros((1, n, G))
+    o = np.zeros((batch, n, num_q_heads, HEAD_DIM), dtype=np.float64)
+    lse = np.zeros((batch, n, num_q_heads), dtype=np.float64)
     rc = _load().oracle_combine(_p(pb, ctypes.c_int32), _p(so, ctypes.c_double),
-                                _p(sl, ctypes.c_double), batch, num_q_heads, num_kv_heads,
+                                _p(sl, ctypes.c_double), batch, num_q_heads, num_kv_heads, n,
                                 _p(o, ctypes.c_double), _p(lse, ctypes.c_double))
     if rc:
         raise ValueError(f"oracle_combine failed ({rc})")
+    if q_len is None:
+        return o[:, 0], lse[:, 0]
     return o, lse
 
 

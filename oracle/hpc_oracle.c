@@ -45,6 +45,18 @@
  *     [num_pages][Hkv][64] (per token, per head); FP8 is OCP e4m3fn.
  *   - a request of length 0 has no chunks; its output is 0 and its LSE -inf.
  *
+ * Several new tokens per request (q_len > 1), as in speculative verification:
+ *   [LL] "SGLang Low-Latency Mode: Kernels and Runtime", section "Where the
+ *   Time Goes" (one request verifies six token rows per step), and the Hy3
+ *   section of [VLLM] (an MTP layer for speculative decoding). The pages give
+ *   no masking rule; the reading taken here is the usual causal one:
+ *   - the q_len new tokens are already in the cache and seq_lens counts them;
+ *     new token qi (0-based) sees tokens [0, L - q_len + qi];
+ *   - the task map is the same as for one token (it walks the chunks of L);
+ *     each descriptor computes q_len * G rows, and a new token whose visible
+ *     range misses the descriptor's chunks gets O = 0, LSE = -inf there;
+ *   - q is [B][q_len][Hq][128] and the split buffers [split][q_len][G][128].
+ *
  * Task-map byte layout (all int32; the CUDA planner must reproduce it
  * bit for bit):
  *   [0, 16)                 header, see the OR_H_* slots below
@@ -60,7 +72,8 @@
  *   max_tasks = Hkv * B + 2 * C.
  *
  * A descriptor's split index is its position in the global walk order; the
- * split buffers are [split][G][head_dim] (outputs) and [split][G] (LSE).
+ * split buffers are [split][q_len][G][head_dim] (outputs) and [split][q_len][G]
+ * (LSE).
  */
 #include <math.h>
 #include <stdint.h>
@@ -349,6 +362,7 @@ typedef struct {
     int pt_stride;
     const int32_t* seq_lens;
     int B, Hq, Hkv;
+    int q_len; /* new tokens per request (1 for plain decode); q is [B][q_len][Hq][128] */
 } or_kv;
 
 static double or_elem(const or_kv* kv, const void* cache, const float* scale, long long page,
@@ -364,7 +378,7 @@ static double or_elem(const or_kv* kv, const void* cache, const float* scale, lo
 /* Softmax attention of query row (b, qh) over tokens [t0, t1) of request b,
  * two passes in float64: scores, max, sum of exp, weighted sum of values.
  * Returns -1 if a page id is outside [0, num_pages). */
-static int or_attend(const or_kv* kv, int b, int qh, long long t0, long long t1, double* o,
+static int or_attend(const or_kv* kv, int b, int qi, int qh, long long t0, long long t1, double* o,
                      double* lse) {
     int G = kv->Hq / kv->Hkv;
     int h = qh / G;
@@ -374,12 +388,13 @@ static int or_attend(const or_kv* kv, int b, int qh, long long t0, long long t1,
         return 0;
     }
     double qv[OR_HEAD_DIM];
-    const long long qoff = ((long long)b * kv->Hq + qh) * OR_HEAD_DIM;
+    const long long row = ((long long)b * kv->q_len + qi) * kv->Hq + qh;
+    const long long qoff = row * OR_HEAD_DIM;
     if (kv->q_scale) {
         /* e4m3 query with one scale per (request, query head), the form the fused
          * attention prologue hands to the attention kernel */
         const uint8_t* qrow = (const uint8_t*)kv->q + qoff;
-        const double qs = kv->q_scale[(long long)b * kv->Hq + qh];
+        const double qs = kv->q_scale[row];
         for (int dd = 0; dd < OR_HEAD_DIM; ++dd) qv[dd] = oracle_e4m3_to_f64(qrow[dd]) * qs;
     } else {
         const uint16_t* qrow = (const uint16_t*)kv->q + qoff;
@@ -422,48 +437,65 @@ static int or_attend(const or_kv* kv, int b, int qh, long long t0, long long t1,
     return 0;
 }
 
+/* Causal length of new token qi of request b: it sees tokens [0, L - q_len + qi]
+ * (the cache already holds all q_len new tokens; seq_lens counts them). */
+static long long or_visible(const or_kv* kv, int b, int qi) {
+    long long len = kv->seq_lens[b] > 0 ? kv->seq_lens[b] : 0;
+    long long v = len - kv->q_len + qi + 1;
+    return v < 0 ? 0 : (v > len ? len : v);
+}
+
 static int or_check_kv(const or_kv* kv) {
+    if (kv->q_len < 1) return -1;
     if (kv->B < 1 || kv->Hkv < 1 || kv->Hq < kv->Hkv || kv->Hq % kv->Hkv) return -1;
     if (kv->num_pages < 1 || kv->pt_stride < 1) return -1;
     if (kv->fp8 && (!kv->ks || !kv->vs)) return -1;
     return 0;
 }
 
-/* Full-sequence attention for selected rows. rows holds nrows (b, qh) pairs;
- * rows == NULL means every row in (b, qh) order (nrows must be B * Hq).
- * q is bf16 bits, or e4m3 codes scaled by q_scale[b][qh] when q_scale != NULL.
+/* Full-sequence attention for selected rows. rows holds nrows (b, r) pairs with
+ * r = qi * Hq + qh (new token qi, query head qh); rows == NULL means every row
+ * in (b, qi, qh) order (nrows must be B * q_len * Hq). New token qi attends
+ * causally: to tokens [0, L_b - q_len + qi].
+ * q is bf16 bits, or e4m3 codes scaled by q_scale[b][qi][qh] when q_scale != NULL.
  * Outputs: out_o [nrows][128], out_lse [nrows]. */
 int oracle_attn_rows(const void* q, const float* q_scale, const void* kc, const void* vc,
                      const float* ks, const float* vs, int kv_fp8, int num_pages, const int32_t* pt,
-                     int pt_stride, const int32_t* seq_lens, int B, int Hq, int Hkv, int nrows,
-                     const int32_t* rows, double* out_o, double* out_lse) {
-    or_kv kv = {q, q_scale, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv};
+                     int pt_stride, const int32_t* seq_lens, int B, int Hq, int Hkv, int q_len,
+                     int nrows, const int32_t* rows, double* out_o, double* out_lse) {
+    or_kv kv = {q, q_scale, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv,
+                q_len};
     if (or_check_kv(&kv)) return -1;
-    if (!rows && nrows != B * Hq) return -1;
+    const int R = q_len * Hq; /* query rows per request: (new token, head) */
+    if (!rows && nrows != B * R) return -1;
     int bad = 0;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (int r = 0; r < nrows; ++r) {
-        int b = rows ? rows[2 * r] : r / Hq;
-        int qh = rows ? rows[2 * r + 1] : r % Hq;
-        if (b < 0 || b >= B || qh < 0 || qh >= Hq) {
+        int b = rows ? rows[2 * r] : r / R;
+        int rr = rows ? rows[2 * r + 1] : r % R;
+        if (b < 0 || b >= B || rr < 0 || rr >= R) {
             bad |= 1;
             continue;
         }
-        long long len = seq_lens[b] > 0 ? seq_lens[b] : 0;
-        if (or_attend(&kv, b, qh, 0, len, out_o + (long long)r * OR_HEAD_DIM, out_lse + r)) bad |= 2;
+        int qi = rr / Hq, qh = rr % Hq;
+        if (or_attend(&kv, b, qi, qh, 0, or_visible(&kv, b, qi), out_o + (long long)r * OR_HEAD_DIM,
+                      out_lse + r))
+            bad |= 2;
     }
     return bad ? -4 : 0;
 }
 
 /* Partial outputs of every descriptor of a task map written by oracle_plan /
- * oracle_plan_static: for descriptor s = (h, b, c0, c1) and each j < G the
- * attention of row (b, h*G + j) over tokens [64*c0, min(64*c1, L_b)).
- * Outputs: split_o [total_splits][G][128], split_lse [total_splits][G]. */
+ * oracle_plan_static: for descriptor s = (h, b, c0, c1), each new token qi and
+ * each j < G the attention of row (b, qi, h*G + j) over tokens
+ * [64*c0, min(64*c1, visible length of qi)).
+ * Outputs: split_o [total_splits][q_len][G][128], split_lse [total_splits][q_len][G]. */
 int oracle_attn_splits(const int32_t* plan, const void* q, const float* q_scale, const void* kc,
                        const void* vc, const float* ks, const float* vs, int kv_fp8, int num_pages,
                        const int32_t* pt, int pt_stride, const int32_t* seq_lens, int B, int Hq,
-                       int Hkv, double* split_o, double* split_lse) {
-    or_kv kv = {q, q_scale, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv};
+                       int Hkv, int q_len, double* split_o, double* split_lse) {
+    or_kv kv = {q, q_scale, kc, vc, ks, vs, kv_fp8, num_pages, pt, pt_stride, seq_lens, B, Hq, Hkv,
+                q_len};
     if (or_check_kv(&kv)) return -1;
     if (plan[OR_H_BATCH] != B || plan[OR_H_NUM_KV_HEADS] != Hkv) return -1;
     int G = Hq / Hkv;
@@ -475,42 +507,47 @@ int oracle_attn_splits(const int32_t* plan, const void* q, const float* q_scale,
         const int32_t* t = tasks + i * OR_TASK_INTS;
         if (t[0] < 0) continue;
         int h = t[0], b = t[1], s = t[4];
-        long long len = seq_lens[b] > 0 ? seq_lens[b] : 0;
         long long t0 = (long long)t[2] * OR_CHUNK_TOKENS;
-        long long t1 = (long long)t[3] * OR_CHUNK_TOKENS;
-        if (t1 > len) t1 = len;
-        for (int j = 0; j < G; ++j) {
-            long long row = (long long)s * G + j;
-            if (or_attend(&kv, b, h * G + j, t0, t1, split_o + row * OR_HEAD_DIM, split_lse + row))
-                bad |= 1;
+        for (int qi = 0; qi < q_len; ++qi) {
+            long long t1 = (long long)t[3] * OR_CHUNK_TOKENS;
+            long long len = or_visible(&kv, b, qi);
+            if (t1 > len) t1 = len;
+            for (int j = 0; j < G; ++j) {
+                long long row = ((long long)s * q_len + qi) * G + j;
+                if (or_attend(&kv, b, qi, h * G + j, t0, t1, split_o + row * OR_HEAD_DIM,
+                              split_lse + row))
+                    bad |= 1;
+            }
         }
     }
     return bad ? -4 : 0;
 }
 
-/* Merge of the partials of each (request, query head) under the global softmax:
- * M = max lse_i, w_i = exp(lse_i - M), O = sum w_i o_i / sum w_i,
+/* Merge of the partials of each (request, new token, query head) under the
+ * global softmax: M = max lse_i, w_i = exp(lse_i - M), O = sum w_i o_i / sum w_i,
  * LSE = M + log(sum w_i). Pairs without partials give O = 0, LSE = -inf.
- * Outputs: out_o [B][Hq][128], out_lse [B][Hq]. */
+ * Outputs: out_o [B][q_len][Hq][128], out_lse [B][q_len][Hq]. */
 int oracle_combine(const int32_t* plan, const double* split_o, const double* split_lse, int B,
-                   int Hq, int Hkv, double* out_o, double* out_lse) {
-    if (plan[OR_H_BATCH] != B || plan[OR_H_NUM_KV_HEADS] != Hkv || Hq % Hkv) return -1;
+                   int Hq, int Hkv, int q_len, double* out_o, double* out_lse) {
+    if (plan[OR_H_BATCH] != B || plan[OR_H_NUM_KV_HEADS] != Hkv || Hq % Hkv || q_len < 1) return -1;
     int G = Hq / Hkv;
     or_layout L = or_layout_of(B, Hkv, plan[OR_H_NUM_CTAS]);
     const int32_t* nsplit = plan + L.nsplit;
     const int32_t* split0 = plan + L.split0;
     for (int b = 0; b < B; ++b)
+        for (int qi = 0; qi < q_len; ++qi)
         for (int qh = 0; qh < Hq; ++qh) {
             int h = qh / G, j = qh % G;
             long long p = (long long)h * B + b;
-            double* o = out_o + ((long long)b * Hq + qh) * OR_HEAD_DIM;
-            double* lse = out_lse + (long long)b * Hq + qh;
+            long long orow = ((long long)b * q_len + qi) * Hq + qh;
+            double* o = out_o + orow * OR_HEAD_DIM;
+            double* lse = out_lse + orow;
             for (int dd = 0; dd < OR_HEAD_DIM; ++dd) o[dd] = 0.0;
             int ns = nsplit[p];
             long long s0 = split0[p];
             double M = -INFINITY;
             for (int i = 0; i < ns; ++i) {
-                double v = split_lse[(s0 + i) * G + j];
+                double v = split_lse[((s0 + i) * q_len + qi) * G + j];
                 if (v > M) M = v;
             }
             if (ns == 0 || M == -INFINITY) {
@@ -519,9 +556,10 @@ int oracle_combine(const int32_t* plan, const double* split_o, const double* spl
             }
             double wsum = 0.0;
             for (int i = 0; i < ns; ++i) {
-                double w = exp(split_lse[(s0 + i) * G + j] - M);
+                long long srow = ((s0 + i) * q_len + qi) * G + j;
+                double w = exp(split_lse[srow] - M);
                 wsum += w;
-                const double* oi = split_o + ((s0 + i) * G + j) * OR_HEAD_DIM;
+                const double* oi = split_o + srow * OR_HEAD_DIM;
                 for (int dd = 0; dd < OR_HEAD_DIM; ++dd) o[dd] += w * oi[dd];
             }
             for (int dd = 0; dd < OR_HEAD_DIM; ++dd) o[dd] /= wsum;

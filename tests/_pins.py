@@ -377,3 +377,126 @@ def check_empty_request():
     o, lse = oracle.attn_rows(c)
     assert np.all(o[:8] == 0) and np.all(np.isneginf(lse[:8]))
     assert np.all(np.isfinite(lse[8:]))
+
+
+# ------------------------------------------------------------------ several new tokens per request
+
+def small_case_mt(lens, q_len, hkv=1, hq=8, dtype="bf16", seed=0, pool=None):
+    w = wl.Workload("pin", len(lens), hq, hkv, dtype, seed, lens=list(lens), pool_pages=pool,
+                    q_len=q_len)
+    return wl.to_numpy_case(wl.make_case(w, device="cpu"))
+
+
+def check_multitoken_vs_sdpa(case, tol=1e-12):
+    """Rows of a q_len > 1 case against torch's float64 scaled_dot_product_attention
+    with an explicit boolean mask: new token qi of request b may attend to key t
+    iff t <= L_b - q_len + qi (the new tokens are the last q_len of the cache)."""
+    B, Q, Hq, _ = case["q"].shape
+    Hkv = case["k_cache"].shape[2]
+    G = Hq // Hkv
+    o, lse = oracle.attn_rows(case)
+    o = o.reshape(B, Q, Hq, 128)
+    lse = lse.reshape(B, Q, Hq)
+    q64 = torch.from_numpy(case["q"].view(np.int16)).view(torch.bfloat16).to(torch.float64)
+    for b in range(B):
+        L = int(case["seq_lens"][b])
+        if L <= 0:
+            assert np.all(o[b] == 0) and np.all(np.isneginf(lse[b]))
+            continue
+        allowed = torch.arange(L)[None, :] <= (L - Q + torch.arange(Q))[:, None]  # [Q, L]
+        for kh in range(Hkv):
+            K, V = dense_kv(case, b, kh)
+            for qi in range(Q):
+                qg = q64[b, qi, kh * G:(kh + 1) * G]
+                got_o = o[b, qi, kh * G:(kh + 1) * G]
+                got_l = lse[b, qi, kh * G:(kh + 1) * G]
+                if not bool(allowed[qi].any()):
+                    assert np.all(got_o == 0) and np.all(np.isneginf(got_l)), (b, qi)
+                    continue
+                mask = allowed[qi][None, None, None, :].expand(1, G, 1, L)
+                ref = torch.nn.functional.scaled_dot_product_attention(
+                    qg[None, :, None, :], K[None, None].expand(1, G, -1, -1),
+                    V[None, None].expand(1, G, -1, -1), attn_mask=mask,
+                    scale=1 / math.sqrt(128))[0, :, 0]
+                sc = (qg @ K.T / math.sqrt(128)).masked_fill(~allowed[qi][None, :], float("-inf"))
+                ref_lse = torch.logsumexp(sc, dim=-1)
+                assert np.allclose(got_o, ref.numpy(), rtol=0, atol=tol), (b, qi, kh)
+                assert np.allclose(got_l, ref_lse.numpy(), rtol=0, atol=tol), (b, qi, kh)
+
+
+def check_multitoken_is_prefix_decode(case):
+    """New token qi with q_len new tokens equals one-token decode of the same
+    query over the first L - q_len + qi + 1 tokens (a shorter seq_lens)."""
+    B, Q, Hq, _ = case["q"].shape
+    o, lse = oracle.attn_rows(case)
+    o = o.reshape(B, Q, Hq, 128)
+    lse = lse.reshape(B, Q, Hq)
+    for qi in range(Q):
+        one = dict(case)
+        one["q"] = np.ascontiguousarray(case["q"][:, qi])
+        one["seq_lens"] = np.maximum(case["seq_lens"] - Q + qi + 1, 0).astype(np.int32)
+        o1, l1 = oracle.attn_rows(one)
+        assert np.array_equal(o1.reshape(B, Hq, 128), o[:, qi]), qi
+        assert np.array_equal(l1.reshape(B, Hq), lse[:, qi]), qi
+
+
+def check_multitoken_combine_equals_full(case, C, m, tol=1e-12):
+    """Partials over a task map's ranges, merged per (request, new token, head),
+    equal the unsplit causal softmax; tokens whose visible range ends before a
+    descriptor's chunks contribute an empty partial there."""
+    B, Q, Hq, _ = case["q"].shape
+    Hkv = case["k_cache"].shape[2]
+    pb = oracle.plan(case["seq_lens"], Hkv, C, m)
+    so, sl = oracle.attn_splits(pb, case)
+    assert so.shape[1:] == (Q, Hq // Hkv, 128)
+    o, lse = oracle.combine(pb, so, sl, B, Hq, Hkv, q_len=Q)
+    fo, fl = oracle.attn_rows(case)
+    fo = fo.reshape(B, Q, Hq, 128)
+    fl = fl.reshape(B, Q, Hq)
+    assert np.allclose(o, fo, rtol=0, atol=tol), np.abs(o - fo).max()
+    fin = np.isfinite(fl)
+    assert np.array_equal(fin, np.isfinite(lse))
+    assert np.allclose(lse[fin], fl[fin], rtol=0, atol=tol)
+    return pb, so, sl
+
+
+def check_multitoken_split_ranges(case, C, m):
+    """A partial of new token qi is plain attention over its descriptor's
+    tokens clipped to qi's visible range (a sub-request cut from the page table)."""
+    B, Q, Hq, _ = case["q"].shape
+    Hkv = case["k_cache"].shape[2]
+    G = Hq // Hkv
+    pb = oracle.plan(case["seq_lens"], Hkv, C, m)
+    so, sl = oracle.attn_splits(pb, case)
+    for lst in oracle.parse_plan(pb)["lists"]:
+        for (kh, b, c0, c1, s, _, _, _) in lst:
+            L = int(case["seq_lens"][b])
+            for qi in range(Q):
+                vis = max(L - Q + qi + 1, 0)
+                n = min(64 * c1, vis) - 64 * c0
+                if n <= 0:
+                    assert np.all(so[s, qi] == 0) and np.all(np.isneginf(sl[s, qi]))
+                    continue
+                sub = dict(case)
+                sub["page_table"] = np.ascontiguousarray(case["page_table"][b:b + 1, c0:c1])
+                sub["seq_lens"] = np.array([n], dtype=np.int32)
+                sub["q"] = np.ascontiguousarray(case["q"][b:b + 1, qi])
+                o, lse = oracle.attn_rows(sub, [(0, kh * G + j) for j in range(G)])
+                assert np.array_equal(o, so[s, qi]) and np.array_equal(lse, sl[s, qi]), (s, qi)
+
+
+def check_multitoken_short_requests():
+    """L < q_len: the first q_len - L new tokens see nothing (O = 0, LSE = -inf);
+    q_len = 1 reproduces the one-token layout."""
+    c = small_case_mt([0, 2, 5, 70], 4, seed=21)
+    o, lse = oracle.attn_rows(c)
+    o = o.reshape(4, 4, 8, 128)
+    lse = lse.reshape(4, 4, 8)
+    assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isneginf(lse[1, :2])) and np.all(np.isfinite(lse[1, 2:]))
+    assert np.all(np.isfinite(lse[2:]))
+    # L = 2, last new token: two keys; the first of the two new tokens sees only key 0
+    K, V = dense_kv(c, 1, 0)
+    assert np.allclose(o[1, 2], V[0].numpy()[None].repeat(8, 0), rtol=0, atol=0)
+    one = small_case_mt([37, 300], 1, seed=22)
+    assert one["q"].ndim == 3

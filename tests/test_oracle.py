@@ -110,3 +110,37 @@ def test_single_chunk_is_plain_attention():
     o, lse = oracle.attn_rows(case)
     assert so.shape[0] == 1
     assert np.array_equal(so[0], o) and np.array_equal(sl[0], lse)
+
+
+# ------------------------------------------------------------------ several new tokens per request
+
+@pytest.mark.parametrize("q_len", [2, 3, 6])
+def test_multitoken_matches_masked_sdpa(q_len):
+    case = pins.small_case_mt([1, 5, 63, 64, 65, 66, 130, 333], q_len, hkv=2, hq=16, seed=20 + q_len)
+    pins.check_multitoken_vs_sdpa(case)
+
+
+def test_multitoken_fp8_matches_masked_sdpa():
+    case = pins.small_case_mt([3, 64, 65, 200], 4, hkv=1, hq=8, dtype="fp8", seed=30)
+    pins.check_multitoken_vs_sdpa(case)
+
+
+def test_multitoken_is_prefix_decode():
+    case = pins.small_case_mt([6, 64, 65, 129, 1000], 6, hkv=2, hq=16, seed=31)
+    pins.check_multitoken_is_prefix_decode(case)
+
+
+@pytest.mark.parametrize("C,m", [(1, 0), (5, 1), (16, 2)])
+@pytest.mark.parametrize("q_len", [2, 6])
+def test_multitoken_combine_of_splits_equals_unsplit(C, m, q_len):
+    case = pins.small_case_mt([37, 64, 65, 128, 129, 300, 1000, 0, 3], q_len, hkv=2, hq=16, seed=32)
+    pins.check_multitoken_combine_equals_full(case, C, m)
+
+
+def test_multitoken_split_ranges():
+    case = pins.small_case_mt([65, 66, 128, 300], 3, hkv=1, hq=8, seed=33)
+    pins.check_multitoken_split_ranges(case, 9, 1)
+
+
+def test_multitoken_short_requests():
+    pins.check_multitoken_short_requests()

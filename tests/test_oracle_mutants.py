@@ -49,6 +49,14 @@ MUTANTS = {
     "norm_weight_dropped": ("x[d] = x[d] * inv * (double)w[d];", "x[d] = x[d] * inv;"),
     "norm_sum_not_mean": ("1.0 / sqrt(ss / OR_HEAD_DIM + eps)", "1.0 / sqrt(ss + eps)"),
     "k_uses_q_weight": ("const float* w = j < Hq ? qw : kw;", "const float* w = qw;"),
+    "causal_off_by_one": ("long long v = len - kv->q_len + qi + 1;", "long long v = len - kv->q_len + qi;"),
+    "causal_reversed": ("long long v = len - kv->q_len + qi + 1;", "long long v = len - qi;"),
+    "query_row_ignores_token": ("const long long row = ((long long)b * kv->q_len + qi) * kv->Hq + qh;",
+                                "const long long row = (long long)b * kv->Hq + qh;"),
+    "split_rows_token_major": ("long long row = ((long long)s * q_len + qi) * G + j;",
+                               "long long row = ((long long)qi * plan[OR_H_TOTAL_SPLITS] + s) * G + j;"),
+    "combine_reads_token_zero": ("long long srow = ((s0 + i) * q_len + qi) * G + j;",
+                                 "long long srow = (s0 + i) * q_len * G + j;"),
 }
 
 
@@ -57,6 +65,7 @@ def _all_pins():
     case_f8 = pins.small_case([1, 65, 333], hkv=2, hq=16, dtype="fp8", seed=11)
     case_cb = pins.small_case([37, 128, 300, 1000, 0, 5], hkv=2, hq=16, seed=12)
     case_q8 = pins.small_case([1, 65, 333], hkv=2, hq=16, dtype="fp8", seed=15, q_dtype="fp8")
+    case_mt = pins.small_case_mt([2, 65, 66, 200], 3, hkv=2, hq=16, seed=23)
     return [
         pins.check_e4m3_closed_forms,
         pins.check_golden_dynamic,
@@ -73,6 +82,9 @@ def _all_pins():
         pp.check_norm_at_position_zero,
         pp.check_rotation_keeps_pair_norms,
         pp.check_relative_position,
+        lambda: pins.check_multitoken_vs_sdpa(case_mt),
+        lambda: pins.check_multitoken_combine_equals_full(case_mt, 5, 1),
+        pins.check_multitoken_short_requests,
         pins.check_plan_bruteforce_tiny,
     ]
 
