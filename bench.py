@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches only")
     ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue timing")
+    ap.add_argument("--no-multi-token", action="store_true", help="skip the q_len > 1 timings")
     return ap.parse_args()
 
 
@@ -91,11 +92,12 @@ def step_bytes(lens, w, n_splits):
     read once)."""
     from load_balanced_paged_02_gb300 import workloads as wl
     kv = wl.kv_bytes(lens, w.num_kv_heads, w.kv_dtype)
-    q = len(lens) * w.num_q_heads * ((128 + 4) if w.q_dtype == "fp8" else 256)
-    part = n_splits * 8 * 129 * 4
+    rows = len(lens) * w.q_len * w.num_q_heads
+    q = rows * ((128 + 4) if w.q_dtype == "fp8" else 256)
+    part = n_splits * w.q_len * 8 * 129 * 4
     pages = int(wl.chunk_counts(lens).sum()) * 4
     return dict(kv=kv, q=q, partials_rw=2 * part, metric=kv + q + 2 * part,
-                attn=kv + q + part + pages, out=len(lens) * w.num_q_heads * 128 * 2)
+                attn=kv + q + part + pages, out=rows * 128 * 2)
 
 
 class ClockSampler:
@@ -206,9 +208,9 @@ def oracle_sample(case, w, seconds, seed=99):
     import oracle
     from load_balanced_paged_02_gb300 import workloads as wl
     lens = np.maximum(case["seq_lens"].cpu().numpy().astype(np.int64), 0)
-    total = float(lens.sum()) * w.num_q_heads
+    Hq = w.num_q_heads * w.q_len  # rows per request: (new token, query head)
+    total = float(lens.sum()) * Hq
     order = [int(b) for b in np.random.default_rng(seed).permutation(len(lens)) if lens[b] > 0]
-    Hq = w.num_q_heads
     spent, done, rows_done, k = 0.0, 0.0, 0, 0
     hosts = {}
     if total <= 4e6:
@@ -238,7 +240,8 @@ def oracle_sample(case, w, seconds, seed=99):
         done += float(lens[b]) * nh
         rows_done += nh
     full = spent * total / max(done, 1.0)
-    text = (f"{rows_done} (request, query head) rows covering {int(done)} token-head pairs "
+    text = (f"{rows_done} (request, query head{', new token' if w.q_len > 1 else ''}) rows covering "
+            f"{int(done)} token-row pairs "
             f"({done / total:.2f} x the batch's {int(total)}), {spent:.1f} s of oracle time, "
             f"rate scaled to one whole batch")
     return full, oracle.num_threads(), text
@@ -297,6 +300,69 @@ def prologue_timing(w, dev, n_rep=200):
 
 # ---------------------------------------------------------------- arms
 
+def multi_token_timing(w, case, plan, C, dev, q_lens=(2, 6), n_rep=100):
+    """Attention + combine for q_len new tokens per request (causal verify rows)
+    on the workload's own batch, cache and task map, replayed from a CUDA
+    graph. Bytes: live K/V, the q_len query rows, the partials written and the
+    page ids (the attention kernel's algorithmic bytes)."""
+    import torch
+    from dataclasses import replace
+    from load_balanced_paged_02_gb300 import binding as hb
+    peak, _ = measured_peaks()
+    lens = case["seq_lens"].cpu().numpy()
+    n_splits = int(plan.buf[3].item())
+    Hkv = w.num_kv_heads
+    res = {}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    for Q in q_lens:
+        wq = replace(w, q_len=Q)
+        q = torch.randn((w.batch, Q, w.num_q_heads, 128), generator=gen, device=dev).to(torch.bfloat16)
+        so, sl = hb.split_buffers(plan, q_len=Q)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+
+        def layer():
+            hb.hpc_decode_attn(q, case["k_cache"], case["v_cache"], case["page_table"], case["seq_lens"], plan,
+                               so, sl, case["k_scale"], case["v_scale"], num_pages=case["num_pages"])
+            hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+        for _ in range(3):
+            layer()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer()
+        g.replay()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_rep)]
+        for e in ev:  # eager, per-kernel events
+            e[0].record(st)
+            hb.hpc_decode_attn(q, case["k_cache"], case["v_cache"], case["page_table"], case["seq_lens"], plan,
+                               so, sl, case["k_scale"], case["v_scale"], num_pages=case["num_pages"])
+            e[1].record(st)
+            hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+            e[2].record(st)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(n_rep):
+            g.replay()
+        b.record(st)
+        torch.cuda.synchronize()
+        attn_us = 1e3 * float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+        comb_us = 1e3 * float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+        layer_us = 1e3 * a.elapsed_time(b) / n_rep
+        byt = step_bytes(lens, wq, n_splits)
+        gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
+        flops = 4.0 * float(np.maximum(lens, 0).sum()) * w.num_q_heads * Q * 128  # QK^T and PV
+        res[f"q_len_{Q}"] = {"attn_us": attn_us, "combine_us": comb_us, "layer_graph_us": layer_us,
+                             "attn_gbs": gbs, "frac_of_peak": gbs / peak,
+                             "mma_tflops": flops / (attn_us * 1e-6) / 1e12,
+                             "algorithmic_bytes_per_launch": byt["attn"]}
+        del so, sl, out, lse, q, g
+    return res
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -353,9 +419,9 @@ def run_ours(args):
 
     plan = hb.Plan(w.batch, Hkv, C, dev)
     hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
-    so, sl = hb.split_buffers(plan)
+    so, sl = hb.split_buffers(plan, q_len=w.q_len)
     out = torch.empty(case["q"].shape, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(case["q"].shape[:2], dtype=torch.float32, device=dev)
+    lse = torch.empty(case["q"].shape[:-1], dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
     n_splits = int(plan.buf[3].item())
     byt = step_bytes(lens, w, n_splits)
@@ -479,7 +545,7 @@ def run_ours(args):
     # ---- static split-KV schedule of the same kernel (comparison)
     if not args.no_static and rank == 0:
         splan = hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits)
-        sso, ssl = hb.split_buffers(splan)
+        sso, ssl = hb.split_buffers(splan, q_len=w.q_len)
         n_static = max(10, args.steps // 3)
 
         def sstep():
@@ -515,7 +581,9 @@ def run_ours(args):
     # ---- end to end through the C ABI with host buffers (bf16 query path)
     if not args.no_e2e and case["q_scale"] is not None and rank == 0:
         result["e2e"] = {"unavailable": "hpc_decode_step_host takes a bf16 query"}
-    if not args.no_e2e and case["q_scale"] is None:
+    if not args.no_e2e and w.q_len > 1 and rank == 0:
+        result["e2e"] = {"unavailable": "hpc_decode_step_host takes one new token per request"}
+    if not args.no_e2e and case["q_scale"] is None and w.q_len == 1:
         B, Hq, D = case["q"].shape
         h_q = case["q"].cpu().pin_memory()
         h_sl = case["seq_lens"].cpu().pin_memory()
@@ -549,6 +617,10 @@ def run_ours(args):
     # ---- the fused prologue that feeds this path (NEXT-1), for context
     if rank == 0 and not args.no_prologue:
         result["prologue"] = prologue_timing(w, dev)
+
+    # ---- several new tokens per request on the same batch and cache (NEXT-4)
+    if rank == 0 and not args.no_multi_token and w.q_len == 1 and w.q_dtype == "bf16":
+        result["multi_token"] = multi_token_timing(w, case, plan, C, dev)
 
     # ---- CPU oracle baseline (rank 0 only, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -10,6 +10,8 @@
  *          Tencent Hunyuan", sub-section "解决方案：按步负载均衡的 decode
  *          调度器" (assign -> compute and combine), and "关于 Hy3 系列模型的
  *          简要说明" (GQA shape: 64 query heads, 8 KV heads, head dim 128).
+ *   [LL]   "SGLang Low-Latency Mode: Kernels and Runtime", section "Where the
+ *          Time Goes" (several verified token rows per request and step).
  *
  * One decode step is three calls on one stream:
  *   hpc_decode_plan     once per step: live lengths -> task map (reused by
@@ -87,6 +89,7 @@ typedef enum hpc_kv_dtype { HPC_KV_BF16 = 0, HPC_KV_FP8_E4M3 = 1 } hpc_kv_dtype;
 #define HPC_MAX_BATCH 16384
 #define HPC_MAX_KV_HEADS 256
 #define HPC_MAX_CTAS (1 << 22)
+#define HPC_MAX_Q_LEN 8          /* new tokens per request in hpc_decode_attn_multi */
 
 /*
  * Task map ([SGL] "Scheduling around live KV work": a global task map built
@@ -206,6 +209,33 @@ hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* 
                               float* split_o, float* split_lse, void* stream);
 
 /*
+ * Persistent decode attention for q_len new tokens per request, the rows that
+ * speculative decoding verifies in one step ([LL] "SGLang Low-Latency Mode:
+ * Kernels and Runtime", section "Where the Time Goes": six token rows per
+ * step; [VLLM] Hy3: an MTP layer for speculative decoding). Same task map,
+ * caches and errors as hpc_decode_attn; the plan does not depend on q_len.
+ * The pages give no mask; the causal reading is taken: the q_len new tokens
+ * are already in the cache and counted by seq_lens, and new token i of
+ * request b attends to tokens [0, seq_lens[b] - q_len + i]. For descriptor
+ * (h, b, c0, c1, s), new token i and j < 8 it writes row (s * q_len + i) * 8 + j:
+ *   split_o[.][:]  = normalised attention of q[b][i][8h+j] over tokens
+ *                    [64*c0, min(64*c1, seq_lens[b] - q_len + i + 1))
+ *   split_lse[.]   = its natural-log LSE (-inf and 0 outputs when empty)
+ *   q          device bf16 [batch][q_len][num_q_heads][128], 16-byte aligned
+ *   q_len      1 <= q_len <= HPC_MAX_Q_LEN (1 runs hpc_decode_attn's kernel)
+ *   split_o    device float32 [split_capacity][q_len][8][128]
+ *   split_lse  device float32 [split_capacity][q_len][8]
+ * Errors: HPC_ERR_INVALID_ARG (also q_len out of range), HPC_ERR_UNSUPPORTED,
+ * HPC_ERR_CUDA.
+ */
+hpc_status hpc_decode_attn_multi(const void* q, int q_len, const void* k_cache, const void* v_cache,
+                                 const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
+                                 const int32_t* page_table, int page_table_stride,
+                                 const int32_t* seq_lens, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
+                                 float* split_o, float* split_lse, void* stream);
+
+/*
  * Combine ([SGL] the paragraph on execution; [VLLM] combine stage). For every
  * (request b, query head qh) with h = qh / 8, j = qh % 8 and the pair's
  * n = pair_nsplit[h*batch+b] partials starting at s0 = pair_split0[...]:
@@ -218,6 +248,18 @@ hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* 
 hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse,
                               void* out, float* out_lse, int batch, int num_q_heads,
                               int num_kv_heads, int head_dim, void* stream);
+
+/*
+ * Combine for q_len new tokens per request (the partials of
+ * hpc_decode_attn_multi): the same merge for every (b, i, qh), reading the
+ * partial rows (s * q_len + i) * 8 + qh % 8 of the pair's splits.
+ *   out       device bf16 [batch][q_len][num_q_heads][128], 8-byte aligned
+ *   out_lse   device float32 [batch][q_len][num_q_heads] or NULL
+ * q_len == 1 is hpc_decode_combine.
+ */
+hpc_status hpc_decode_combine_multi(const hpc_plan* plan, int q_len, const float* split_o,
+                                    const float* split_lse, void* out, float* out_lse, int batch,
+                                    int num_q_heads, int num_kv_heads, int head_dim, void* stream);
 
 /*
  * Fused attention prologue, HpcRopeNorm ([SGL] "A fused attention prologue";

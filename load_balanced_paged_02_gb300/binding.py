@@ -53,7 +53,10 @@ SIGNATURES = {
                              _vp, _vp, _vp]),
     "hpc_decode_attn_q8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _P,
                                 _vp, _vp, _vp]),
+    "hpc_decode_attn_multi": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                                   _P, _vp, _vp, _vp]),
     "hpc_decode_combine": (_i, [_P, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "hpc_decode_combine_multi": (_i, [_P, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "hpc_rope_norm": (_i, [_vp, _vp, _vp, _i, _vp, _vp, ctypes.c_float, _vp, _i, _i, _i, _i, _i, _vp, _vp,
                            _vp, _vp, _vp, _vp, _i, _i, _vp, _vp]),
     "hpc_decode_step_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
@@ -189,21 +192,26 @@ def hpc_decode_plan_static(seq_lens: torch.Tensor, num_kv_heads: int, num_splits
     return plan
 
 
-def split_buffers(plan: Plan, device=None):
-    """Allocate split_o [capacity, 8, 128] and split_lse [capacity, 8] (float32)."""
+def split_buffers(plan: Plan, device=None, q_len: int = 1):
+    """Allocate split_o [capacity, 8, 128] and split_lse [capacity, 8] (float32);
+    with q_len > 1, [capacity, q_len, 8, 128] and [capacity, q_len, 8]."""
     device = device or plan.buf.device
     cap = plan.split_capacity
-    return (torch.empty((cap, GROUP, HEAD_DIM), dtype=torch.float32, device=device),
-            torch.empty((cap, GROUP), dtype=torch.float32, device=device))
+    rows = (cap, GROUP) if q_len == 1 else (cap, q_len, GROUP)
+    return (torch.empty(rows + (HEAD_DIM,), dtype=torch.float32, device=device),
+            torch.empty(rows, dtype=torch.float32, device=device))
 
 
 def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split_o, split_lse,
                     k_scale=None, v_scale=None, num_pages: int | None = None, stream=None,
                     q_scale=None):
     """Persistent attention over the task map; writes split_o / split_lse.
-    A float8_e4m3fn q with its q_scale [B, Hq] goes to hpc_decode_attn_q8."""
+    A float8_e4m3fn q with its q_scale [B, Hq] goes to hpc_decode_attn_q8; a
+    bf16 q of shape [B, q_len, Hq, 128] (several new tokens per request, causal)
+    goes to hpc_decode_attn_multi."""
     kvd = kv_dtype_of(k_cache)
-    B, Hq, D = q.shape
+    q_len = q.shape[1] if q.dim() == 4 else 1
+    B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
     Hkv = k_cache.shape[2]
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (split_o, "split_o"),
                  (split_lse, "split_lse")):
@@ -211,8 +219,9 @@ def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split
             raise HpcError(n, detail="must be a contiguous CUDA tensor")
     _cuda_i32(page_table, "page_table")
     _cuda_i32(seq_lens, "seq_lens")
-    if split_o.shape[0] < plan.split_capacity or split_lse.shape[0] < plan.split_capacity:
-        raise HpcError("split buffers", detail=f"need {plan.split_capacity} rows")
+    need = plan.split_capacity * q_len * GROUP
+    if split_o.numel() < need * HEAD_DIM or split_lse.numel() < need:
+        raise HpcError("split buffers", detail=f"need {plan.split_capacity} x {q_len} x 8 rows")
     npages = int(num_pages if num_pages is not None else k_cache.shape[0])
     if q.dtype in (torch.float8_e4m3fn, torch.uint8):
         if q_scale is None:
@@ -223,6 +232,13 @@ def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split
             int(k_cache.shape[1]), plan.ref(), _ptr(split_o), _ptr(split_lse), _stream(stream))
         _check("hpc_decode_attn_q8", rc)
         return
+    if q.dim() == 4:
+        rc = lib().hpc_decode_attn_multi(
+            _ptr(q), q_len, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd, npages,
+            _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D, int(k_cache.shape[1]),
+            plan.ref(), _ptr(split_o), _ptr(split_lse), _stream(stream))
+        _check("hpc_decode_attn_multi", rc)
+        return
     rc = lib().hpc_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd, npages, _ptr(page_table),
         int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D, int(k_cache.shape[1]), plan.ref(),
@@ -232,9 +248,15 @@ def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split
 
 def hpc_decode_combine(plan: Plan, split_o, split_lse, out, out_lse=None, num_kv_heads=None,
                        stream=None):
-    """LSE-weighted merge of the partials into out (bf16) and out_lse (float32)."""
-    B, Hq, D = out.shape
+    """LSE-weighted merge of the partials into out (bf16) and out_lse (float32).
+    A 4-D out [B, q_len, Hq, 128] merges the partials of hpc_decode_attn_multi."""
+    B, Hq, D = out.shape[0], out.shape[-2], out.shape[-1]
     Hkv = num_kv_heads if num_kv_heads is not None else Hq // GROUP
+    if out.dim() == 4:
+        rc = lib().hpc_decode_combine_multi(plan.ref(), int(out.shape[1]), _ptr(split_o), _ptr(split_lse),
+                                            _ptr(out), _ptr(out_lse), B, Hq, Hkv, D, _stream(stream))
+        _check("hpc_decode_combine_multi", rc)
+        return
     rc = lib().hpc_decode_combine(plan.ref(), _ptr(split_o), _ptr(split_lse), _ptr(out),
                                   _ptr(out_lse), B, Hq, Hkv, D, _stream(stream))
     _check("hpc_decode_combine", rc)
@@ -251,11 +273,11 @@ def decode(q, k_cache, v_cache, page_table, seq_lens, k_scale=None, v_scale=None
         if num_ctas is None:
             num_ctas = default_num_ctas(kv_dtype_of(k_cache))
         plan = hpc_decode_plan(seq_lens, Hkv, num_ctas, min_chunks_per_cta, stream=stream)
-    so, sl = split_buffers(plan)
+    so, sl = split_buffers(plan, q_len=q.shape[1] if q.dim() == 4 else 1)
     hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan, so, sl, k_scale, v_scale,
                     stream=stream, q_scale=q_scale)
     out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
     hpc_decode_combine(plan, so, sl, out, lse, Hkv, stream=stream)
     return out, lse, plan
 

@@ -119,12 +119,13 @@ hpc_status hpc_decode_plan_static(const int32_t* d_seq_lens, int batch, int num_
 
 namespace {
 
-// Shared by hpc_decode_attn (bf16 Q) and hpc_decode_attn_q8 (e4m3 Q + scales).
+// Shared by hpc_decode_attn (bf16 Q), hpc_decode_attn_q8 (e4m3 Q + scales)
+// and hpc_decode_attn_multi (q_len bf16 query rows per request).
 hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache, const void* v_cache,
                        const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
                        const int32_t* page_table, int page_table_stride, const int32_t* seq_lens, int batch,
                        int num_q_heads, int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
-                       float* split_o, float* split_lse, void* stream) {
+                       float* split_o, float* split_lse, void* stream, int q_len = 1) {
     hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
     if (st != HPC_OK) return st;
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
@@ -140,6 +141,7 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     if (fp8 && (long long)num_pages * num_kv_heads > 2147483647LL) return HPC_ERR_INVALID_ARG;
     if (q_scale && (!fp8 || !aligned(q_scale, 16))) return fp8 ? HPC_ERR_INVALID_ARG : HPC_ERR_UNSUPPORTED;
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN || (q_len > 1 && q_scale)) return HPC_ERR_INVALID_ARG;
     AttnArgs a;
     a.q = q;
     a.q_scale = q_scale;
@@ -161,7 +163,8 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     a.split_cap = (long long)hpc_decode_split_capacity(batch, num_kv_heads, plan->num_ctas);
     a.split_o = split_o;
     a.split_lse = split_lse;
-    cudaError_t e = launch_attn(a, static_cast<cudaStream_t>(stream));
+    cudaError_t e = q_len == 1 ? launch_attn(a, static_cast<cudaStream_t>(stream))
+                               : launch_attn_mt(a, q_len, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue) return HPC_ERR_INVALID_ARG;
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
@@ -191,17 +194,36 @@ hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* 
                        split_o, split_lse, stream);
 }
 
-hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse, void* out,
-                              float* out_lse, int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                              void* stream) {
+hpc_status hpc_decode_attn_multi(const void* q, int q_len, const void* k_cache, const void* v_cache,
+                                 const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
+                                 const int32_t* page_table, int page_table_stride, const int32_t* seq_lens,
+                                 int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                 const hpc_plan* plan, float* split_o, float* split_lse, void* stream) {
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN) return HPC_ERR_INVALID_ARG;
+    return attn_common(q, nullptr, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
+                       page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
+                       split_o, split_lse, stream, q_len);
+}
+
+hpc_status hpc_decode_combine_multi(const hpc_plan* plan, int q_len, const float* split_o, const float* split_lse,
+                                    void* out, float* out_lse, int batch, int num_q_heads, int num_kv_heads,
+                                    int head_dim, void* stream) {
     hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, kChunk);
     if (st != HPC_OK) return st;
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN) return HPC_ERR_INVALID_ARG;
     if (!split_o || !split_lse || !out || !aligned(split_o, 16) || !aligned(out, 8)) return HPC_ERR_INVALID_ARG;
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     cudaError_t e = launch_combine(plan->buf, plan->num_ctas, split_o, split_lse,
                                    static_cast<__nv_bfloat16*>(out), out_lse, batch, num_q_heads, num_kv_heads,
-                                   static_cast<cudaStream_t>(stream));
+                                   q_len, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+hpc_status hpc_decode_combine(const hpc_plan* plan, const float* split_o, const float* split_lse, void* out,
+                              float* out_lse, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                              void* stream) {
+    return hpc_decode_combine_multi(plan, 1, split_o, split_lse, out, out_lse, batch, num_q_heads, num_kv_heads,
+                                    head_dim, stream);
 }
 
 hpc_status hpc_rope_norm(const void* qkv, const int32_t* positions, const float* cos_sin, int max_pos,

@@ -1,0 +1,311 @@
+// Pieces shared by the decode attention kernels (attn.cu: one new token per
+// request; attn_mt.cu: several new tokens per request): launch parameters,
+// bounded mbarrier waits, query fragment loads, the online-softmax step, the
+// V tail fill and the producer warp that streams K/V pages with TMA.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "hpc_internal.cuh"
+
+namespace hpc {
+namespace attn {
+
+constexpr int kScratchStride = 132;  // floats per (query) merge row
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <bool FP8>
+struct KvCfg;
+template <>
+struct KvCfg<false> {
+    static constexpr int kStageBytes = 32768;  // K dims 0-63 | K 64-127 | V 0-63 | V 64-127
+    static constexpr uint32_t kTxBytes = 32768;
+    static constexpr float kPScale = 1.0f;
+};
+template <>
+struct KvCfg<true> {
+    static constexpr int kStageBytes = 17408;  // K 8 KB | V 8 KB | K scales 256 B | V scales 256 B
+    static constexpr uint32_t kTxBytes = 16384 + 512;
+    static constexpr float kPScale = 256.0f;
+};
+
+struct Params {
+    const __nv_bfloat16* q;
+    const uint8_t* q8;      // e4m3 query codes (QF8 instances)
+    const float* q_scale;   // one float32 scale per (request, query head) (QF8 instances)
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* page_table;
+    long long pt_stride;
+    const int32_t* seq_lens;
+    int batch, num_q_heads, num_kv_heads, num_pages;
+    int q_len;              // new tokens per request (multi-token instances; 1 otherwise)
+    const int32_t* cta_off;
+    const int32_t* tasks;
+    int* err;
+    long long split_cap;
+    float* split_o;
+    float* split_lse;
+    float scale_log2;
+};
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool desc_ok(const Params& p, int h, int b, int c0, int c1, int s) {
+    return h < p.num_kv_heads && b >= 0 && b < p.batch && c0 >= 0 && c1 > c0 && c1 <= p.pt_stride &&
+           s >= 0 && s < p.split_cap;
+}
+
+// ------------------------------------------------------------------ consumer math
+
+template <bool FP8, bool QF8>
+__device__ __forceinline__ void load_q_frags(uint32_t qbase, int lane, uint32_t (&qf)[8][2]) {
+    if constexpr (QF8) {
+        // e4m3 Q codes, rows of 128 bytes: thread (g, c) takes bytes [32c, 32c+32)
+        // of query g; k-step ks (32 dims) uses words 2ks and 2ks+1 of that slice,
+        // matching the K words the same thread reads (see chunk_compute).
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t base = qbase + (uint32_t)g * 128u + (uint32_t)c * 32u;
+        const uint4 v0 = lds128(base), v1 = lds128(base + 16u);
+        qf[0][0] = v0.x;
+        qf[0][1] = v0.y;
+        qf[1][0] = v0.z;
+        qf[1][1] = v0.w;
+        qf[2][0] = v1.x;
+        qf[2][1] = v1.y;
+        qf[3][0] = v1.z;
+        qf[3][1] = v1.w;
+#pragma unroll
+        for (int i = 4; i < 8; ++i) qf[i][0] = qf[i][1] = 0u;
+    } else if constexpr (!FP8) {
+        // Q^T B-fragments: rows are the 8 query heads, 16-byte columns are dims.
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+            uint32_t r[4];
+            ldsm_x4(r, qbase + (uint32_t)(lane & 7) * 256u + (uint32_t)(4 * kp + (lane >> 3)) * 16u);
+            qf[2 * kp][0] = r[0];
+            qf[2 * kp][1] = r[1];
+            qf[2 * kp + 1][0] = r[2];
+            qf[2 * kp + 1][1] = r[3];
+        }
+    } else {
+        // Thread (g, c) holds dims [32c, 32c+32) of query g; k-step ks uses
+        // dims 32c+4ks+{0,1} (b0b1) and 32c+4ks+{2,3} (b2b3), widened to f16.
+        const int g = lane >> 2, c = lane & 3;
+        const uint32_t base = qbase + (uint32_t)g * 256u + (uint32_t)c * 64u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = lds128(base + 16u * i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int word = 4 * i + j;  // dims 32c + 2*word, +1
+                __nv_bfloat162 bv = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+                const float2 f = __bfloat1622float2(bv);
+                qf[word >> 1][word & 1] = pack_f16x2(f.x, f.y);
+            }
+        }
+    }
+}
+
+// Online-softmax update of one warp's state with a 16-token x 8-query score
+// tile s (log2 domain, masked entries -inf). Returns P in p.
+__device__ __forceinline__ void softmax_step(float (&s)[4], float (&m)[2], float (&l)[2],
+                                             float (&o)[8][4], float (&p)[4]) {
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
+    const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
+    const float al0 = fast_exp2(m[0] - mu0), al1 = fast_exp2(m[1] - mu1);
+    m[0] = mn0;
+    m[1] = mn1;
+    p[0] = fast_exp2(s[0] - mu0);
+    p[1] = fast_exp2(s[1] - mu1);
+    p[2] = fast_exp2(s[2] - mu0);
+    p[3] = fast_exp2(s[3] - mu1);
+    l[0] = l[0] * al0 + p[0] + p[2];
+    l[1] = l[1] * al1 + p[1] + p[3];
+    // Once a long sequence's running max settles, alpha is 1 for every lane;
+    // skip the rescale of O then (warp-uniform branch).
+    if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i][0] *= al0;
+            o[i][1] *= al1;
+            o[i][2] *= al0;
+            o[i][3] *= al1;
+        }
+    }
+}
+
+// Zero V rows [16*wq + nv, 16*wq + 16) of a stage (tokens past the live length
+// in the last page may hold any bits, and 0 * NaN would poison P V).
+template <bool FP8>
+__device__ __forceinline__ void zero_v_tail(uint8_t* stage, int wq, int nv, int lane) {
+    constexpr int kVecPerRow = FP8 ? 8 : 16;
+    const int n = (16 - nv) * kVecPerRow;
+    for (int i = lane; i < n; i += 32) {
+        const int r = 16 * wq + nv + i / kVecPerRow;
+        const int part = i % kVecPerRow;
+        uint8_t* dst;
+        if constexpr (FP8)
+            dst = stage + 8192 + r * 128 + part * 16;
+        else
+            dst = stage + 16384 + (part >> 3) * 8192 + r * 128 + (part & 7) * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+}
+
+
+
+// How the producer stages the query rows of a descriptor.
+enum class QStage {
+    kBf16,      // one new token: 8 bf16 rows (2 KB)
+    kE4m3,      // one new token: 8 rows of e4m3 codes, then their 8 float32 scales
+    kBf16Rows,  // p.q_len new tokens: p.q_len blocks of 8 bf16 rows
+};
+
+constexpr int kQRowsBytes = kGroup * kHeadDim * 2;  // 8 bf16 query rows
+
+// Producer warp of a decode attention CTA. It walks the CTA's descriptor list;
+// for each descriptor it stages the query rows into a 2-slot ring (qfull /
+// qempty) and then streams every chunk (= page) of K and V, plus the page's
+// two e4m3 scale rows, into the STAGES-deep ring (full / empty) with TMA. The
+// lanes fetch 32 page ids at a time; lane 0 issues the copies. meta[stage]
+// carries the chunk's valid token count (0: skip, page id out of range).
+// Chunk k of the CTA goes to stage k % STAGES. Every wait is bounded; on
+// expiry it raises the abort flag, records HPC_DEVERR_WAIT_TIMEOUT and waits
+// (bounded) for its own copies in flight before returning.
+template <bool FP8, int STAGES, QStage QM>
+__device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                        const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, int list0, int lane,
+                                        uint8_t* smem, uint8_t* qbuf, uint32_t q_slot_bytes, uint64_t* full,
+                                        uint64_t* empty, uint64_t* qfull, uint64_t* qempty, volatile int* meta,
+                                        volatile int* abort_flag) {
+    using Cfg = KvCfg<FP8>;
+    const uint64_t pol = l2_evict_first_policy();
+    uint32_t seq = 0;
+    int qd = 0;
+    bool ok = true;
+    for (int slot = list0; ok; ++slot) {
+        const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
+        const int4 t1 =
+            __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
+        const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
+        if (h < 0) break;
+        if (!desc_ok(p, h, b, c0, c1, t1.x)) {
+            if (lane == 0) atomicOr(p.err, (int)HPC_DEVERR_BAD_DESCRIPTOR);
+            continue;
+        }
+        const int L = __ldg(p.seq_lens + b);
+        const int qs = qd & 1;
+        if (lane == 0) {
+            ok = wait_bounded(&qempty[qs], ((qd >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
+            if (ok) {
+                uint8_t* qdst = qbuf + qs * q_slot_bytes;
+                if constexpr (QM == QStage::kE4m3) {
+                    // 8 rows of 128 e4m3 codes, then their 8 scales
+                    const long long qrow = (long long)b * p.num_q_heads + (long long)h * kGroup;
+                    mbar_arrive_expect_tx(&qfull[qs], kGroup * kHeadDim + kGroup * 4);
+                    bulk_load_nohint(qdst, p.q8 + qrow * kHeadDim, kGroup * kHeadDim, &qfull[qs]);
+                    bulk_load_nohint(qdst + kGroup * kHeadDim, p.q_scale + qrow, kGroup * 4, &qfull[qs]);
+                } else {
+                    // q_len blocks of 8 bf16 rows (2 KB each): new token i of request b,
+                    // query heads [8h, 8h + 8)
+                    const int nq = QM == QStage::kBf16 ? 1 : p.q_len;
+                    mbar_arrive_expect_tx(&qfull[qs], (uint32_t)nq * kQRowsBytes);
+                    for (int i = 0; i < nq; ++i) {
+                        const long long qrow = ((long long)b * nq + i) * p.num_q_heads + (long long)h * kGroup;
+                        bulk_load_nohint(qdst + i * kQRowsBytes, p.q + qrow * kHeadDim, kQRowsBytes, &qfull[qs]);
+                    }
+                }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ++qd;
+        const int32_t* prow = p.page_table + (long long)b * p.pt_stride;
+        for (int cb = c0; cb < c1 && ok; cb += 32) {
+            const int cl = cb + lane;
+            const int pg = cl < c1 ? __ldg(prow + cl) : 0;
+            const int n = min(32, c1 - cb);
+            for (int j = 0; j < n; ++j, ++seq) {
+                const int page = __shfl_sync(0xffffffffu, pg, j);
+                const int cc = cb + j;
+                const int nvalid = min(kChunk, L - kChunk * cc);
+                const bool page_ok = (unsigned)page < (unsigned)p.num_pages;
+                const int st = (int)(seq % STAGES);
+                const uint32_t ph = (seq / STAGES) & 1;
+                if (lane == 0) {
+                    ok = wait_bounded(&empty[st], ph ^ 1, abort_flag, kWaitLimitNs);
+                    if (ok) {
+                        if (!page_ok) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
+                        if (page_ok && nvalid > 0) {
+                            meta[st] = nvalid;
+                            mbar_arrive_expect_tx(&full[st], Cfg::kTxBytes);
+                            uint8_t* sbuf = smem + (size_t)st * Cfg::kStageBytes;
+                            const int tok = page * kChunk;
+                            if constexpr (FP8) {
+                                // The 256-byte scale rows go through 2-D tensor maps: on
+                                // GB300 that measured 6 % faster for the whole kernel than
+                                // plain bulk copies of the same rows. Issued first, so
+                                // they are not the last bytes of the stage to land.
+                                const int srow = page * p.num_kv_heads + h;
+                                tma_load_2d(sbuf + 16384, tm_ks, &full[st], 0, srow, pol);
+                                tma_load_2d(sbuf + 16640, tm_vs, &full[st], 0, srow, pol);
+                                tma_load_3d(sbuf, tm_k, &full[st], 0, h, tok, pol);
+                                tma_load_3d(sbuf + 8192, tm_v, &full[st], 0, h, tok, pol);
+                            } else {
+                                tma_load_3d(sbuf, tm_k, &full[st], 0, h, tok, pol);
+                                tma_load_3d(sbuf + 8192, tm_k, &full[st], 64, h, tok, pol);
+                                tma_load_3d(sbuf + 16384, tm_v, &full[st], 0, h, tok, pol);
+                                tma_load_3d(sbuf + 24576, tm_v, &full[st], 64, h, tok, pol);
+                            }
+                        } else {
+                            meta[st] = 0;
+                            mbar_arrive(&full[st]);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        *abort_flag = 1;
+        atomicOr(p.err, (int)HPC_DEVERR_WAIT_TIMEOUT);
+        // wait (bounded) for the copies this warp may still have in flight
+        const uint32_t first = seq > (uint32_t)STAGES ? seq - STAGES : 0u;
+        for (uint32_t k = first; k < seq; ++k)
+            wait_bounded(&full[k % STAGES], (k / STAGES) & 1, nullptr, kDrainLimitNs);
+        if (qd > 0) wait_bounded(&qfull[(qd - 1) & 1], ((qd - 1) >> 1) & 1, nullptr, kDrainLimitNs);
+    }
+}
+
+}  // namespace attn
+
+// Tensor maps (defined in attn.cu).
+bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int Hkv);
+bool make_scale_map(CUtensorMap* map, const float* base, int num_pages, int Hkv);
+
+}  // namespace hpc

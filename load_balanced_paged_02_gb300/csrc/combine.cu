@@ -4,8 +4,8 @@
 // normalisation; vLLM x HPC-Ops blog, "解决方案：按步负载均衡的 decode 调度器",
 // the final combine into the BF16 output).
 //
-// One warp per output row (request b, query head qh); lane k owns dims
-// [4k, 4k+4). With n partials (o_i, lse_i) of pair (qh / 8, b):
+// One warp per output row (request b, new token i, query head qh); lane k
+// owns dims [4k, 4k+4). With n partials (o_i, lse_i) of pair (qh / 8, b):
 //   M = max lse_i, w_i = exp(lse_i - M), out = sum w_i o_i / sum w_i,
 //   out_lse = M + ln sum w_i.
 // A long request can leave a pair with ~100 partials, so the weights of a
@@ -37,27 +37,33 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const int32_t* __restrict__ pair_nsplit, const int32_t* __restrict__ pair_split0,
                    const float* __restrict__ split_o, const float* __restrict__ split_lse,
-                   __nv_bfloat16* __restrict__ out, float* __restrict__ out_lse, int B, int Hq) {
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ out_lse, int B, int Hq, int Q) {
     __shared__ float wsh[kCombineWarps][kWTile];
     grid_dependency_wait();  // the partials come from the attention kernel
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * kCombineWarps + warp;
-    if (row >= (long long)B * Hq) return;
-    const int b = (int)(row / Hq), qh = (int)(row % Hq);
-    const int h = qh / kGroup, j = qh % kGroup;
+    if (row >= (long long)B * Q * Hq) return;
+    const int b = (int)(row / ((long long)Q * Hq));
+    const int r = (int)(row % ((long long)Q * Hq));
+    const int qi = r / Hq, qh = r % Hq;
+    const int h = qh / kGroup;
     const long long pair = (long long)h * B + b;
     const int n = pair_nsplit[pair];
+    // partial rows of split s are [s][Q][8]: this row's partial of split s is
+    // s * rs + j with rs = 8 * Q rows per split
     const long long s0 = pair_split0[pair];
+    const long long rs = (long long)Q * kGroup;
+    const int j = qi * kGroup + qh % kGroup;
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float lse = -INFINITY;
     if (n == 1) {
-        acc = *reinterpret_cast<const float4*>(split_o + (s0 * kGroup + j) * kHeadDim + 4 * lane);
-        lse = split_lse[s0 * kGroup + j];
+        acc = *reinterpret_cast<const float4*>(split_o + (s0 * rs + j) * kHeadDim + 4 * lane);
+        lse = split_lse[s0 * rs + j];
     } else if (n > 1) {
         float M = -INFINITY;
-        for (int i = lane; i < n; i += 32) M = fmaxf(M, split_lse[(s0 + i) * kGroup + j]);
+        for (int i = lane; i < n; i += 32) M = fmaxf(M, split_lse[(s0 + i) * rs + j]);
         M = warp_max(M);
         if (M != -INFINITY) {
             float wpart = 0.f;
@@ -65,19 +71,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                 const int tn = min(kWTile, n - t0);
                 // weights of this tile, one per lane-strided split
                 for (int i = lane; i < tn; i += 32) {
-                    const float w = exp2f((split_lse[(s0 + t0 + i) * kGroup + j] - M) * kLog2e);
+                    const float w = exp2f((split_lse[(s0 + t0 + i) * rs + j] - M) * kLog2e);
                     wsh[warp][i] = w;
                     wpart += w;
                 }
                 __syncwarp();
                 // weighted rows, kUnroll independent loads in flight per lane
-                const float* base = split_o + ((s0 + t0) * kGroup + j) * kHeadDim + 4 * lane;
+                const float* base = split_o + ((s0 + t0) * rs + j) * kHeadDim + 4 * lane;
                 int i = 0;
                 for (; i + kUnroll <= tn; i += kUnroll) {
                     float4 x[kUnroll];
 #pragma unroll
                     for (int u = 0; u < kUnroll; ++u)
-                        x[u] = *reinterpret_cast<const float4*>(base + (long long)(i + u) * kGroup * kHeadDim);
+                        x[u] = *reinterpret_cast<const float4*>(base + (long long)(i + u) * rs * kHeadDim);
 #pragma unroll
                     for (int u = 0; u < kUnroll; ++u) {
                         const float w = wsh[warp][i + u];
@@ -88,7 +94,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                     }
                 }
                 for (; i < tn; ++i) {
-                    const float4 x = *reinterpret_cast<const float4*>(base + (long long)i * kGroup * kHeadDim);
+                    const float4 x = *reinterpret_cast<const float4*>(base + (long long)i * rs * kHeadDim);
                     const float w = wsh[warp][i];
                     acc.x += w * x.x;
                     acc.y += w * x.y;
@@ -118,12 +124,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 }  // namespace
 
 cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o, const float* split_lse,
-                           __nv_bfloat16* out, float* out_lse, int B, int Hq, int Hkv, cudaStream_t s) {
+                           __nv_bfloat16* out, float* out_lse, int B, int Hq, int Hkv, int q_len, cudaStream_t s) {
     const PlanLayout L = plan_layout(B, Hkv, C);
-    const long long rows = (long long)B * Hq;
+    const long long rows = (long long)B * q_len * Hq;
     const long long blocks = (rows + kCombineWarps - 1) / kCombineWarps;
     return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
-                      plan + L.pair_nsplit, plan + L.pair_split0, split_o, split_lse, out, out_lse, B, Hq);
+                      plan + L.pair_nsplit, plan + L.pair_split0, split_o, split_lse, out, out_lse, B, Hq, q_len);
 }
 
 }  // namespace hpc

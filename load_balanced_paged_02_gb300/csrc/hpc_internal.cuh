@@ -84,6 +84,11 @@ struct AttnArgs {
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 int attn_default_ctas(int fp8);
 
+// Several new tokens per request (attn_mt.cu): q is bf16 [B][q_len][Hq][128],
+// split rows are [split][q_len][8]; 2 <= q_len <= kMaxQLen.
+constexpr int kMaxQLen = HPC_MAX_Q_LEN;
+cudaError_t launch_attn_mt(const AttnArgs& a, int q_len, cudaStream_t s);
+
 struct RopeNormArgs {
     const void* qkv;
     const int32_t* positions;
@@ -106,9 +111,10 @@ struct RopeNormArgs {
 };
 cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s);
 
+// q_len new tokens per request (1 for plain decode): rows (b, i, qh) of out.
 cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o,
                            const float* split_lse, __nv_bfloat16* out, float* out_lse, int B,
-                           int Hq, int Hkv, cudaStream_t s);
+                           int Hq, int Hkv, int q_len, cudaStream_t s);
 
 // ----------------------------------------------------------------- PTX helpers
 #if defined(__CUDACC__)

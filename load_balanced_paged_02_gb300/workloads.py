@@ -98,9 +98,15 @@ def table3_workload(mix: str, num_q_heads: int = 8, num_kv_heads: int = 1, seed:
 def by_name(name: str) -> Workload:
     """A workload by name: one of WORKLOADS, or "t3:<mix>[:<Hq>/<Hkv>][:q8]" for a
     length mix of the decode-latency table (default 8 query / 1 KV head; ":q8"
-    gives it an e4m3 query with per-head scales)."""
+    gives it an e4m3 query with per-head scales). A trailing ":qlen<N>" gives any
+    of them N new tokens per request (causal verification rows)."""
+    from dataclasses import replace
     if name in WORKLOADS:
         return WORKLOADS[name]
+    if ":qlen" in name:
+        base, n = name.rsplit(":qlen", 1)
+        w = by_name(base)
+        return replace(w, name=name, q_len=int(n), note=f"{w.note}; {int(n)} new tokens per request (causal)")
     parts = name.split(":")
     q8 = parts[-1] == "q8"
     if q8:

@@ -24,14 +24,15 @@ def run(case, num_ctas=None, min_chunks=2, static_splits=None, plan=None):
             if num_ctas is None:
                 num_ctas = hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"]))
             plan = hb.hpc_decode_plan(case["seq_lens"], Hkv, num_ctas, min_chunks)
-    so, sl = hb.split_buffers(plan)
+    q_len = case["q"].shape[1] if case["q"].dim() == 4 else 1
+    so, sl = hb.split_buffers(plan, q_len=q_len)
     so.fill_(float("nan"))
     sl.fill_(float("nan"))
     hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                        case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
                        num_pages=case["num_pages"], q_scale=case.get("q_scale"))
     out = torch.full(case["q"].shape, float("nan"), dtype=torch.bfloat16, device=case["q"].device)
-    lse = torch.full(case["q"].shape[:2], float("nan"), dtype=torch.float32, device=case["q"].device)
+    lse = torch.full(case["q"].shape[:-1], float("nan"), dtype=torch.float32, device=case["q"].device)
     hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
     torch.cuda.synchronize()
     return dict(plan=plan, split_o=so, split_lse=sl, out=out, lse=lse)
@@ -75,10 +76,10 @@ def check_plan_exact(res, case, num_ctas=None, min_chunks=2, static_splits=None)
 def check_full(case, res, check_splits=True):
     """Compare every output row (and every split partial) with the oracle."""
     host = wl.to_numpy_case(case)
-    B, Hq, _ = host["q"].shape
+    shape = host["q"].shape[:-1]  # [B, Hq] or [B, q_len, Hq]
     ro, rl = oracle.attn_rows(host)
-    assert_close(res["out"].float().cpu().numpy(), res["lse"].cpu().numpy(), ro.reshape(B, Hq, 128),
-                 rl.reshape(B, Hq), case, "output")
+    assert_close(res["out"].float().cpu().numpy(), res["lse"].cpu().numpy(), ro.reshape(shape + (128,)),
+                 rl.reshape(shape), case, "output")
     if check_splits:
         pb = res["plan"].buf.cpu().numpy()
         so, sl = oracle.attn_splits(pb, host)
@@ -91,14 +92,15 @@ def check_sampled(case, res, requests, heads=None):
     """Compare rows of the given requests (all query heads, or `heads`) with the
     oracle run on a host copy of just those requests' pages."""
     host = wl.to_numpy_case(case, requests=requests)
-    Hq = host["q"].shape[1]
+    Hq = host["q"].shape[-2]
+    Q = host["q"].shape[1] if host["q"].ndim == 4 else 1
     heads = list(range(Hq)) if heads is None else list(heads)
-    rows = [(i, h) for i in range(len(requests)) for h in heads]
+    rows = [(i, qi * Hq + h) for i in range(len(requests)) for qi in range(Q) for h in heads]
     ro, rl = oracle.attn_rows(host, rows)
-    out = res["out"].float().cpu().numpy()
-    lse = res["lse"].cpu().numpy()
-    got_o = np.stack([out[requests[i], h] for i, h in rows])
-    got_l = np.array([lse[requests[i], h] for i, h in rows])
+    out = res["out"].float().cpu().numpy().reshape(len(case["seq_lens"]), Q, Hq, 128)
+    lse = res["lse"].cpu().numpy().reshape(len(case["seq_lens"]), Q, Hq)
+    got_o = np.stack([out[requests[i], r // Hq, r % Hq] for i, r in rows])
+    got_l = np.array([lse[requests[i], r // Hq, r % Hq] for i, r in rows])
     return assert_close(got_o, got_l, ro, rl, case, f"sampled rows of requests {list(requests)}")
 
 
@@ -109,9 +111,18 @@ def check_split_invariants(case, res):
     n = int(pb[3])
     so = res["split_o"][:n].double().cpu().numpy()
     sl = res["split_lse"][:n].double().cpu().numpy()
-    assert np.all(np.isfinite(so)) and np.all(np.isfinite(sl))
-    B, Hq, _ = case["q"].shape
-    o, l = oracle.combine(pb, so, sl, B, Hq, case["k_cache"].shape[2])
+    assert np.all(np.isfinite(so))
+    B, Hq = case["q"].shape[0], case["q"].shape[-2]
+    q_len = case["q"].shape[1] if case["q"].dim() == 4 else None
+    if q_len is None:
+        assert np.all(np.isfinite(sl))
+    else:
+        # a new token whose visible range ends before a descriptor's chunks has an
+        # empty partial there (LSE -inf, output 0); only the last q_len - 1 tokens
+        # of a request can be cut off, so such partials sit at the end of a pair
+        assert not np.any(np.isnan(sl)) and not np.any(np.isposinf(sl))
+        assert np.all(so[np.isneginf(sl)] == 0)
+    o, l = oracle.combine(pb, so, sl, B, Hq, case["k_cache"].shape[2], q_len=q_len)
     got = res["out"].float().cpu().numpy()
     # the only difference is the float32 merge and the bf16 rounding of the output
     assert np.all(np.abs(got - o) <= 2.0 ** -8 * np.abs(o) + 1e-5)

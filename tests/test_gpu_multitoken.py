@@ -1,0 +1,159 @@
+"""Several new tokens per request (speculative verification rows), CUDA path
+against the float64 oracle through the C ABI (GPU only).
+
+New token i of request b attends causally to tokens [0, L_b - q_len + i]. The
+task map is the one-token map; every descriptor computes q_len x 8 rows. Same
+bounds as the one-token path: BF16 KV max abs <= 2e-2 and mean abs <= 2e-3,
+e4m3 KV max abs <= 6e-2, LSE <= 1e-3 abs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+import oracle
+from load_balanced_paged_02_gb300 import binding as hb
+from load_balanced_paged_02_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+# lengths around chunk edges, shorter than q_len, and empty
+RAGGED = [1, 2, 5, 63, 64, 65, 66, 67, 70, 127, 128, 129, 130, 200, 333, 1000, 0, 4097]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hb.lib()
+
+
+def case_for(lens, q_len, hkv=1, dtype="bf16", seed=0, pool=None):
+    w = wl.Workload("t", len(lens), 8 * hkv, hkv, dtype, seed, lens=list(lens), pool_pages=pool,
+                    q_len=q_len)
+    return wl.make_case(w, device=DEV)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("q_len", [2, 3, 4, 5, 6, 7, 8])
+def test_ragged_full(dtype, q_len):
+    case = case_for(RAGGED, q_len, hkv=2, dtype=dtype, seed=40 + q_len)
+    res = _gpu.run(case, num_ctas=152, min_chunks=2)
+    _gpu.check_plan_exact(res, case, min_chunks=2)
+    _gpu.check_full(case, res)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("C,m", [(1, 0), (7, 1), (300, 4)])
+def test_cta_budgets(dtype, C, m):
+    case = case_for(RAGGED, 6, hkv=1, dtype=dtype, seed=50 + C)
+    res = _gpu.run(case, num_ctas=C, min_chunks=m)
+    _gpu.check_full(case, res)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_static_split(dtype):
+    case = case_for([37, 128, 300, 1000, 0, 5, 4096], 4, hkv=2, dtype=dtype, seed=60)
+    res = _gpu.run(case, static_splits=16)
+    _gpu.check_plan_exact(res, case, static_splits=16)
+    _gpu.check_full(case, res)
+
+
+def test_one_token_through_the_multi_entry_matches_decode():
+    """q_len = 1 through hpc_decode_attn_multi / hpc_decode_combine_multi gives
+    the bytes of hpc_decode_attn / hpc_decode_combine."""
+    case = case_for([37, 128, 300, 1000], 1, hkv=2, seed=61)
+    ref = _gpu.run(case, num_ctas=16)
+    q4 = case["q"].unsqueeze(1).contiguous()
+    plan = ref["plan"]
+    so, sl = hb.split_buffers(plan, q_len=1)
+    L = hb.lib()
+    rc = L.hpc_decode_attn_multi(
+        hb._ptr(q4), 1, hb._ptr(case["k_cache"]), hb._ptr(case["v_cache"]), None, None, hb.KV_BF16,
+        case["num_pages"], hb._ptr(case["page_table"]), case["page_table"].shape[1], hb._ptr(case["seq_lens"]),
+        4, 16, 2, 128, 64, plan.ref(), hb._ptr(so), hb._ptr(sl), hb._stream(None))
+    assert rc == 0
+    out = torch.empty_like(q4)
+    lse = torch.empty(q4.shape[:-1], dtype=torch.float32, device=DEV)
+    hb.hpc_decode_combine(plan, so, sl, out, lse, 2)
+    torch.cuda.synchronize()
+    n = int(plan.buf[3].item())
+    assert torch.equal(so[:n], ref["split_o"][:n]) and torch.equal(sl[:n], ref["split_lse"][:n])
+    assert torch.equal(out[:, 0], ref["out"]) and torch.equal(lse[:, 0], ref["lse"])
+
+
+def test_q_len_out_of_range_is_rejected():
+    case = case_for([100, 200], 2, seed=62)
+    plan = hb.hpc_decode_plan(case["seq_lens"], 1, 8, 2)
+    so, sl = hb.split_buffers(plan, q_len=8)
+    L = hb.lib()
+    for bad in (0, -1, 9):
+        rc = L.hpc_decode_attn_multi(
+            hb._ptr(case["q"]), bad, hb._ptr(case["k_cache"]), hb._ptr(case["v_cache"]), None, None,
+            hb.KV_BF16, case["num_pages"], hb._ptr(case["page_table"]), case["page_table"].shape[1],
+            hb._ptr(case["seq_lens"]), 2, 8, 1, 128, 64, plan.ref(), hb._ptr(so), hb._ptr(sl),
+            hb._stream(None))
+        assert rc == 1, bad
+        out = torch.empty((2, 8, 8, 128), dtype=torch.bfloat16, device=DEV)
+        rc = L.hpc_decode_combine_multi(plan.ref(), bad, hb._ptr(so), hb._ptr(sl), hb._ptr(out), None, 2, 8, 1,
+                                        128, hb._stream(None))
+        assert rc == 1, bad
+    assert hb.hpc_decode_read_error(plan) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_garbage_beyond_live_length_is_ignored(dtype):
+    """Slots past the live length of the last page hold NaN codes; the causal
+    mask and the tail fill must keep them out of every row."""
+    case = case_for([65, 130, 7, 200], 5, hkv=1, dtype=dtype, seed=63)
+    pt = case["page_table"].cpu().numpy()
+    for b, L in enumerate(case["seq_lens"].cpu().numpy()):
+        if L % 64:
+            pg = int(pt[b, (L - 1) // 64])
+            for cache in (case["k_cache"], case["v_cache"]):
+                if dtype == "fp8":
+                    cache.view(torch.uint8)[pg, L % 64:] = 0x7F
+                else:
+                    cache[pg, L % 64:] = float("nan")
+            if dtype == "fp8":
+                case["k_scale"][pg, :, L % 64:] = float("nan")
+                case["v_scale"][pg, :, L % 64:] = float("nan")
+    res = _gpu.run(case, num_ctas=5, min_chunks=1)
+    _gpu.check_full(case, res)
+
+
+def test_peaky_scores():
+    """A query aligned with one key: the row is dominated by that key, for the
+    new token that sees it and not for the earlier ones."""
+    case = case_for([300], 4, hkv=1, seed=64)
+    pt = case["page_table"].cpu().numpy()
+    key = 298  # visible to new tokens 2 and 3 (they see [0, 298] and [0, 299])
+    k = case["k_cache"][int(pt[0, key // 64]), key % 64, 0].float()
+    case["q"][0, :, 0] = (k * 4.0).to(torch.bfloat16)
+    res = _gpu.run(case, num_ctas=3, min_chunks=1)
+    _gpu.check_full(case, res)
+    v = case["v_cache"][int(pt[0, key // 64]), key % 64, 0].float()
+    out = res["out"][0, :, 0].float()
+    assert torch.allclose(out[2], v, atol=0.05) and torch.allclose(out[3], v, atol=0.05)
+    assert not torch.allclose(out[0], v, atol=0.05)
+
+
+@pytest.mark.parametrize("name,q_len", [("mixed", 2), ("mixed", 6), ("fp8", 6)])
+def test_full_size_sampled(name, q_len):
+    """The full-size batch with q_len new tokens, in the launch configuration
+    the benchmark times: sampled requests against the oracle, plus the
+    size-independent split/combine property."""
+    from dataclasses import replace
+    w = replace(wl.WORKLOADS[name], q_len=q_len)
+    case = wl.make_case(w, device=DEV)
+    res = _gpu.run(case, num_ctas=hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"])), min_chunks=w.min_chunks)
+    _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
+    lens = case["seq_lens"].cpu().numpy()
+    order = np.argsort(lens)
+    pick = [int(order[0]), int(order[-1])] + [int(x) for x in np.random.default_rng(7).choice(len(lens), 2)]
+    _gpu.check_sampled(case, res, pick[:2], heads=range(0, 64, 9))
+    _gpu.check_sampled(case, res, pick[2:], heads=[0, 17, 63])
+    _gpu.check_split_invariants(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
