@@ -175,15 +175,21 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "decode_attn_kernel": ("attn.cu", "attn_common.cuh", "hpc_internal.cuh"),
+    "decode_attn_mt_kernel": ("attn_mt.cu", "attn_common.cuh", "hpc_internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel="decode_attn_kernel"):
     h = hashlib.sha256()
-    for f in ("attn.cu", "hpc_internal.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "load_balanced_paged_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload, dtype):
+def recorded_traffic(workload, dtype, kernel="decode_attn_kernel"):
     """DRAM bytes per attention launch from a committed ncu summary, if it was
     taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "attn_traffic.json")
@@ -192,7 +198,7 @@ def recorded_traffic(workload, dtype):
     with open(path) as f:
         d = json.load(f)
     rec = d.get(f"{workload}:{dtype}")
-    if not rec or rec.get("kernel_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_hash") != kernel_source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -517,6 +523,7 @@ def run_ours(args):
     value = units_all / (ms_step * 1e-3) / 1e9
     attn_gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
 
+    kname = "decode_attn_kernel" if w.q_len == 1 else "decode_attn_mt_kernel"
     result = None
     if rank == 0:
         clocks = clk.summary()
@@ -536,8 +543,8 @@ def run_ours(args):
                                        "layer_attn_combine": layer_us}},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
-                         "traffic": recorded_traffic(w.name, "bf16" if kvd == hb.KV_BF16 else "e4m3"),
-                         "kernel": "decode_attn_kernel", "algorithmic_bytes_per_launch": byt["attn"]},
+                         "traffic": recorded_traffic(w.name, "bf16" if kvd == hb.KV_BF16 else "e4m3", kname),
+                         "kernel": kname, "algorithmic_bytes_per_launch": byt["attn"]},
             "gpu_launches": (6 if graph is not None else 3) * args.steps,
             "clocks": clocks,
         }
