@@ -235,6 +235,29 @@ hpc_status hpc_decode_attn_multi(const void* q, int q_len, const void* k_cache, 
                                  int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
                                  float* split_o, float* split_lse, void* stream);
 
+/* Kernels behind hpc_decode_attn_multi_engine. */
+#define HPC_ENGINE_AUTO 0       /* the faster one for the cache dtype and q_len (below) */
+#define HPC_ENGINE_MMA_SYNC 1   /* warp-level mma.sync kernels (every dtype and q_len) */
+#define HPC_ENGINE_TCGEN05 2    /* tcgen05.mma with TMEM accumulators (bf16 caches) */
+
+/*
+ * hpc_decode_attn_multi with a choice of kernel, for callers that pin one and
+ * for tests. HPC_ENGINE_AUTO (what hpc_decode_attn_multi uses) takes the
+ * tcgen05 kernel for bf16 caches with q_len >= 3 and the warp-level kernels
+ * otherwise. Both compute the same rows with bf16 probabilities and float32
+ * accumulation; they differ in summation order and in where the softmax
+ * reference maximum moves. Errors: as hpc_decode_attn_multi, plus
+ * HPC_ERR_INVALID_ARG for an unknown engine and HPC_ERR_UNSUPPORTED for
+ * HPC_ENGINE_TCGEN05 on an e4m3 cache.
+ */
+hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_cache, const void* v_cache,
+                                        const float* k_scale, const float* v_scale, int kv_dtype,
+                                        int num_pages, const int32_t* page_table, int page_table_stride,
+                                        const int32_t* seq_lens, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int page_size,
+                                        const hpc_plan* plan, float* split_o, float* split_lse,
+                                        int engine, void* stream);
+
 /*
  * Combine ([SGL] the paragraph on execution; [VLLM] combine stage). For every
  * (request b, query head qh) with h = qh / 8, j = qh % 8 and the pair's

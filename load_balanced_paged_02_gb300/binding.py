@@ -17,6 +17,7 @@ from . import _build
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+ENGINE_AUTO, ENGINE_MMA_SYNC, ENGINE_TCGEN05 = 0, 1, 2
 HEAD_DIM = 128
 PAGE = 64
 GROUP = 8
@@ -55,6 +56,8 @@ SIGNATURES = {
                                 _vp, _vp, _vp]),
     "hpc_decode_attn_multi": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i,
                                    _P, _vp, _vp, _vp]),
+    "hpc_decode_attn_multi_engine": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i,
+                                          _i, _P, _vp, _vp, _i, _vp]),
     "hpc_decode_combine": (_i, [_P, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "hpc_decode_combine_multi": (_i, [_P, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "hpc_rope_norm": (_i, [_vp, _vp, _vp, _i, _vp, _vp, ctypes.c_float, _vp, _i, _i, _i, _i, _i, _vp, _vp,
@@ -204,11 +207,12 @@ def split_buffers(plan: Plan, device=None, q_len: int = 1):
 
 def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split_o, split_lse,
                     k_scale=None, v_scale=None, num_pages: int | None = None, stream=None,
-                    q_scale=None):
+                    q_scale=None, engine: int | None = None):
     """Persistent attention over the task map; writes split_o / split_lse.
     A float8_e4m3fn q with its q_scale [B, Hq] goes to hpc_decode_attn_q8; a
     bf16 q of shape [B, q_len, Hq, 128] (several new tokens per request, causal)
-    goes to hpc_decode_attn_multi."""
+    goes to hpc_decode_attn_multi (or hpc_decode_attn_multi_engine when ``engine``
+    is given: ENGINE_AUTO, ENGINE_MMA_SYNC or ENGINE_TCGEN05)."""
     kvd = kv_dtype_of(k_cache)
     q_len = q.shape[1] if q.dim() == 4 else 1
     B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
@@ -231,6 +235,13 @@ def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split
             _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D,
             int(k_cache.shape[1]), plan.ref(), _ptr(split_o), _ptr(split_lse), _stream(stream))
         _check("hpc_decode_attn_q8", rc)
+        return
+    if q.dim() == 4 and engine is not None:
+        rc = lib().hpc_decode_attn_multi_engine(
+            _ptr(q), q_len, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd, npages,
+            _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D, int(k_cache.shape[1]),
+            plan.ref(), _ptr(split_o), _ptr(split_lse), int(engine), _stream(stream))
+        _check("hpc_decode_attn_multi_engine", rc)
         return
     if q.dim() == 4:
         rc = lib().hpc_decode_attn_multi(

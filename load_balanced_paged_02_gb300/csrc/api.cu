@@ -119,13 +119,23 @@ hpc_status hpc_decode_plan_static(const int32_t* d_seq_lens, int batch, int num_
 
 namespace {
 
+// Engine used by HPC_ENGINE_AUTO: measured on GB300 (mixed-length bf16 batch),
+// the warp-level kernels are fastest for one and two new tokens (353 / 373 us
+// against 377 / 379 us), the tcgen05 kernel from three on (381 against 426 us
+// at three, 385 against 816 us at six); e4m3 caches run the warp-level kernels.
+int multi_engine_for(bool fp8, int q_len) {
+    if (fp8) return HPC_ENGINE_MMA_SYNC;
+    return q_len >= 3 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
+}
+
 // Shared by hpc_decode_attn (bf16 Q), hpc_decode_attn_q8 (e4m3 Q + scales)
 // and hpc_decode_attn_multi (q_len bf16 query rows per request).
 hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache, const void* v_cache,
                        const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
                        const int32_t* page_table, int page_table_stride, const int32_t* seq_lens, int batch,
                        int num_q_heads, int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
-                       float* split_o, float* split_lse, void* stream, int q_len = 1) {
+                       float* split_o, float* split_lse, void* stream, int q_len = 1,
+                       int engine = HPC_ENGINE_AUTO) {
     hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
     if (st != HPC_OK) return st;
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
@@ -142,6 +152,8 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     if (q_scale && (!fp8 || !aligned(q_scale, 16))) return fp8 ? HPC_ERR_INVALID_ARG : HPC_ERR_UNSUPPORTED;
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     if (q_len < 1 || q_len > HPC_MAX_Q_LEN || (q_len > 1 && q_scale)) return HPC_ERR_INVALID_ARG;
+    if (engine < HPC_ENGINE_AUTO || engine > HPC_ENGINE_TCGEN05) return HPC_ERR_INVALID_ARG;
+    if (engine == HPC_ENGINE_TCGEN05 && fp8) return HPC_ERR_UNSUPPORTED;
     AttnArgs a;
     a.q = q;
     a.q_scale = q_scale;
@@ -163,8 +175,13 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     a.split_cap = (long long)hpc_decode_split_capacity(batch, num_kv_heads, plan->num_ctas);
     a.split_o = split_o;
     a.split_lse = split_lse;
-    cudaError_t e = q_len == 1 ? launch_attn(a, static_cast<cudaStream_t>(stream))
-                               : launch_attn_mt(a, q_len, static_cast<cudaStream_t>(stream));
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (engine == HPC_ENGINE_AUTO) engine = multi_engine_for(fp8, q_len);
+    cudaError_t e;
+    if (engine == HPC_ENGINE_TCGEN05)
+        e = launch_attn_tc(a, q_len, cs);
+    else
+        e = q_len == 1 ? launch_attn(a, cs) : launch_attn_mt(a, q_len, cs);
     if (e == cudaErrorInvalidValue) return HPC_ERR_INVALID_ARG;
     return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
@@ -203,6 +220,18 @@ hpc_status hpc_decode_attn_multi(const void* q, int q_len, const void* k_cache, 
     return attn_common(q, nullptr, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
                        page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
                        split_o, split_lse, stream, q_len);
+}
+
+hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_cache, const void* v_cache,
+                                        const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
+                                        const int32_t* page_table, int page_table_stride, const int32_t* seq_lens,
+                                        int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                        const hpc_plan* plan, float* split_o, float* split_lse, int engine,
+                                        void* stream) {
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN) return HPC_ERR_INVALID_ARG;
+    return attn_common(q, nullptr, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
+                       page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
+                       split_o, split_lse, stream, q_len, engine);
 }
 
 hpc_status hpc_decode_combine_multi(const hpc_plan* plan, int q_len, const float* split_o, const float* split_lse,

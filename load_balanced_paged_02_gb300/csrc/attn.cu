@@ -366,7 +366,10 @@ timeout:
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -380,12 +383,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-}  // namespace
-
 // 2-D map over a scale array [num_pages * Hkv rows][64 float32]; box = one
 // 256-byte row (the 64 scales of one page and KV head).
 bool make_scale_map(CUtensorMap* map, const float* base, int num_pages, int Hkv) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kChunk, (cuuint64_t)num_pages * Hkv};
     cuuint64_t strides[1] = {kChunk * sizeof(float)};
@@ -400,7 +401,7 @@ bool make_scale_map(CUtensorMap* map, const float* base, int num_pages, int Hkv)
 // 3-D map over a paged cache [num_pages*64 tokens][Hkv][128]; box = 64 tokens
 // x 1 head x (64 bf16 or 128 e4m3 = 128 bytes), 128-byte swizzle.
 bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int Hkv) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     const cuuint64_t esz = fp8 ? 1 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)Hkv, (cuuint64_t)num_pages * kChunk};

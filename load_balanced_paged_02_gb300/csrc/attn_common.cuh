@@ -183,6 +183,8 @@ enum class QStage {
     kBf16,      // one new token: 8 bf16 rows (2 KB)
     kE4m3,      // one new token: 8 rows of e4m3 codes, then their 8 float32 scales
     kBf16Rows,  // p.q_len new tokens: p.q_len blocks of 8 bf16 rows
+    kBf16Tile,  // p.q_len new tokens as one 128-byte-swizzled tile [2 dim halves][8 q_len rows][128 B]
+                // by two 3-D TMA loads through tm_q (an MMA operand as it lands)
 };
 
 constexpr int kQRowsBytes = kGroup * kHeadDim * 2;  // 8 bf16 query rows
@@ -201,7 +203,7 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
                                         const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, int list0, int lane,
                                         uint8_t* smem, uint8_t* qbuf, uint32_t q_slot_bytes, uint64_t* full,
                                         uint64_t* empty, uint64_t* qfull, uint64_t* qempty, volatile int* meta,
-                                        volatile int* abort_flag) {
+                                        volatile int* abort_flag, const CUtensorMap* tm_q = nullptr) {
     using Cfg = KvCfg<FP8>;
     const uint64_t pol = l2_evict_first_policy();
     uint32_t seq = 0;
@@ -223,7 +225,14 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
             ok = wait_bounded(&qempty[qs], ((qd >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
             if (ok) {
                 uint8_t* qdst = qbuf + qs * q_slot_bytes;
-                if constexpr (QM == QStage::kE4m3) {
+                if constexpr (QM == QStage::kBf16Tile) {
+                    // rows (i, j) = new token i, query head 8h + j of request b; box
+                    // 64 dims x 8 heads x q_len tokens per dim half
+                    const uint32_t half = (uint32_t)p.q_len * kQRowsBytes / 2;
+                    mbar_arrive_expect_tx(&qfull[qs], 2 * half);
+                    tma_load_3d(qdst, tm_q, &qfull[qs], 0, h * kGroup, b * p.q_len, pol);
+                    tma_load_3d(qdst + q_slot_bytes / 2, tm_q, &qfull[qs], 64, h * kGroup, b * p.q_len, pol);
+                } else if constexpr (QM == QStage::kE4m3) {
                     // 8 rows of 128 e4m3 codes, then their 8 scales
                     const long long qrow = (long long)b * p.num_q_heads + (long long)h * kGroup;
                     mbar_arrive_expect_tx(&qfull[qs], kGroup * kHeadDim + kGroup * 4);
@@ -305,6 +314,7 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
 }  // namespace attn
 
 // Tensor maps (defined in attn.cu).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int Hkv);
 bool make_scale_map(CUtensorMap* map, const float* base, int num_pages, int Hkv);
 

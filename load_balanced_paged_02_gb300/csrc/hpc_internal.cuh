@@ -88,6 +88,8 @@ int attn_default_ctas(int fp8);
 // split rows are [split][q_len][8]; 2 <= q_len <= kMaxQLen.
 constexpr int kMaxQLen = HPC_MAX_Q_LEN;
 cudaError_t launch_attn_mt(const AttnArgs& a, int q_len, cudaStream_t s);
+// The same on tcgen05 tensor cores with TMEM accumulators (attn_tc.cu), bf16 KV.
+cudaError_t launch_attn_tc(const AttnArgs& a, int q_len, cudaStream_t s);
 
 struct RopeNormArgs {
     const void* qkv;

@@ -36,29 +36,63 @@ def case_for(lens, q_len, hkv=1, dtype="bf16", seed=0, pool=None):
     return wl.make_case(w, device=DEV)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-@pytest.mark.parametrize("q_len", [2, 3, 4, 5, 6, 7, 8])
-def test_ragged_full(dtype, q_len):
+# (cache dtype, kernel): the warp-level kernels serve both dtypes, the tcgen05
+# kernel bf16 caches
+ENGINES = [("bf16", hb.ENGINE_MMA_SYNC), ("bf16", hb.ENGINE_TCGEN05), ("fp8", hb.ENGINE_MMA_SYNC)]
+ENGINE_IDS = ["bf16-mma_sync", "bf16-tcgen05", "fp8-mma_sync"]
+
+
+@pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_ragged_full(dtype, engine, q_len):
     case = case_for(RAGGED, q_len, hkv=2, dtype=dtype, seed=40 + q_len)
-    res = _gpu.run(case, num_ctas=152, min_chunks=2)
+    if q_len == 1:
+        case["q"] = case["q"].unsqueeze(1).contiguous()
+    res = _gpu.run(case, num_ctas=152, min_chunks=2, engine=engine)
     _gpu.check_plan_exact(res, case, min_chunks=2)
     _gpu.check_full(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
 @pytest.mark.parametrize("C,m", [(1, 0), (7, 1), (300, 4)])
-def test_cta_budgets(dtype, C, m):
+def test_cta_budgets(dtype, engine, C, m):
     case = case_for(RAGGED, 6, hkv=1, dtype=dtype, seed=50 + C)
-    res = _gpu.run(case, num_ctas=C, min_chunks=m)
+    res = _gpu.run(case, num_ctas=C, min_chunks=m, engine=engine)
     _gpu.check_full(case, res)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-def test_static_split(dtype):
+@pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
+def test_static_split(dtype, engine):
     case = case_for([37, 128, 300, 1000, 0, 5, 4096], 4, hkv=2, dtype=dtype, seed=60)
-    res = _gpu.run(case, static_splits=16)
+    res = _gpu.run(case, static_splits=16, engine=engine)
     _gpu.check_plan_exact(res, case, static_splits=16)
     _gpu.check_full(case, res)
+
+
+def test_tcgen05_rejects_e4m3_cache():
+    case = case_for([100, 200], 3, dtype="fp8", seed=65)
+    plan = hb.hpc_decode_plan(case["seq_lens"], 1, 8, 2)
+    so, sl = hb.split_buffers(plan, q_len=3)
+    with pytest.raises(hb.HpcError, match="UNSUPPORTED"):
+        hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"], case["seq_lens"], plan,
+                           so, sl, case["k_scale"], case["v_scale"], engine=hb.ENGINE_TCGEN05)
+
+
+def test_large_scores_move_the_reference_max():
+    """Scores that grow along the sequence force the tcgen05 kernel to rescale
+    its TMEM output several times (lazy rescale beyond 2^8); both kernels must
+    still match the oracle."""
+    case = case_for([700, 1500], 3, hkv=1, seed=66)
+    pt = case["page_table"].cpu().numpy()
+    for b, L in enumerate(case["seq_lens"].cpu().numpy()):
+        for tok in range(0, int(L), 37):
+            pg, sl = int(pt[b, tok // 64]), tok % 64
+            case["k_cache"][pg, sl, 0] = (case["k_cache"][pg, sl, 0].float() * (1 + tok / 300.0)).to(torch.bfloat16)
+    case["q"] *= 2
+    for engine in (hb.ENGINE_MMA_SYNC, hb.ENGINE_TCGEN05):
+        res = _gpu.run(case, num_ctas=4, min_chunks=1, engine=engine)
+        _gpu.check_full(case, res)
 
 
 def test_one_token_through_the_multi_entry_matches_decode():
@@ -103,8 +137,8 @@ def test_q_len_out_of_range_is_rejected():
     assert hb.hpc_decode_read_error(plan) == 0
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
-def test_garbage_beyond_live_length_is_ignored(dtype):
+@pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
+def test_garbage_beyond_live_length_is_ignored(dtype, engine):
     """Slots past the live length of the last page hold NaN codes; the causal
     mask and the tail fill must keep them out of every row."""
     case = case_for([65, 130, 7, 200], 5, hkv=1, dtype=dtype, seed=63)
@@ -120,11 +154,12 @@ def test_garbage_beyond_live_length_is_ignored(dtype):
             if dtype == "fp8":
                 case["k_scale"][pg, :, L % 64:] = float("nan")
                 case["v_scale"][pg, :, L % 64:] = float("nan")
-    res = _gpu.run(case, num_ctas=5, min_chunks=1)
+    res = _gpu.run(case, num_ctas=5, min_chunks=1, engine=engine)
     _gpu.check_full(case, res)
 
 
-def test_peaky_scores():
+@pytest.mark.parametrize("engine", [hb.ENGINE_MMA_SYNC, hb.ENGINE_TCGEN05], ids=["mma_sync", "tcgen05"])
+def test_peaky_scores(engine):
     """A query aligned with one key: the row is dominated by that key, for the
     new token that sees it and not for the earlier ones."""
     case = case_for([300], 4, hkv=1, seed=64)
@@ -132,7 +167,7 @@ def test_peaky_scores():
     key = 298  # visible to new tokens 2 and 3 (they see [0, 298] and [0, 299])
     k = case["k_cache"][int(pt[0, key // 64]), key % 64, 0].float()
     case["q"][0, :, 0] = (k * 4.0).to(torch.bfloat16)
-    res = _gpu.run(case, num_ctas=3, min_chunks=1)
+    res = _gpu.run(case, num_ctas=3, min_chunks=1, engine=engine)
     _gpu.check_full(case, res)
     v = case["v_cache"][int(pt[0, key // 64]), key % 64, 0].float()
     out = res["out"][0, :, 0].float()
@@ -140,7 +175,7 @@ def test_peaky_scores():
     assert not torch.allclose(out[0], v, atol=0.05)
 
 
-@pytest.mark.parametrize("name,q_len", [("mixed", 2), ("mixed", 6), ("fp8", 6)])
+@pytest.mark.parametrize("name,q_len", [("mixed", 2), ("mixed", 4), ("mixed", 6), ("mixed", 8), ("fp8", 6)])
 def test_full_size_sampled(name, q_len):
     """The full-size batch with q_len new tokens, in the launch configuration
     the benchmark times: sampled requests against the oracle, plus the
