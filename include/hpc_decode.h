@@ -238,17 +238,21 @@ hpc_status hpc_decode_attn_multi(const void* q, int q_len, const void* k_cache, 
 /* Kernels behind hpc_decode_attn_multi_engine. */
 #define HPC_ENGINE_AUTO 0       /* the faster one for the cache dtype and q_len (below) */
 #define HPC_ENGINE_MMA_SYNC 1   /* warp-level mma.sync kernels (every dtype and q_len) */
-#define HPC_ENGINE_TCGEN05 2    /* tcgen05.mma with TMEM accumulators (bf16 caches) */
+#define HPC_ENGINE_TCGEN05 2    /* tcgen05.mma with TMEM accumulators (every dtype and q_len) */
 
 /*
  * hpc_decode_attn_multi with a choice of kernel, for callers that pin one and
  * for tests. HPC_ENGINE_AUTO (what hpc_decode_attn_multi uses) takes the
- * tcgen05 kernel for bf16 caches with q_len >= 3 and the warp-level kernels
- * otherwise. Both compute the same rows with bf16 probabilities and float32
+ * faster kernel measured for the cache dtype and q_len (see multi_engine_for
+ * in api.cu). Both compute the same rows with 16-bit probabilities and float32
  * accumulation; they differ in summation order and in where the softmax
- * reference maximum moves. Errors: as hpc_decode_attn_multi, plus
- * HPC_ERR_INVALID_ARG for an unknown engine and HPC_ERR_UNSUPPORTED for
- * HPC_ENGINE_TCGEN05 on an e4m3 cache.
+ * reference maximum moves. On an e4m3 cache the tcgen05 kernel multiplies the
+ * exact K codes by Q in f16 and applies the K scales to the float32 scores (as
+ * the warp-level kernel does); V enters the P . V product dequantised and
+ * rounded to f16, so its values must lie within the f16 range (|v| <= 65504),
+ * and Q must fit f16 as well (as for the warp-level e4m3 kernel).
+ * Errors: as hpc_decode_attn_multi, plus HPC_ERR_INVALID_ARG for an unknown
+ * engine.
  */
 hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_cache, const void* v_cache,
                                         const float* k_scale, const float* v_scale, int kv_dtype,

@@ -119,12 +119,15 @@ hpc_status hpc_decode_plan_static(const int32_t* d_seq_lens, int batch, int num_
 
 namespace {
 
-// Engine used by HPC_ENGINE_AUTO: measured on GB300 (mixed-length bf16 batch),
-// the warp-level kernels are fastest for one and two new tokens (353 / 373 us
-// against 377 / 379 us), the tcgen05 kernel from three on (381 against 426 us
-// at three, 385 against 816 us at six); e4m3 caches run the warp-level kernels.
+// Engine used by HPC_ENGINE_AUTO, as measured on GB300 (median attention
+// launch on the full batches). bf16 (mixed-length batch): the warp-level
+// kernels are fastest for one and two new tokens (367 / 389 us against
+// 391 / 394 us), the tcgen05 kernel from three on (397 against 440 us at three,
+// 398 against 831 us at six). e4m3 (the long-context batch): the warp-level
+// kernels up to six new tokens (1777 us at two, 4660 against 4698 at six), the
+// tcgen05 kernel from seven (4704 against 6954 us at seven and eight).
 int multi_engine_for(bool fp8, int q_len) {
-    if (fp8) return HPC_ENGINE_MMA_SYNC;
+    if (fp8) return q_len >= 7 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
     return q_len >= 3 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
 }
 
@@ -153,7 +156,6 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     if (q_len < 1 || q_len > HPC_MAX_Q_LEN || (q_len > 1 && q_scale)) return HPC_ERR_INVALID_ARG;
     if (engine < HPC_ENGINE_AUTO || engine > HPC_ENGINE_TCGEN05) return HPC_ERR_INVALID_ARG;
-    if (engine == HPC_ENGINE_TCGEN05 && fp8) return HPC_ERR_UNSUPPORTED;
     AttnArgs a;
     a.q = q;
     a.q_scale = q_scale;

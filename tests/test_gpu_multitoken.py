@@ -36,10 +36,10 @@ def case_for(lens, q_len, hkv=1, dtype="bf16", seed=0, pool=None):
     return wl.make_case(w, device=DEV)
 
 
-# (cache dtype, kernel): the warp-level kernels serve both dtypes, the tcgen05
-# kernel bf16 caches
-ENGINES = [("bf16", hb.ENGINE_MMA_SYNC), ("bf16", hb.ENGINE_TCGEN05), ("fp8", hb.ENGINE_MMA_SYNC)]
-ENGINE_IDS = ["bf16-mma_sync", "bf16-tcgen05", "fp8-mma_sync"]
+# (cache dtype, kernel): both kernels serve both cache dtypes
+ENGINES = [("bf16", hb.ENGINE_MMA_SYNC), ("bf16", hb.ENGINE_TCGEN05), ("fp8", hb.ENGINE_MMA_SYNC),
+           ("fp8", hb.ENGINE_TCGEN05)]
+ENGINE_IDS = ["bf16-mma_sync", "bf16-tcgen05", "fp8-mma_sync", "fp8-tcgen05"]
 
 
 @pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
@@ -70,25 +70,44 @@ def test_static_split(dtype, engine):
     _gpu.check_full(case, res)
 
 
-def test_tcgen05_rejects_e4m3_cache():
-    case = case_for([100, 200], 3, dtype="fp8", seed=65)
-    plan = hb.hpc_decode_plan(case["seq_lens"], 1, 8, 2)
-    so, sl = hb.split_buffers(plan, q_len=3)
-    with pytest.raises(hb.HpcError, match="UNSUPPORTED"):
-        hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"], case["seq_lens"], plan,
-                           so, sl, case["k_scale"], case["v_scale"], engine=hb.ENGINE_TCGEN05)
+@pytest.mark.parametrize("engine", [hb.ENGINE_MMA_SYNC, hb.ENGINE_TCGEN05], ids=["mma_sync", "tcgen05"])
+def test_e4m3_peaky_scores_and_uneven_scales(engine):
+    """e4m3 cache: a query aligned with one key (its score is 30, far above the
+    first chunk's maximum, so the reference max moves) and K/V scales that vary
+    by two orders of magnitude between tokens; the K scales weight the score
+    columns and the V scales the value rows."""
+    case = case_for([300, 700], 3, hkv=1, dtype="fp8", seed=65)
+    g = torch.Generator(device="cpu").manual_seed(65)
+    for cache, name in (("k_cache", "k_scale"), ("v_cache", "v_scale")):
+        # codes / f and scale x f: the values keep their size (so the bf16
+        # output rounding stays far below the bound) while the scales spread
+        f = torch.exp(torch.empty(case[name].shape).uniform_(-2.3, 2.3, generator=g)).to(DEV)
+        codes = case[cache].float() / f.permute(0, 2, 1).unsqueeze(-1)
+        case[cache].copy_(codes.clamp(-448, 448).to(torch.float8_e4m3fn))
+        case[name] *= f
+    pt = case["page_table"].cpu().numpy()
+    key = 290  # visible to new tokens 1 and 2 of request 0 (they see [0, 298] and [0, 299])
+    pg, sl = int(pt[0, key // 64]), key % 64
+    kv = case["k_cache"][pg, sl, 0].float() * case["k_scale"][pg, 0, sl]
+    case["q"][0, :, 0] = (kv * (30.0 * 128 ** 0.5 / kv.dot(kv))).to(torch.bfloat16)
+    res = _gpu.run(case, num_ctas=3, min_chunks=1, engine=engine)
+    _gpu.check_full(case, res)
 
 
-def test_large_scores_move_the_reference_max():
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_large_scores_move_the_reference_max(dtype):
     """Scores that grow along the sequence force the tcgen05 kernel to rescale
     its TMEM output several times (lazy rescale beyond 2^8); both kernels must
     still match the oracle."""
-    case = case_for([700, 1500], 3, hkv=1, seed=66)
+    case = case_for([700, 1500], 3, hkv=1, dtype=dtype, seed=66)
     pt = case["page_table"].cpu().numpy()
     for b, L in enumerate(case["seq_lens"].cpu().numpy()):
         for tok in range(0, int(L), 37):
             pg, sl = int(pt[b, tok // 64]), tok % 64
-            case["k_cache"][pg, sl, 0] = (case["k_cache"][pg, sl, 0].float() * (1 + tok / 300.0)).to(torch.bfloat16)
+            if dtype == "fp8":  # e4m3 codes saturate: grow the token's K scale instead
+                case["k_scale"][pg, 0, sl] *= 1 + tok / 300.0
+            else:
+                case["k_cache"][pg, sl, 0] = (case["k_cache"][pg, sl, 0].float() * (1 + tok / 300.0)).to(torch.bfloat16)
     case["q"] *= 2
     for engine in (hb.ENGINE_MMA_SYNC, hb.ENGINE_TCGEN05):
         res = _gpu.run(case, num_ctas=4, min_chunks=1, engine=engine)
@@ -175,15 +194,18 @@ def test_peaky_scores(engine):
     assert not torch.allclose(out[0], v, atol=0.05)
 
 
-@pytest.mark.parametrize("name,q_len", [("mixed", 2), ("mixed", 4), ("mixed", 6), ("mixed", 8), ("fp8", 6)])
-def test_full_size_sampled(name, q_len):
+@pytest.mark.parametrize("name,q_len,engine", [("mixed", 2, None), ("mixed", 4, None), ("mixed", 6, None),
+                                               ("mixed", 8, None), ("fp8", 6, hb.ENGINE_MMA_SYNC),
+                                               ("fp8", 2, hb.ENGINE_TCGEN05), ("fp8", 8, hb.ENGINE_TCGEN05)])
+def test_full_size_sampled(name, q_len, engine):
     """The full-size batch with q_len new tokens, in the launch configuration
     the benchmark times: sampled requests against the oracle, plus the
     size-independent split/combine property."""
     from dataclasses import replace
     w = replace(wl.WORKLOADS[name], q_len=q_len)
     case = wl.make_case(w, device=DEV)
-    res = _gpu.run(case, num_ctas=hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"])), min_chunks=w.min_chunks)
+    res = _gpu.run(case, num_ctas=hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"])), min_chunks=w.min_chunks,
+                   engine=engine)
     _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
     lens = case["seq_lens"].cpu().numpy()
     order = np.argsort(lens)
