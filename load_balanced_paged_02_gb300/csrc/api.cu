@@ -122,12 +122,13 @@ namespace {
 // Engine used by HPC_ENGINE_AUTO, as measured on GB300 (median attention
 // launch on the full batches). bf16 (mixed-length batch): the warp-level
 // kernels are fastest for one and two new tokens (367 / 389 us against
-// 391 / 394 us), the tcgen05 kernel from three on (397 against 440 us at three,
-// 398 against 831 us at six). e4m3 (the long-context batch): the warp-level
-// kernels up to six new tokens (1777 us at two, 4660 against 4698 at six), the
-// tcgen05 kernel from seven (4704 against 6954 us at seven and eight).
+// 389 / 391 us), the tcgen05 kernel from three on (about 395 us for any q_len,
+// against 440 us at three and 831 us at six). e4m3 (the long-context batch):
+// the warp-level kernels for one and two new tokens (1309 / 1777 us), the
+// tcgen05 kernel from three (about 2165 us for any q_len, against 3252 us at
+// three, 4660 at six and 6954 at eight).
 int multi_engine_for(bool fp8, int q_len) {
-    if (fp8) return q_len >= 7 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
+    if (fp8) return q_len >= 3 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
     return q_len >= 3 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
 }
 

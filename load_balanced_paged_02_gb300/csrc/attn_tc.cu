@@ -12,7 +12,7 @@
 //    into a 2-slot ring as one swizzled tile (two 3-D TMA loads).
 //  * warp 9, S issuer: one thread issues, per chunk k of 64 tokens,
 //      S_k = Q . K_k^T   (M = 64 query rows, N = 64 tokens, K = 128 dims)
-//    into TMEM score buffer k % 2 (tcgen05.mma kind::f16, 16-bit operands in
+//    into TMEM score buffer k % 3 (tcgen05.mma kind::f16, 16-bit operands in
 //    shared memory, f32 accumulator; K and Q are K-major).
 //  * warp 10, P.V issuer: one thread issues O_g += P_k . V_k (M = 64, N = 128
 //    dims, K = 64 tokens; V is the MN-major operand) into TMEM output tile
@@ -20,33 +20,40 @@
 //    the two MMA chains from waiting on each other; tcgen05.commit arrives on
 //    the mbarriers that free score buffers, P buffers, stages and query slots.
 //  * warps 0-3 and 4-7, two softmax warpgroups: warpgroup g takes the chunks
-//    k with k % 2 == g. Thread (w, l < 16) of a warpgroup owns query row
-//    r = 16 w + l (= new token r / 8, head r % 8), which the M = 64 layout puts
-//    in TMEM lane 32 w + l. It loads its 64 scores, masks tokens past the
-//    chunk's valid count and its causal limit, and keeps a reference max m and
-//    sum l (log2 domain) for its warpgroup's chunks. P = exp2(s - m) goes to
-//    shared memory as a 16-bit value; O_g is rescaled in TMEM only when a
-//    chunk's max exceeds m by more than 8 (so P <= 256), which after the first
-//    chunks is rare. At the descriptor's end warpgroup 1 publishes its (m, l)
-//    and warpgroup 0 merges both states and both O tiles into the partial row
-//    and its LSE.
-// e4m3 caches (one float32 scale per token and KV head), 15 warps: the same
-// roles on f16 operands, plus
-//  * warps 11-14, converter: the producer fills a deeper ring of e4m3 stages
-//    (K codes, V codes, their two 256-byte scale rows); the converter widens
-//    each stage into an f16 operand slot laid out like a bf16 stage: K as its
-//    exact codes (every e4m3 value is an f16 value), V dequantised (code x
-//    scale, rounded to f16), rows past the live length zero. The K scales,
-//    times log2(e)/sqrt(d), go beside the slot: the softmax multiplies score
-//    column t by them in float32, so the scores carry no rounding of the
-//    scales. The descriptor's bf16 query tile is converted to f16 in place
-//    (exact for |q| in [2^-14, 65504]).
-//    The dequantised V values must lie within the f16 range (|v| <= 65504).
+//    k with k % 2 == g. The M = 64 layout puts query row r (= new token r / 8,
+//    head r % 8) in TMEM lane 32 (r / 16) + r % 16; the 16x256b load shape
+//    gives every thread of warp w half of rows 16 w + t / 4 and 16 w + t / 4 + 8
+//    (all 32 lanes busy; a row's max and sum combine its four threads). The
+//    warpgroup masks tokens past the chunk's valid count and each row's causal
+//    limit, and keeps a reference max m and sum l (log2 domain) per row for its
+//    chunks. P = exp2(s - m) goes to shared memory as 16-bit values, into one of
+//    the warpgroup's two P buffers; O_g is rescaled in TMEM only when a chunk's
+//    max exceeds m by more than 8 (so P <= 256), which after the first chunks
+//    is rare. At the descriptor's end warpgroup 1 publishes its (m, l) and
+//    warpgroup 0 merges both states and both O tiles into the partial rows and
+//    their LSEs.
+// e4m3 caches (one float32 scale per token and KV head), 15 warps, the same
+// roles with these changes:
+//  * warps 11-14, converter. Once per descriptor it splits each bf16 query row
+//    into two e4m3 tiles, Q = (Q_hi + Q_lo) x 2^e_r with a power-of-two row
+//    scale (exact to the bf16 input but for elements under 2^-11 of the row's
+//    maximum). Per chunk it widens the V codes of the e4m3 stage into an f16
+//    V slot (code x scale, rounded to f16; rows past the live length zero)
+//    and puts the chunk's K scales times log2(e)/sqrt(d) beside it. The
+//    dequantised V values must lie within the f16 range (|v| <= 65504).
+//  * S issuer: S = Q_hi . K^T + Q_lo . K^T as kind::f8f6f4 MMAs straight on
+//    the K codes of the stage (4 steps of 32 dims, each hi then lo), so K is
+//    never converted.
+//  * softmax: score column t is multiplied by its K scale factor in float32
+//    and the row by 2^e_r in the exponent, so the scores carry no rounding of
+//    the scales; P is f16 and P . V runs kind::f16 on the V slot.
 // Every wait is bounded (2 s); on expiry the CTA records
 // HPC_DEVERR_WAIT_TIMEOUT and, after a bounded drain, frees its TMEM and
 // returns.
 #include <atomic>
 #include <cstring>
+
+#include <cuda_fp8.h>
 
 #include "attn_common.cuh"
 
@@ -56,23 +63,27 @@ namespace {
 using namespace attn;
 
 constexpr int kQTile = 16384;            // [2 dim halves][64 rows][128 B]
+constexpr int kQ8Tile = 16384;           // e4m3: hi codes [64 rows][128 B], then lo codes
 constexpr int kPTile = 8192;             // [64 rows][64 tokens x 2 B]
-constexpr int kOpBytes = 32768;          // 16-bit K and V operand tiles of one chunk (a bf16 stage)
-constexpr uint32_t kTmemCols = 512;      // S buffers 2 x 64 columns, O tiles 2 x 128 columns
-constexpr uint32_t kOCol = 128;          // O tile g at column kOCol + 128 g
+constexpr int kPBufs = 4;                // two per softmax warpgroup
+constexpr int kSBufs = 3;                // TMEM score buffers: S_k goes to buffer k % 3
+constexpr uint32_t kTmemCols = 512;      // S buffers 3 x 64 columns, O tiles 2 x 128 columns
+constexpr uint32_t kOCol = 64 * kSBufs;  // O tile g at column kOCol + 128 g
+static_assert(kOCol + 256 <= kTmemCols, "TMEM columns");
 constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold: P <= 2^8
 constexpr int kSoftmaxThreads = 128;     // one warpgroup
 constexpr int kConvWarp0 = 11;           // first converter warp (e4m3 instances)
 constexpr int kConvThreads = 128;        // converter warpgroup
-constexpr int kCMeta = 8;                // meta[kCMeta + slot]: valid tokens of a converted slot
 
 template <bool FP8>
 struct TcCfg {
-    static constexpr int kStages = FP8 ? 6 : 4;                   // TMA ring depth
+    static constexpr int kStages = 4;                             // TMA ring depth
     static constexpr int kStageBytes = KvCfg<FP8>::kStageBytes;   // 17 KB e4m3, 32 KB bf16
-    // operand slots the MMAs read: the TMA stages themselves for bf16, two
-    // converted f16 slots for e4m3
-    static constexpr int kOpSlots = FP8 ? 2 : kStages;
+    // operand slots the P . V product reads V from: the TMA stages themselves
+    // for bf16, three f16 V slots for e4m3 (conversion runs ahead of the MMAs)
+    static constexpr int kOpSlots = FP8 ? 3 : kStages;
+    static constexpr int kOpBytes = FP8 ? 16384 : 32768;
+    static constexpr int kVOff = FP8 ? 0 : 16384;                 // V tile inside an operand slot
     static constexpr int kWarps = FP8 ? 15 : 11;
 };
 
@@ -81,24 +92,27 @@ struct TcLayout {
     using C = TcCfg<FP8>;
     static constexpr size_t kStages = 0;
     static constexpr size_t kOps = kStages + (size_t)C::kStages * C::kStageBytes;
-    static constexpr size_t kQ = kOps + (FP8 ? (size_t)C::kOpSlots * kOpBytes : 0);
-    static constexpr size_t kP = kQ + 2 * (size_t)kQTile;
-    static constexpr size_t kKsl = kP + 2 * (size_t)kPTile;  // float [op slot][64]: K scale x log2(e)/sqrt(d)
-    static constexpr size_t kML = kKsl + (FP8 ? (size_t)C::kOpSlots * 256 : 0);  // float2 [2 parities][64 rows]
-    static constexpr size_t kMeta = kML + 2 * 64 * 8;  // int: stage valid counts, then slot counts at kCMeta
+    static constexpr size_t kQ = kOps + (FP8 ? (size_t)C::kOpSlots * C::kOpBytes : 0);
+    static constexpr size_t kQ8 = kQ + 2 * (size_t)kQTile;
+    static constexpr size_t kP = kQ8 + (FP8 ? 2 * (size_t)kQ8Tile : 0);
+    static constexpr size_t kQsc = kP + kPBufs * (size_t)kPTile;  // float [2][64]: e4m3 Q row scales
+    static constexpr size_t kML = kQsc + (FP8 ? 2 * 256 : 0);  // float2 [2 parities][64 rows]
+    static constexpr size_t kMeta = kML + 2 * 64 * 8;  // int [stage]: valid tokens of the staged chunk
     static constexpr size_t kBars = kMeta + 128;
-    // full, empty (stages); qfull, qempty, sfull, sfree, pfull, pvdone, published, consumed (2 each); ofree;
-    // e4m3: cfull, cfree (op slots), qconv (2)
-    static constexpr int kNumBars = 2 * C::kStages + 16 + 1 + (FP8 ? 2 * C::kOpSlots + 2 : 0);
+    // full, empty (stages); qfull, qempty, published, consumed (2 each); sfull, sfree (one per S buffer);
+    // pfull, pvdone (one per P buffer); ofree; e4m3: cfull, cfree (op slots), q8full, qdone (2 each)
+    static constexpr int kNumBars =
+        2 * C::kStages + 8 + 2 * kSBufs + 2 * kPBufs + 1 + (FP8 ? 2 * C::kOpSlots + 4 : 0);
     static constexpr size_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr size_t kFlag = kTmemSlot + 8;
     static constexpr size_t kTotal = kFlag + 8;
     static constexpr size_t kAlloc = kTotal + 1024;
     static constexpr int kThreads = C::kWarps * 32;
     static_assert(kAlloc <= 232448, "over the 227 KB shared-memory limit of a CTA");
-    static_assert(kOps % 1024 == 0 && kQ % 1024 == 0 && kP % 1024 == 0, "swizzled tiles need 1 KB alignment");
-    static_assert(C::kStageBytes % 1024 == 0, "stages need 1 KB alignment");
-    static_assert(C::kStages <= kCMeta && C::kOpSlots <= 8, "meta words");
+    static_assert(kOps % 1024 == 0 && kQ % 1024 == 0 && kQ8 % 1024 == 0 && kP % 1024 == 0,
+                  "swizzled tiles need 1 KB alignment");
+    static_assert(C::kStageBytes % 1024 == 0 && C::kOpBytes % 1024 == 0, "stages and slots need 1 KB alignment");
+    static_assert(C::kStages <= 32, "meta words");
 };
 
 // ------------------------------------------------------------------ tcgen05 wrappers
@@ -133,6 +147,22 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b
         : "memory");
 }
 
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format 0), f32
+// accumulator, M x N, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) (+)= A . B^T, e4m3 operands from shared-memory descriptors (32
+// elements of K per instruction).
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // Arrives on bar once every MMA this thread issued before it has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -142,10 +172,12 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// 16x256b shape, 16 lanes from the warp's base lane: register 4 m + k of
+// thread t holds lane t / 4 (k < 2) or t / 4 + 8 (k >= 2), column
+// 8 m + 2 (t % 4) + (k & 1), for m < 8 (x8: 64 columns) or m < 4 (x4: 32).
+__device__ __forceinline__ void tmem_ld16_x8(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
@@ -155,23 +187,49 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld16_x4(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// bf16 pair -> f16 pair (exact for magnitudes in [2^-14, 65504]).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+// Eight floats (exact multiples of the row scale's inverse, |x| <= 448) ->
+// eight e4m3 "hi" codes (round to nearest even) and eight "lo" codes of the
+// remainders x - hi. A bf16 value has eight significant bits; rounding it to
+// e4m3's four leaves a remainder of at most four, so hi + lo is x exactly
+// unless the remainder falls below e4m3's smallest subnormal (2^-9), i.e. for
+// |x| < 2^-2 (elements under 2^-11 of the row maximum). Byte i of the
+// outputs holds element i.
+__device__ __forceinline__ void split_e4m3x8(const float (&x)[8], uint2& hi, uint2& lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const __nv_fp8x2_storage_t hc =
+            __nv_cvt_float2_to_fp8x2(make_float2(x[2 * j], x[2 * j + 1]), __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hc, __NV_E4M3);
+        const float2 hv = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_fp8x2_storage_t lc = __nv_cvt_float2_to_fp8x2(
+            make_float2(x[2 * j] - hv.x, x[2 * j + 1] - hv.y), __NV_SATFINITE, __NV_E4M3);
+        h[j] = hc;
+        l[j] = lc;
+    }
+    hi = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    lo = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
@@ -202,15 +260,19 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     uint64_t* qfull = empty + NS;
     uint64_t* qempty = qfull + 2;
     uint64_t* sfull = qempty + 2;
-    uint64_t* sfree = sfull + 2;
-    uint64_t* pfull = sfree + 2;
-    uint64_t* pvdone = pfull + 2;
-    uint64_t* published = pvdone + 2;
+    uint64_t* sfree = sfull + kSBufs;
+    uint64_t* pfull = sfree + kSBufs;
+    // pfull and pvdone: one per P buffer 2 g + j (chunks k with k % 2 = g and
+    // (k / 2) % 2 = j); a warpgroup refills a buffer only after the P . V that
+    // read it, so neither barrier can run two phases ahead of its waiter
+    uint64_t* pvdone = pfull + kPBufs;
+    uint64_t* published = pvdone + kPBufs;
     uint64_t* consumed = published + 2;
     uint64_t* ofree = consumed + 2;
     uint64_t* cfull = ofree + 1;      // e4m3: op slot converted
     uint64_t* cfree = cfull + NO;     // e4m3: op slot read by both MMAs
-    uint64_t* qconv = cfree + NO;     // e4m3: query tile converted to f16
+    uint64_t* q8full = cfree + NO;    // e4m3: query row split into hi / lo e4m3 tiles and scales
+    uint64_t* qdone = q8full + 2;     // e4m3: both softmax warpgroups finished a descriptor
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + LY::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kFlag);
     volatile int* meta = reinterpret_cast<volatile int*>(smem + LY::kMeta);
@@ -223,8 +285,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     uint8_t* const opbase = FP8 ? smem + LY::kOps : smem;
     uint64_t* const op_ready = FP8 ? cfull : full;
     uint64_t* const op_free = FP8 ? cfree : empty;
-    uint64_t* const q_ready = FP8 ? qconv : qfull;
-    volatile int* const op_meta = FP8 ? meta + kCMeta : meta;
+    uint64_t* const q_ready = FP8 ? q8full : qfull;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Q = p.q_len;
@@ -232,17 +293,23 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
             // bf16: released by the P . V issuer's commit; e4m3: by the converter
-            mbar_init(&empty[i], FP8 ? kConvThreads : 1);
+            // (V codes and scales read), the S issuer's commit (K codes read) and
+            // the chunk's softmax warpgroup (valid count and K scales read)
+            mbar_init(&empty[i], FP8 ? kConvThreads + 1 + kSoftmaxThreads : 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
-            mbar_init(&qempty[i], 1);
-            mbar_init(&sfull[i], 1);
-            mbar_init(&sfree[i], kSoftmaxThreads);
-            mbar_init(&pfull[i], kSoftmaxThreads);
-            mbar_init(&pvdone[i], 1);
+            mbar_init(&qempty[i], FP8 ? kConvThreads : 1);  // e4m3: the converter read the bf16 tile
             mbar_init(&published[i], kSoftmaxThreads);
             mbar_init(&consumed[i], kSoftmaxThreads);
+        }
+        for (int i = 0; i < kSBufs; ++i) {
+            mbar_init(&sfull[i], 1);
+            mbar_init(&sfree[i], kSoftmaxThreads);
+        }
+        for (int i = 0; i < kPBufs; ++i) {
+            mbar_init(&pfull[i], kSoftmaxThreads);
+            mbar_init(&pvdone[i], 1);
         }
         mbar_init(ofree, kSoftmaxThreads);
         if constexpr (FP8) {
@@ -250,13 +317,16 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 mbar_init(&cfull[i], kConvThreads);
                 mbar_init(&cfree[i], 1);
             }
-            for (int i = 0; i < 2; ++i) mbar_init(&qconv[i], kConvThreads);
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&q8full[i], kConvThreads);
+                mbar_init(&qdone[i], 2 * kSoftmaxThreads);
+            }
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     // P rows of dead query rows (r >= 8 q_len) stay zero for the whole kernel
-    for (int i = threadIdx.x; i < 2 * kPTile / 16; i += blockDim.x)
+    for (int i = threadIdx.x; i < kPBufs * kPTile / 16; i += blockDim.x)
         reinterpret_cast<uint4*>(pbuf)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 0) {
@@ -280,7 +350,9 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     } else if (warp == 9) {
         // ============================ S issuer (one thread): S_k = Q . K_k^T
         if (lane == 0) {
-            constexpr uint32_t kIdS = idesc_16bit(FP8, 64, 64, 0);
+            // bf16: Q . K^T in 8 steps of 16 dims; e4m3: (Q_hi + Q_lo) . K^T in 4
+            // steps of 32 dims on the K codes of the TMA stage
+            constexpr uint32_t kIdS = FP8 ? idesc_e4m3(64, 64) : idesc_16bit(false, 64, 64, 0);
             uint32_t seq = 0;  // chunks of this CTA
             int qd = 0;
             bool ok = true;
@@ -294,23 +366,40 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 ok = wait_bounded(&q_ready[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(qbuf + qs * kQTile);
+                const uint32_t qa = smem_u32(FP8 ? smem + LY::kQ8 + qs * kQ8Tile : qbuf + qs * kQTile);
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
-                    const uint32_t os = seq % NO;
-                    const uint32_t sb = seq & 1;
-                    ok = wait_bounded(&op_ready[os], (seq / NO) & 1, abort_flag, kWaitLimitNs);
-                    if (ok && seq >= 2) ok = wait_bounded(&sfree[sb], ((seq - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
+                    const uint32_t sb = seq % kSBufs;
+                    // bf16: the K tile of the chunk's stage; e4m3: its K codes
+                    const uint32_t ks_ = FP8 ? seq % NS : seq % NO;
+                    ok = wait_bounded(FP8 ? &full[ks_] : &op_ready[ks_], (seq / (FP8 ? NS : NO)) & 1, abort_flag,
+                                      kWaitLimitNs);
+                    if (ok && seq >= (uint32_t)kSBufs)
+                        ok = wait_bounded(&sfree[sb], (seq / kSBufs - 1) & 1, abort_flag, kWaitLimitNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t ka = smem_u32(opbase + (size_t)os * kOpBytes);
+                    if constexpr (FP8) {
+                        const uint32_t ka = smem_u32(smem + (size_t)ks_ * C::kStageBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
-                        umma_f16(tmem + sb * 64, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                                 kIdS, kk > 0);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t off = (uint32_t)kk * 32u;
+                            umma_e4m3(tmem + sb * 64, sdesc_sw128(qa + off, 16, 1024),
+                                      sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0);
+                            umma_e4m3(tmem + sb * 64, sdesc_sw128(qa + 8192 + off, 16, 1024),
+                                      sdesc_sw128(ka + off, 16, 1024), kIdS, 1);
+                        }
+                        umma_commit(&sfull[sb]);
+                        umma_commit(&empty[ks_]);  // the K codes are read once S is done
+                    } else {
+                        const uint32_t ka = smem_u32(opbase + (size_t)ks_ * C::kOpBytes);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t off = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
+                            umma_f16(tmem + sb * 64, sdesc_sw128(qa + off, 16, 1024),
+                                     sdesc_sw128(ka + off, 16, 1024), kIdS, kk > 0);
+                        }
+                        umma_commit(&sfull[sb]);
+                        if (cc + 1 == c1) umma_commit(&qempty[qs]);  // the query slot is free once S is done
                     }
-                    umma_commit(&sfull[sb]);
-                    if (cc + 1 == c1) umma_commit(&qempty[qs]);  // the query slot is free once S is done
                 }
                 ++qd;
             }
@@ -323,7 +412,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     } else if (warp == 10) {
         // ============================ P . V issuer (one thread): O_g += P_k . V_k
         if (lane == 0) {
-            constexpr uint32_t kIdO = idesc_16bit(FP8, 64, 128, 1);
+            constexpr uint32_t kIdO = idesc_16bit(FP8, 64, 128, 1);  // f16 P and V for e4m3 caches
             uint32_t seq = 0;
             int nd = 0;
             bool ok = true;
@@ -342,18 +431,22 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
                     const uint32_t os = seq % NO;
                     const uint32_t g = seq & 1;
-                    ok = wait_bounded(&pfull[g], (seq >> 1) & 1, abort_flag, kWaitLimitNs);
+                    const uint32_t pb = 2 * g + ((seq >> 1) & 1);  // P buffer of the chunk
+                    ok = wait_bounded(&pfull[pb], (seq >> 2) & 1, abort_flag, kWaitLimitNs);
+                    // e4m3: the converted V slot (bf16: the stage, waited by the softmax)
+                    if (FP8 && ok) ok = wait_bounded(&op_ready[os], (seq / NO) & 1, abort_flag, kWaitLimitNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t va = smem_u32(opbase + (size_t)os * kOpBytes + 16384);
-                    const uint32_t pa = smem_u32(pbuf + g * kPTile);
+                    const uint32_t va = smem_u32(opbase + (size_t)os * C::kOpBytes + C::kVOff);
+                    const uint32_t pa = smem_u32(pbuf + pb * kPTile);
                     const bool first = cc - c0 < 2;  // the first chunk of this parity overwrites
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_f16(tmem + kOCol + 128 * g, sdesc_sw128(pa + kk * 32, 16, 1024),
                                  sdesc_sw128(va + kk * 2048, 8192, 1024), kIdO, !first || kk > 0);
-                    umma_commit(&pvdone[g]);
-                    umma_commit(&op_free[os]);  // S_k finished before P_k was written
+                    umma_commit(&pvdone[pb]);
+                    // bf16: the stage (S_k finished before P_k was written); e4m3: the V slot
+                    umma_commit(&op_free[os]);
                 }
                 ++nd;
             }
@@ -364,11 +457,10 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
         }
         __syncwarp();
     } else if (warp >= kConvWarp0) {
-        // ============================ converter (e4m3 instances only): e4m3 stage ->
-        // f16 operand slot, bf16 query tile -> f16 in place
+        // ============================ converter (e4m3 instances only): bf16 query
+        // tile -> hi / lo e4m3 tiles and row scales; V codes -> f16 V slot
         if constexpr (FP8) {
             const int ct = threadIdx.x - kConvWarp0 * 32;
-            float* ksl = reinterpret_cast<float*>(smem + LY::kKsl);
             uint32_t seq = 0;
             int qd = 0;
             bool ok = true;
@@ -380,24 +472,70 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 if (!desc_ok(p, h, b, c0, c1, t1.x)) continue;
                 const int qs = qd & 1;
                 ok = wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs);
+                // the hi / lo tiles and row scales of slot qs were last used two
+                // descriptors ago: both softmax warpgroups must be done with it
+                if (ok && qd >= 2) ok = wait_bounded(&qdone[qs], ((qd - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 {
-                    // rows [0, 8 q_len) of both dim halves, 16-byte pieces (8 per row)
-                    uint8_t* qt = qbuf + qs * kQTile;
-                    const int npiece = kGroup * Q * 8;
-                    for (int i = ct; i < 2 * npiece; i += kConvThreads) {
-                        const int half = i >= npiece ? 1 : 0;
-                        uint4* ptr = reinterpret_cast<uint4*>(qt + half * 8192 + (i - half * npiece) * 16);
-                        uint4 v = *ptr;
-                        v.x = bf16x2_to_f16x2(v.x);
-                        v.y = bf16x2_to_f16x2(v.y);
-                        v.z = bf16x2_to_f16x2(v.z);
-                        v.w = bf16x2_to_f16x2(v.w);
-                        *ptr = v;
+                    // two threads per query row r, thread half hh takes dims [64 hh, 64 hh + 64)
+                    const int r = ct >> 1, hh = ct & 1;
+                    const bool in = r < kGroup * Q;
+                    const uint8_t* qb = qbuf + qs * kQTile + hh * 8192 + r * 128;
+                    uint8_t* q8 = smem + LY::kQ8 + qs * kQ8Tile;
+                    float amax = 0.f;
+                    if (in) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(qb + ((c ^ (r & 7)) << 4));
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                                         fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+                        }
+                    }
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    // the smallest power of two 2^ex with amax / 2^ex <= 448: q / 2^ex is exact
+                    float qscale = 1.f, qinv = 1.f;
+                    if (amax > 0.f && amax <= 3.0e38f) {
+                        int e;
+                        const float m = frexpf(amax * (1.f / 448.f), &e);
+                        const int ex = m == 0.5f ? e - 1 : e;
+                        qscale = ldexpf(1.f, ex);
+                        qinv = ldexpf(1.f, -ex);
+                    }
+                    if (hh == 0) reinterpret_cast<float*>(smem + LY::kQsc)[qs * 64 + r] = qscale;
+#pragma unroll
+                    for (int c2 = 0; c2 < 4; ++c2) {
+                        // bf16 pieces c = 2 c2 + u (dims 64 hh + 8 c ...) -> bytes 8 u of the
+                        // e4m3 row's 16-byte piece 4 hh + c2
+                        uint2 hp[2], lp[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            float x[8];
+                            if (in) {
+                                const int c = 2 * c2 + u;
+                                const uint4 v = *reinterpret_cast<const uint4*>(qb + ((c ^ (r & 7)) << 4));
+                                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    x[2 * j] = __uint_as_float(w[j] << 16) * qinv;
+                                    x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * qinv;
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) x[j] = 0.f;
+                            }
+                            split_e4m3x8(x, hp[u], lp[u]);
+                        }
+                        const int off = r * 128 + (((4 * hh + c2) ^ (r & 7)) << 4);
+                        *reinterpret_cast<uint4*>(q8 + off) = make_uint4(hp[0].x, hp[0].y, hp[1].x, hp[1].y);
+                        *reinterpret_cast<uint4*>(q8 + 8192 + off) = make_uint4(lp[0].x, lp[0].y, lp[1].x, lp[1].y);
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&qconv[qs]);
+                mbar_arrive(&qempty[qs]);  // the bf16 tile is read
+                mbar_arrive(&q8full[qs]);
                 ++qd;
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
                     const uint32_t st = seq % NS, os = seq % NO;
@@ -407,48 +545,47 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                     if (!ok) break;
                     const int nv = meta[st];  // 0: page id out of range (nothing loaded)
                     const uint8_t* sb = smem + (size_t)st * C::kStageBytes;
-                    uint8_t* ob = opbase + (size_t)os * kOpBytes;
-                    const float* ks = reinterpret_cast<const float*>(sb + 16384);
+                    uint8_t* ob = opbase + (size_t)os * C::kOpBytes;
                     const float* vs = reinterpret_cast<const float*>(sb + 16640);
-                    if (ct < kChunk) ksl[os * kChunk + ct] = ct < nv ? ks[ct] * p.scale_log2 : 0.f;
-                    // 1024 source pieces of 16 codes: K then V, 8 per 128-byte row; a
-                    // warp reads four whole rows per step
-#pragma unroll 2
-                    for (int i = ct; i < 1024; i += kConvThreads) {
-                        const int mat = i >> 9, row = (i >> 3) & 63, c16 = i & 7;
-                        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-                        if (row < nv) {
-                            const uint4 w = *reinterpret_cast<const uint4*>(sb + mat * 8192 + row * 128 +
-                                                                           ((c16 ^ (row & 7)) << 4));
-                            e4m3x4_to_f16x2x2(w.x, lo.x, lo.y);
-                            e4m3x4_to_f16x2x2(w.y, lo.z, lo.w);
-                            e4m3x4_to_f16x2x2(w.z, hi.x, hi.y);
-                            e4m3x4_to_f16x2x2(w.w, hi.z, hi.w);
-                            if (mat == 1) {
-                                const float sv = vs[row];
-                                const uint32_t s2 = pack_f16x2(sv, sv);
-                                lo.x = hmul2_u32(lo.x, s2);
-                                lo.y = hmul2_u32(lo.y, s2);
-                                lo.z = hmul2_u32(lo.z, s2);
-                                lo.w = hmul2_u32(lo.w, s2);
-                                hi.x = hmul2_u32(hi.x, s2);
-                                hi.y = hmul2_u32(hi.y, s2);
-                                hi.z = hmul2_u32(hi.z, s2);
-                                hi.w = hmul2_u32(hi.w, s2);
+                    // Thread ct takes the 16-code V pieces c16 = (ct & 3) + 4 hf of rows
+                    // 32 rr + ct / 4: a warp's loads cover 8 rows x 4 pieces and its
+                    // stores 8 rows x 4 f16 pieces, each in the minimum of four 16-byte
+                    // bank-group passes.
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int row = 32 * rr + (ct >> 2);
+                        const bool in = row < nv;
+                        const float sv = in ? vs[row] : 0.f;
+                        const uint32_t s2 = pack_f16x2(sv, sv);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int c16 = (ct & 3) + 4 * hf;
+                            uint4 vl = make_uint4(0, 0, 0, 0), vh = vl;
+                            if (in) {
+                                const uint4 vw = *reinterpret_cast<const uint4*>(sb + 8192 + row * 128 +
+                                                                                ((c16 ^ (row & 7)) << 4));
+                                e4m3x4_to_f16x2x2(vw.x, vl.x, vl.y);
+                                e4m3x4_to_f16x2x2(vw.y, vl.z, vl.w);
+                                e4m3x4_to_f16x2x2(vw.z, vh.x, vh.y);
+                                e4m3x4_to_f16x2x2(vw.w, vh.z, vh.w);
+                                vl.x = hmul2_u32(vl.x, s2);
+                                vl.y = hmul2_u32(vl.y, s2);
+                                vl.z = hmul2_u32(vl.z, s2);
+                                vl.w = hmul2_u32(vl.w, s2);
+                                vh.x = hmul2_u32(vh.x, s2);
+                                vh.y = hmul2_u32(vh.y, s2);
+                                vh.z = hmul2_u32(vh.z, s2);
+                                vh.w = hmul2_u32(vh.w, s2);
                             }
+                            // dims [16 c16, 16 c16 + 16) are f16 pieces f0 and f0 + 1 of dim
+                            // half hf, f0 = 2 (c16 & 3)
+                            const int f0 = 2 * (ct & 3);
+                            *reinterpret_cast<uint4*>(ob + hf * 8192 + row * 128 + ((f0 ^ (row & 7)) << 4)) = vl;
+                            *reinterpret_cast<uint4*>(ob + hf * 8192 + row * 128 + (((f0 + 1) ^ (row & 7)) << 4)) = vh;
                         }
-                        // dims [16 c16, 16 c16 + 16) = f16 pieces 2 (c16 & 3) and +1 of dim half
-                        // c16 >> 2; the second half stores its pieces in the other order, so
-                        // each store of a warp fills 8 distinct 16-byte bank groups per row
-                        const int half = c16 >> 2, f0 = 2 * (c16 & 3);
-                        uint8_t* rp = ob + mat * 16384 + half * 8192 + row * 128;
-                        const int pa = half ? f0 + 1 : f0, pb = half ? f0 : f0 + 1;
-                        *reinterpret_cast<uint4*>(rp + ((pa ^ (row & 7)) << 4)) = half ? hi : lo;
-                        *reinterpret_cast<uint4*>(rp + ((pb ^ (row & 7)) << 4)) = half ? lo : hi;
                     }
-                    if (ct == 0) op_meta[os] = nv;
                     fence_proxy_async_smem();
-                    mbar_arrive(&empty[st]);
+                    mbar_arrive(&empty[st]);  // V codes and scales read
                     mbar_arrive(&cfull[os]);
                 }
             }
@@ -459,17 +596,25 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
         }
     } else {
         // ============================ softmax warpgroups: g = warp / 4 takes the
-        // computed chunks k with k % 2 == g, into S buffer g, P buffer g and O tile g
+        // computed chunks k with k % 2 == g, from S buffer k % 3, into P buffer
+        // 2 g + (k / 2) % 2 and O tile g. The M = 64 accumulator holds query row i
+        // in TMEM lane 32 (i / 16) + i % 16; the 16x256b load shape spreads warp
+        // wq's 16 rows over all its threads: thread t holds half rows ra = 16 wq +
+        // t / 4 and rb = ra + 8 (query head t / 4 of new tokens 2 wq and 2 wq + 1),
+        // columns 8 m + 2 (t % 4) + {0, 1}, m < 8 (registers 4 m + {0, 1} of ra,
+        // 4 m + {2, 3} of rb). A row's max and sum combine its four threads.
         const int g = warp >> 2, wq = warp & 3;
         const int tg = threadIdx.x & (kSoftmaxThreads - 1);
-        const int r = 16 * wq + lane;            // query row (valid for lane < 16)
-        const bool live = lane < 16 && r < kGroup * Q;
-        const int qi = r >> 3;                   // new token of the row
+        const int hq = lane >> 2, cq = lane & 3;  // query head, column pair
+        const int ra = 16 * wq + hq, rb = ra + 8;  // query rows
+        const int qa = 2 * wq, qb = qa + 1;        // their new tokens
+        const bool live_a = qa < Q, live_b = qb < Q;
         const uint32_t lane_addr = (uint32_t)(32 * wq) << 16;
         const uint32_t ocol = kOCol + 128 * g;
         // bf16: raw scores times log2(e)/sqrt(d) in the exponent; e4m3: the score
-        // columns are already multiplied by their K scale times that factor
-        const float sc = FP8 ? 1.f : p.scale_log2;
+        // columns are multiplied by their K scales first, and the row's query
+        // scale joins log2(e)/sqrt(d) in the exponent
+        float sc_a = p.scale_log2, sc_b = p.scale_log2;
         uint32_t seq = 0;
         int nd = 0;
         for (int slot = list0;; ++slot) {
@@ -479,106 +624,145 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
             if (h < 0) break;
             if (!desc_ok(p, h, b, c0, c1, s)) continue;
             const int L = __ldg(p.seq_lens + b);
-            float m_ref = kNegInf, l_sum = 0.f;
+            // reference maxima (log2 domain) and this thread's part of the row sums
+            float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
+            if constexpr (FP8) {
+                // the rows' query scales, kept until both warpgroups arrive on qdone
+                if (!wait_bounded(&q8full[nd & 1], (nd >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                const float* qsc = reinterpret_cast<const float*>(smem + LY::kQsc) + (nd & 1) * 64;
+                sc_a = qsc[ra] * p.scale_log2;
+                sc_b = qsc[rb] * p.scale_log2;
+            }
             for (int cc = c0; cc < c1; ++cc, ++seq) {
                 if ((int)(seq & 1) != g) continue;
-                const uint32_t os = seq % NO;
-                // the slot's valid-token word: the slot is not refilled before this
-                // warpgroup releases P of this chunk, so waiting on its fill is exact
-                if (!wait_bounded(&op_ready[os], (seq / NO) & 1, abort_flag, kWaitLimitNs)) goto timeout;
-                if (!wait_bounded(&sfull[g], (seq >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                // the staged chunk's valid-token word (and, e4m3, its K scales): the
+                // stage is not refilled before this warpgroup releases it (e4m3) or
+                // releases P of this chunk (bf16), so waiting on its fill is exact
+                const uint32_t st = seq % NS;
+                if (!wait_bounded(&full[st], (seq / NS) & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                const uint32_t sbuf = seq % kSBufs;
+                if (!wait_bounded(&sfull[sbuf], (seq / kSBufs) & 1, abort_flag, kWaitLimitNs)) goto timeout;
                 tc_fence_after();
-                uint32_t sr[2][32];
-                tmem_ld32(tmem + lane_addr + g * 64, sr[0]);
-                tmem_ld32(tmem + lane_addr + g * 64 + 32, sr[1]);
+                uint32_t sr[32];
+                tmem_ld16_x8(tmem + lane_addr + sbuf * 64, sr);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&sfree[g]);
-                const int nv = op_meta[os];  // 0: page id out of range (nothing loaded)
+                mbar_arrive(&sfree[sbuf]);
+                const int nv = meta[st];  // 0: page id out of range (nothing loaded)
                 if constexpr (FP8) {
-                    const float4* kp = reinterpret_cast<const float4*>(smem + LY::kKsl + os * 256);
+                    // score column c times its K scale (tokens past nv are masked below)
+                    const float* ks = reinterpret_cast<const float*>(smem + (size_t)st * C::kStageBytes + 16384);
 #pragma unroll
-                    for (int t4 = 0; t4 < 16; ++t4) {
-                        const float4 f = kp[t4];
-                        const int t = 4 * t4;
-                        sr[t >> 5][t & 31] = __float_as_uint(__uint_as_float(sr[t >> 5][t & 31]) * f.x);
-                        sr[t >> 5][(t + 1) & 31] = __float_as_uint(__uint_as_float(sr[t >> 5][(t + 1) & 31]) * f.y);
-                        sr[t >> 5][(t + 2) & 31] = __float_as_uint(__uint_as_float(sr[t >> 5][(t + 2) & 31]) * f.z);
-                        sr[t >> 5][(t + 3) & 31] = __float_as_uint(__uint_as_float(sr[t >> 5][(t + 3) & 31]) * f.w);
+                    for (int m = 0; m < 8; ++m) {
+                        const float2 f = *reinterpret_cast<const float2*>(ks + 8 * m + 2 * cq);
+                        sr[4 * m] = __float_as_uint(__uint_as_float(sr[4 * m]) * f.x);
+                        sr[4 * m + 1] = __float_as_uint(__uint_as_float(sr[4 * m + 1]) * f.y);
+                        sr[4 * m + 2] = __float_as_uint(__uint_as_float(sr[4 * m + 2]) * f.x);
+                        sr[4 * m + 3] = __float_as_uint(__uint_as_float(sr[4 * m + 3]) * f.y);
+                    }
+                    mbar_arrive(&empty[st]);
+                }
+                // valid tokens of this chunk for each row: the chunk's and the causal limit;
+                // tokens past it get -inf (after any scale, which is positive); full
+                // chunks skip this
+                const int lim_a = min(nv, L - kChunk * cc - (Q - 1 - qa));
+                const int lim_b = min(nv, L - kChunk * cc - (Q - 1 - qb));
+                if (!__all_sync(0xffffffffu, lim_a >= kChunk && lim_b >= kChunk)) {
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const int c = 8 * m + 2 * cq;
+                        if (c >= lim_a) sr[4 * m] = __float_as_uint(kNegInf);
+                        if (c + 1 >= lim_a) sr[4 * m + 1] = __float_as_uint(kNegInf);
+                        if (c >= lim_b) sr[4 * m + 2] = __float_as_uint(kNegInf);
+                        if (c + 1 >= lim_b) sr[4 * m + 3] = __float_as_uint(kNegInf);
                     }
                 }
-                // valid tokens of this chunk for this row: the chunk's and the causal limit
-                const int lim = min(nv, L - kChunk * cc - (Q - 1 - qi));
-                // tokens past the limit get -inf (after any scale, which is positive and
-                // keeps the order); full chunks skip this
-                if (!__all_sync(0xffffffffu, !live || lim >= kChunk)) {
+                // row maxima: two chains per row over the thread's 16 columns, then the
+                // row's four threads
+                float ma0 = __uint_as_float(sr[0]), ma1 = __uint_as_float(sr[1]);
+                float mb0 = __uint_as_float(sr[2]), mb1 = __uint_as_float(sr[3]);
 #pragma unroll
-                    for (int t = 0; t < 64; ++t)
-                        if (t >= lim) sr[t >> 5][t & 31] = __float_as_uint(kNegInf);
+                for (int m = 1; m < 8; ++m) {
+                    ma0 = fmaxf(ma0, __uint_as_float(sr[4 * m]));
+                    ma1 = fmaxf(ma1, __uint_as_float(sr[4 * m + 1]));
+                    mb0 = fmaxf(mb0, __uint_as_float(sr[4 * m + 2]));
+                    mb1 = fmaxf(mb1, __uint_as_float(sr[4 * m + 3]));
                 }
-                // row max in eight independent chains, then a tree
-                float m8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    m8[j] = __uint_as_float(sr[0][j]);
-#pragma unroll
-                    for (int t = j + 8; t < 64; t += 8) m8[j] = fmaxf(m8[j], __uint_as_float(sr[t >> 5][t & 31]));
-                }
-                const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                float mx = mraw * sc;
-                if (!live) mx = kNegInf;
-                // P buffer g and O tile g were last used by this warpgroup's previous chunk
-                if (seq >= 2 && !wait_bounded(&pvdone[g], ((seq - 2) >> 1) & 1, abort_flag, kWaitLimitNs))
+                float mra = fmaxf(ma0, ma1), mrb = fmaxf(mb0, mb1);
+                mra = fmaxf(mra, __shfl_xor_sync(0xffffffffu, mra, 1));
+                mrb = fmaxf(mrb, __shfl_xor_sync(0xffffffffu, mrb, 1));
+                mra = fmaxf(mra, __shfl_xor_sync(0xffffffffu, mra, 2));
+                mrb = fmaxf(mrb, __shfl_xor_sync(0xffffffffu, mrb, 2));
+                const float mxa = live_a ? mra * sc_a : kNegInf;
+                const float mxb = live_b ? mrb * sc_b : kNegInf;
+                // this chunk's P buffer (2 g + pj) last served the chunk four back: its
+                // P . V must be done; the one two back may still run
+                const uint32_t pj = (seq >> 1) & 1;
+                if (seq >= 4 && !wait_bounded(&pvdone[2 * g + pj], ((seq >> 2) - 1) & 1, abort_flag, kWaitLimitNs))
                     goto timeout;
                 tc_fence_after();
-                // lazy rescale: move the reference max only when this chunk's max is far above it
-                const bool move = mx != kNegInf && (m_ref == kNegInf || mx > m_ref + kRescaleLog2);
-                const bool rescale_o = move && m_ref != kNegInf;
-                if (__any_sync(0xffffffffu, rescale_o)) {
-                    const float alpha = rescale_o ? fast_exp2(m_ref - mx) : 1.f;
+                // lazy rescale: move a reference max only when the chunk's max is far above it
+                const bool move_a = mxa != kNegInf && (m_a == kNegInf || mxa > m_a + kRescaleLog2);
+                const bool move_b = mxb != kNegInf && (m_b == kNegInf || mxb > m_b + kRescaleLog2);
+                const bool resc_a = move_a && m_a != kNegInf, resc_b = move_b && m_b != kNegInf;
+                if (__any_sync(0xffffffffu, resc_a || resc_b)) {
+                    // O tile g is final only once the P . V of the chunk two back is done
+                    if (seq >= 2 &&
+                        !wait_bounded(&pvdone[2 * g + (pj ^ 1)], ((seq - 2) >> 2) & 1, abort_flag, kWaitLimitNs))
+                        goto timeout;
+                    tc_fence_after();
+                    const float al_a = resc_a ? fast_exp2(m_a - mxa) : 1.f;
+                    const float al_b = resc_b ? fast_exp2(m_b - mxb) : 1.f;
 #pragma unroll 1
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_addr + ocol + 32 * c4, o);
+                    for (int c32 = 0; c32 < 4; ++c32) {
+                        uint32_t o[16];
+                        tmem_ld16_x4(tmem + lane_addr + ocol + 32 * c32, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-                        tmem_st32(tmem + lane_addr + ocol + 32 * c4, o);
+                        for (int j = 0; j < 16; ++j)
+                            o[j] = __float_as_uint(__uint_as_float(o[j]) * ((j & 2) ? al_b : al_a));
+                        tmem_st16_x4(tmem + lane_addr + ocol + 32 * c32, o);
                     }
                     tmem_st_wait();
                 }
-                if (move) {
-                    if (m_ref != kNegInf) l_sum *= fast_exp2(m_ref - mx);
-                    m_ref = mx;
+                if (move_a) {
+                    if (m_a != kNegInf) l_a *= fast_exp2(m_a - mxa);
+                    m_a = mxa;
                 }
-                if (live) {
-                    // P = exp2(s * scale - m), eight partial sums
-                    const float nmu = m_ref == kNegInf ? 0.f : -m_ref;
-                    uint8_t* prow = pbuf + g * kPTile + r * 128;
-                    float l8[8];
+                if (move_b) {
+                    if (m_b != kNegInf) l_b *= fast_exp2(m_b - mxb);
+                    m_b = mxb;
+                }
+                // P = exp2(s * scale - m) as 16-bit pairs; row r's columns 8 m .. 8 m + 7 are
+                // the 16-byte piece m of its 128-byte P row (swizzled), pair cq at byte 4 cq
+                {
+                    const float na = m_a == kNegInf ? 0.f : -m_a, nb = m_b == kNegInf ? 0.f : -m_b;
+                    uint8_t* pbase = pbuf + (2 * g + pj) * kPTile;
+                    float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) l8[j] = 0.f;
-#pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int t = 8 * c8 + 2 * u;
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[t >> 5][t & 31]), sc, nmu));
-                            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[(t + 1) >> 5][(t + 1) & 31]), sc, nmu));
-                            l8[2 * u] += p0;
-                            l8[2 * u + 1] += p1;
-                            w[u] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-                        }
-                        *reinterpret_cast<uint4*>(prow + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int m = 0; m < 8; ++m) {
+                        const float pa0 = fast_exp2(fmaf(__uint_as_float(sr[4 * m]), sc_a, na));
+                        const float pa1 = fast_exp2(fmaf(__uint_as_float(sr[4 * m + 1]), sc_a, na));
+                        const float pb0 = fast_exp2(fmaf(__uint_as_float(sr[4 * m + 2]), sc_b, nb));
+                        const float pb1 = fast_exp2(fmaf(__uint_as_float(sr[4 * m + 3]), sc_b, nb));
+                        sa0 += pa0;
+                        sa1 += pa1;
+                        sb0 += pb0;
+                        sb1 += pb1;
+                        if (live_a)
+                            *reinterpret_cast<uint32_t*>(pbase + ra * 128 + ((m ^ (ra & 7)) << 4) + 4 * cq) =
+                                FP8 ? pack_f16x2(pa0, pa1) : pack_bf16x2(pa0, pa1);
+                        if (live_b)
+                            *reinterpret_cast<uint32_t*>(pbase + rb * 128 + ((m ^ (rb & 7)) << 4) + 4 * cq) =
+                                FP8 ? pack_f16x2(pb0, pb1) : pack_bf16x2(pb0, pb1);
                     }
-                    l_sum += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+                    l_a += sa0 + sa1;
+                    l_b += sb0 + sb1;
                 }
                 // rows of the last page past the live length may hold any bits: zero them
                 // in V (the e4m3 converter already wrote zeros there)
                 if (!FP8 && nv < kChunk) {
-                    uint8_t* vst = opbase + (size_t)os * kOpBytes + 16384;
+                    uint8_t* vst = opbase + (size_t)st * C::kOpBytes + C::kVOff;  // bf16: the stage
                     const int nz = (kChunk - nv) * 16;  // 16-byte pieces over both dim halves
                     for (int i = tg; i < nz; i += kSoftmaxThreads) {
                         const int row = nv + i / 16, part = i % 16;
@@ -588,63 +772,94 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&pfull[g]);
+                mbar_arrive(&pfull[2 * g + pj]);
             }
+            // the rows' sums over their four threads
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+            l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+            l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
             if (g == 1) {
                 // ---- publish this warpgroup's (m, l) of the descriptor for warpgroup 0,
                 // once warpgroup 0 has read what this slot held two descriptors ago
                 if (nd >= 2 && !wait_bounded(&consumed[nd & 1], ((nd - 2) >> 1) & 1, abort_flag, kWaitLimitNs))
                     goto timeout;
-                if (lane < 16) mlx[(nd & 1) * 64 + r] = make_float2(m_ref, l_sum);
+                if (cq == 0) {
+                    mlx[(nd & 1) * 64 + ra] = make_float2(m_a, l_a);
+                    mlx[(nd & 1) * 64 + rb] = make_float2(m_b, l_b);
+                }
                 mbar_arrive(&published[nd & 1]);
             } else {
                 // ---- epilogue: merge the two warpgroups' states and O tiles
                 if (!wait_bounded(&published[nd & 1], (nd >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
                 const uint32_t k_last = seq - 1;  // every P . V of the descriptor is done with it
-                if (!wait_bounded(&pvdone[k_last & 1], (k_last >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                if (!wait_bounded(&pvdone[2 * (k_last & 1) + ((k_last >> 1) & 1)], (k_last >> 2) & 1, abort_flag,
+                                  kWaitLimitNs))
+                    goto timeout;
                 tc_fence_after();
                 // a warpgroup without a chunk in this descriptor published (-inf, 0) and
                 // its O tile holds another descriptor's bits: weight 0, never multiplied
-                const float2 other = mlx[(nd & 1) * 64 + (r & 63)];
-                const float m1 = other.x, l1 = other.y;
+                const float2 oa = mlx[(nd & 1) * 64 + ra], ob = mlx[(nd & 1) * 64 + rb];
                 mbar_arrive(&consumed[nd & 1]);
-                const float M = fmaxf(m_ref, m1);
-                const float f0 = l_sum > 0.f ? fast_exp2(m_ref - M) : 0.f;
-                const float f1 = l1 > 0.f ? fast_exp2(m1 - M) : 0.f;
-                const float lt = f0 * l_sum + f1 * l1;
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
-                const float w0 = f0 * inv, w1 = f1 * inv;
-                float* dst = p.split_o + (((long long)s * Q + qi) * kGroup + (r & 7)) * kHeadDim;
+                float w0a, w1a, w0b, w1b, lsa, lsb;
+                {
+                    const float M = fmaxf(m_a, oa.x);
+                    const float f0 = l_a > 0.f ? fast_exp2(m_a - M) : 0.f;
+                    const float f1 = oa.y > 0.f ? fast_exp2(oa.x - M) : 0.f;
+                    const float lt = f0 * l_a + f1 * oa.y;
+                    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                    w0a = f0 * inv;
+                    w1a = f1 * inv;
+                    lsa = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+                }
+                {
+                    const float M = fmaxf(m_b, ob.x);
+                    const float f0 = l_b > 0.f ? fast_exp2(m_b - M) : 0.f;
+                    const float f1 = ob.y > 0.f ? fast_exp2(ob.x - M) : 0.f;
+                    const float lt = f0 * l_b + f1 * ob.y;
+                    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                    w0b = f0 * inv;
+                    w1b = f1 * inv;
+                    lsb = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+                }
+                float* dst_a = p.split_o + (((long long)s * Q + qa) * kGroup + hq) * kHeadDim;
+                float* dst_b = p.split_o + (((long long)s * Q + qb) * kGroup + hq) * kHeadDim;
 #pragma unroll 1
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t o0[32], o1[32];
-                    tmem_ld32(tmem + lane_addr + kOCol + 32 * c4, o0);
-                    tmem_ld32(tmem + lane_addr + kOCol + 128 + 32 * c4, o1);
+                for (int c32 = 0; c32 < 4; ++c32) {
+                    uint32_t o0[16], o1[16];
+                    tmem_ld16_x4(tmem + lane_addr + kOCol + 32 * c32, o0);
+                    tmem_ld16_x4(tmem + lane_addr + kOCol + 128 + 32 * c32, o1);
                     tmem_ld_wait();
-                    if (live) {
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            float4 v;
-                            v.x = w0 * __uint_as_float(o0[j]) + (w1 != 0.f ? w1 * __uint_as_float(o1[j]) : 0.f);
-                            v.y = w0 * __uint_as_float(o0[j + 1]) + (w1 != 0.f ? w1 * __uint_as_float(o1[j + 1]) : 0.f);
-                            v.z = w0 * __uint_as_float(o0[j + 2]) + (w1 != 0.f ? w1 * __uint_as_float(o1[j + 2]) : 0.f);
-                            v.w = w0 * __uint_as_float(o0[j + 3]) + (w1 != 0.f ? w1 * __uint_as_float(o1[j + 3]) : 0.f);
-                            if (w0 == 0.f) {  // tile 0 holds nothing of this row: ignore its bits
-                                v.x = w1 * __uint_as_float(o1[j]);
-                                v.y = w1 * __uint_as_float(o1[j + 1]);
-                                v.z = w1 * __uint_as_float(o1[j + 2]);
-                                v.w = w1 * __uint_as_float(o1[j + 3]);
-                                if (w1 == 0.f) v = make_float4(0.f, 0.f, 0.f, 0.f);
-                            }
-                            *reinterpret_cast<float4*>(dst + 32 * c4 + j) = v;
+                    for (int m = 0; m < 4; ++m) {
+                        const int col = 32 * c32 + 8 * m + 2 * cq;
+                        // a tile whose weight is 0 may hold any bits: never multiplied
+                        if (live_a) {
+                            float2 v;
+                            v.x = (w0a != 0.f ? w0a * __uint_as_float(o0[4 * m]) : 0.f) +
+                                  (w1a != 0.f ? w1a * __uint_as_float(o1[4 * m]) : 0.f);
+                            v.y = (w0a != 0.f ? w0a * __uint_as_float(o0[4 * m + 1]) : 0.f) +
+                                  (w1a != 0.f ? w1a * __uint_as_float(o1[4 * m + 1]) : 0.f);
+                            *reinterpret_cast<float2*>(dst_a + col) = v;
+                        }
+                        if (live_b) {
+                            float2 v;
+                            v.x = (w0b != 0.f ? w0b * __uint_as_float(o0[4 * m + 2]) : 0.f) +
+                                  (w1b != 0.f ? w1b * __uint_as_float(o1[4 * m + 2]) : 0.f);
+                            v.y = (w0b != 0.f ? w0b * __uint_as_float(o0[4 * m + 3]) : 0.f) +
+                                  (w1b != 0.f ? w1b * __uint_as_float(o1[4 * m + 3]) : 0.f);
+                            *reinterpret_cast<float2*>(dst_b + col) = v;
                         }
                     }
                 }
-                if (live)
-                    p.split_lse[((long long)s * Q + qi) * kGroup + (r & 7)] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+                if (cq == 0) {
+                    if (live_a) p.split_lse[((long long)s * Q + qa) * kGroup + hq] = lsa;
+                    if (live_b) p.split_lse[((long long)s * Q + qb) * kGroup + hq] = lsb;
+                }
                 tc_fence_before();
                 mbar_arrive(ofree);
             }
+            if constexpr (FP8) mbar_arrive(&qdone[nd & 1]);  // this descriptor's query slot is free
             ++nd;
         }
         goto done;
