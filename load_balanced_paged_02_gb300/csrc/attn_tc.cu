@@ -63,7 +63,6 @@ namespace {
 using namespace attn;
 
 constexpr int kQTile = 16384;            // [2 dim halves][64 rows][128 B]
-constexpr int kQ8Tile = 16384;           // e4m3: hi codes [64 rows][128 B], then lo codes
 constexpr int kPTile = 8192;             // [64 rows][64 tokens x 2 B]
 constexpr int kPBufs = 4;                // two per softmax warpgroup
 constexpr int kSBufs = 3;                // TMEM score buffers: S_k goes to buffer k % 3
@@ -77,7 +76,7 @@ constexpr int kConvThreads = 128;        // converter warpgroup
 
 template <bool FP8>
 struct TcCfg {
-    static constexpr int kStages = 4;                             // TMA ring depth
+    static constexpr int kStages = FP8 ? 6 : 4;                   // TMA ring depth
     static constexpr int kStageBytes = KvCfg<FP8>::kStageBytes;   // 17 KB e4m3, 32 KB bf16
     // operand slots the P . V product reads V from: the TMA stages themselves
     // for bf16, three f16 V slots for e4m3 (conversion runs ahead of the MMAs)
@@ -93,8 +92,7 @@ struct TcLayout {
     static constexpr size_t kStages = 0;
     static constexpr size_t kOps = kStages + (size_t)C::kStages * C::kStageBytes;
     static constexpr size_t kQ = kOps + (FP8 ? (size_t)C::kOpSlots * C::kOpBytes : 0);
-    static constexpr size_t kQ8 = kQ + 2 * (size_t)kQTile;
-    static constexpr size_t kP = kQ8 + (FP8 ? 2 * (size_t)kQ8Tile : 0);
+    static constexpr size_t kP = kQ + 2 * (size_t)kQTile;
     static constexpr size_t kQsc = kP + kPBufs * (size_t)kPTile;  // float [2][64]: e4m3 Q row scales
     static constexpr size_t kML = kQsc + (FP8 ? 2 * 256 : 0);  // float2 [2 parities][64 rows]
     static constexpr size_t kMeta = kML + 2 * 64 * 8;  // int [stage]: valid tokens of the staged chunk
@@ -109,7 +107,7 @@ struct TcLayout {
     static constexpr size_t kAlloc = kTotal + 1024;
     static constexpr int kThreads = C::kWarps * 32;
     static_assert(kAlloc <= 232448, "over the 227 KB shared-memory limit of a CTA");
-    static_assert(kOps % 1024 == 0 && kQ % 1024 == 0 && kQ8 % 1024 == 0 && kP % 1024 == 0,
+    static_assert(kOps % 1024 == 0 && kQ % 1024 == 0 && kP % 1024 == 0,
                   "swizzled tiles need 1 KB alignment");
     static_assert(C::kStageBytes % 1024 == 0 && C::kOpBytes % 1024 == 0, "stages and slots need 1 KB alignment");
     static_assert(C::kStages <= 32, "meta words");
@@ -272,7 +270,9 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     uint64_t* cfull = ofree + 1;      // e4m3: op slot converted
     uint64_t* cfree = cfull + NO;     // e4m3: op slot read by both MMAs
     uint64_t* q8full = cfree + NO;    // e4m3: query row split into hi / lo e4m3 tiles and scales
-    uint64_t* qdone = q8full + 2;     // e4m3: both softmax warpgroups finished a descriptor
+    // e4m3: both softmax warpgroups finished a descriptor, so its query slot
+    // (split in place) is free for the producer
+    uint64_t* qdone = q8full + 2;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + LY::kTmemSlot);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kFlag);
     volatile int* meta = reinterpret_cast<volatile int*>(smem + LY::kMeta);
@@ -299,7 +299,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
-            mbar_init(&qempty[i], FP8 ? kConvThreads : 1);  // e4m3: the converter read the bf16 tile
+            mbar_init(&qempty[i], 1);  // bf16 only (e4m3 frees query slots through qdone)
             mbar_init(&published[i], kSoftmaxThreads);
             mbar_init(&consumed[i], kSoftmaxThreads);
         }
@@ -346,7 +346,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
 
     if (warp == 8) {
         produce<FP8, NS, QStage::kBf16Tile>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, list0, lane, smem, qbuf, kQTile, full,
-                                            empty, qfull, qempty, meta, abort_flag, &tm_q);
+                                            empty, qfull, FP8 ? qdone : qempty, meta, abort_flag, &tm_q);
     } else if (warp == 9) {
         // ============================ S issuer (one thread): S_k = Q . K_k^T
         if (lane == 0) {
@@ -366,7 +366,8 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 ok = wait_bounded(&q_ready[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t qa = smem_u32(FP8 ? smem + LY::kQ8 + qs * kQ8Tile : qbuf + qs * kQTile);
+                // e4m3: the slot holds the hi codes [64 rows][128 B], then the lo codes
+                const uint32_t qa = smem_u32(qbuf + qs * kQTile);
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
                     const uint32_t sb = seq % kSBufs;
                     // bf16: the K tile of the chunk's stage; e4m3: its K codes
@@ -471,30 +472,32 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 if (h < 0) break;
                 if (!desc_ok(p, h, b, c0, c1, t1.x)) continue;
                 const int qs = qd & 1;
+                // (the producer refills slot qs only after both softmax warpgroups
+                // finished the descriptor two back)
                 ok = wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs);
-                // the hi / lo tiles and row scales of slot qs were last used two
-                // descriptors ago: both softmax warpgroups must be done with it
-                if (ok && qd >= 2) ok = wait_bounded(&qdone[qs], ((qd - 2) >> 1) & 1, abort_flag, kWaitLimitNs);
                 if (!ok) break;
                 {
-                    // two threads per query row r, thread half hh takes dims [64 hh, 64 hh + 64)
+                    // In place: two threads per query row r, half hh reads bf16 dims
+                    // [64 hh, 64 hh + 64), which sit where row r of the hi tile (hh = 0)
+                    // or of the lo tile (hh = 1) goes; each thread writes the hi and lo
+                    // codes of its dims after both threads of the row have read.
                     const int r = ct >> 1, hh = ct & 1;
                     const bool in = r < kGroup * Q;
-                    const uint8_t* qb = qbuf + qs * kQTile + hh * 8192 + r * 128;
-                    uint8_t* q8 = smem + LY::kQ8 + qs * kQ8Tile;
+                    uint8_t* qt = qbuf + qs * kQTile;
+                    uint4 raw[8];
                     float amax = 0.f;
-                    if (in) {
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(qb + ((c ^ (r & 7)) << 4));
-                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    for (int c = 0; c < 8; ++c) {
+                        raw[c] = in ? *reinterpret_cast<const uint4*>(qt + hh * 8192 + r * 128 + ((c ^ (r & 7)) << 4))
+                                    : make_uint4(0, 0, 0, 0);
+                        const uint32_t w[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
-                                                         fabsf(__uint_as_float(w[j] & 0xffff0000u))));
-                        }
+                        for (int j = 0; j < 4; ++j)
+                            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[j] << 16)),
+                                                     fabsf(__uint_as_float(w[j] & 0xffff0000u))));
                     }
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                    __syncwarp();  // the partner has read its half row
                     // the smallest power of two 2^ex with amax / 2^ex <= 448: q / 2^ex is exact
                     float qscale = 1.f, qinv = 1.f;
                     if (amax > 0.f && amax <= 3.0e38f) {
@@ -512,29 +515,22 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                         uint2 hp[2], lp[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
+                            const uint4 v = raw[2 * c2 + u];
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                             float x[8];
-                            if (in) {
-                                const int c = 2 * c2 + u;
-                                const uint4 v = *reinterpret_cast<const uint4*>(qb + ((c ^ (r & 7)) << 4));
-                                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    x[2 * j] = __uint_as_float(w[j] << 16) * qinv;
-                                    x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * qinv;
-                                }
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 8; ++j) x[j] = 0.f;
+                            for (int j = 0; j < 4; ++j) {
+                                x[2 * j] = __uint_as_float(w[j] << 16) * qinv;
+                                x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * qinv;
                             }
                             split_e4m3x8(x, hp[u], lp[u]);
                         }
                         const int off = r * 128 + (((4 * hh + c2) ^ (r & 7)) << 4);
-                        *reinterpret_cast<uint4*>(q8 + off) = make_uint4(hp[0].x, hp[0].y, hp[1].x, hp[1].y);
-                        *reinterpret_cast<uint4*>(q8 + 8192 + off) = make_uint4(lp[0].x, lp[0].y, lp[1].x, lp[1].y);
+                        *reinterpret_cast<uint4*>(qt + off) = make_uint4(hp[0].x, hp[0].y, hp[1].x, hp[1].y);
+                        *reinterpret_cast<uint4*>(qt + 8192 + off) = make_uint4(lp[0].x, lp[0].y, lp[1].x, lp[1].y);
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&qempty[qs]);  // the bf16 tile is read
                 mbar_arrive(&q8full[qs]);
                 ++qd;
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
