@@ -178,7 +178,16 @@ def measured_peaks():
 KERNEL_SOURCES = {
     "decode_attn_kernel": ("attn.cu", "attn_common.cuh", "hpc_internal.cuh"),
     "decode_attn_mt_kernel": ("attn_mt.cu", "attn_common.cuh", "hpc_internal.cuh"),
+    "decode_attn_tc_kernel": ("attn_tc.cu", "attn_common.cuh", "hpc_internal.cuh"),
 }
+
+
+def attn_kernel_name(kv_dtype, q_len):
+    """The attention kernel the library's automatic engine choice launches."""
+    from load_balanced_paged_02_gb300 import binding as hb
+    if hb.auto_engine(kv_dtype, q_len) == hb.ENGINE_TCGEN05:
+        return "decode_attn_tc_kernel"
+    return "decode_attn_kernel" if q_len == 1 else "decode_attn_mt_kernel"
 
 
 def kernel_source_hash(kernel="decode_attn_kernel"):
@@ -361,10 +370,14 @@ def multi_token_timing(w, case, plan, C, dev, q_lens=(2, 6), n_rep=100):
         byt = step_bytes(lens, wq, n_splits)
         gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
         flops = 4.0 * float(np.maximum(lens, 0).sum()) * w.num_q_heads * Q * 128  # QK^T and PV
+        kvd = hb.kv_dtype_of(case["k_cache"])
+        kname = attn_kernel_name(kvd, Q)
         res[f"q_len_{Q}"] = {"attn_us": attn_us, "combine_us": comb_us, "layer_graph_us": layer_us,
                              "attn_gbs": gbs, "frac_of_peak": gbs / peak,
                              "mma_tflops": flops / (attn_us * 1e-6) / 1e12,
-                             "algorithmic_bytes_per_launch": byt["attn"]}
+                             "algorithmic_bytes_per_launch": byt["attn"], "kernel": kname,
+                             "traffic": recorded_traffic(f"{w.name}:qlen{Q}",
+                                                         "bf16" if kvd == hb.KV_BF16 else "e4m3", kname)}
         del so, sl, out, lse, q, g
     return res
 
@@ -523,7 +536,7 @@ def run_ours(args):
     value = units_all / (ms_step * 1e-3) / 1e9
     attn_gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
 
-    kname = "decode_attn_kernel" if w.q_len == 1 else "decode_attn_mt_kernel"
+    kname = attn_kernel_name(kvd, w.q_len)
     result = None
     if rank == 0:
         clocks = clk.summary()

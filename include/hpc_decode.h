@@ -262,6 +262,13 @@ hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_
                                         const hpc_plan* plan, float* split_o, float* split_lse,
                                         int engine, void* stream);
 
+/* The kernel HPC_ENGINE_AUTO runs for a cache dtype and q_len new tokens per
+ * request: HPC_ENGINE_MMA_SYNC or HPC_ENGINE_TCGEN05 (the measured faster one;
+ * q_len = 1 runs hpc_decode_attn's kernel, reported as HPC_ENGINE_MMA_SYNC).
+ * Returns 0 for an unknown kv_dtype or q_len outside [1, HPC_MAX_Q_LEN]. Host
+ * only, no device call. */
+int hpc_decode_attn_multi_auto_engine(int kv_dtype, int q_len);
+
 /*
  * Combine ([SGL] the paragraph on execution; [VLLM] combine stage). For every
  * (request b, query head qh) with h = qh / 8, j = qh % 8 and the pair's

@@ -48,6 +48,7 @@ SIGNATURES = {
     "hpc_decode_plan_bytes": (_sz, [_i, _i, _i]),
     "hpc_decode_split_capacity": (_sz, [_i, _i, _i]),
     "hpc_decode_default_num_ctas": (_i, [_i]),
+    "hpc_decode_attn_multi_auto_engine": (_i, [_i, _i]),
     "hpc_decode_plan": (_i, [_vp, _i, _i, _i, _i, _P, _vp]),
     "hpc_decode_plan_static": (_i, [_vp, _i, _i, _i, _P, _vp]),
     "hpc_decode_attn": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _P,
@@ -131,6 +132,14 @@ def kv_dtype_of(cache: torch.Tensor) -> int:
 
 def sm_count(device=None) -> int:
     return torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count
+
+
+def auto_engine(kv_dtype: int, q_len: int) -> int:
+    """ENGINE_MMA_SYNC or ENGINE_TCGEN05: the kernel ENGINE_AUTO runs."""
+    e = lib().hpc_decode_attn_multi_auto_engine(kv_dtype, q_len)
+    if e == 0:
+        raise HpcError("hpc_decode_attn_multi_auto_engine", detail=f"kv_dtype {kv_dtype}, q_len {q_len}")
+    return e
 
 
 def default_num_ctas(kv_dtype: int = KV_BF16) -> int:

@@ -225,6 +225,12 @@ hpc_status hpc_decode_attn_multi(const void* q, int q_len, const void* k_cache, 
                        split_o, split_lse, stream, q_len);
 }
 
+int hpc_decode_attn_multi_auto_engine(int kv_dtype, int q_len) {
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return 0;
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN) return 0;
+    return multi_engine_for(kv_dtype == HPC_KV_FP8_E4M3, q_len);
+}
+
 hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_cache, const void* v_cache,
                                         const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
                                         const int32_t* page_table, int page_table_stride, const int32_t* seq_lens,

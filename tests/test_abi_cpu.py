@@ -52,6 +52,17 @@ def test_plan_bytes_match_layout(L):
     assert L.hpc_decode_plan_bytes(1, 1, 0) == 0
 
 
+def test_auto_engine_choice(L):
+    """Warp-level kernels for one and two new tokens, tcgen05 from three, for
+    both cache dtypes; bad arguments give 0."""
+    for kvd in (hb.KV_BF16, hb.KV_FP8_E4M3):
+        assert [L.hpc_decode_attn_multi_auto_engine(kvd, q) for q in range(1, 9)] == \
+            [hb.ENGINE_MMA_SYNC] * 2 + [hb.ENGINE_TCGEN05] * 6
+        assert L.hpc_decode_attn_multi_auto_engine(kvd, 0) == 0
+        assert L.hpc_decode_attn_multi_auto_engine(kvd, 9) == 0
+    assert L.hpc_decode_attn_multi_auto_engine(7, 3) == 0
+
+
 def test_status_strings(L):
     for code in range(6):
         assert L.hpc_status_string(code)
