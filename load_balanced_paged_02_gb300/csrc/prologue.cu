@@ -8,9 +8,10 @@
 //
 // One block per token. A half-warp owns one (token, head) row, lane k of the
 // half owning dims [8k, 8k+8) (16-byte loads and stores); a warp covers two
-// rows per round and the block's 8 warps cover 16 rows per round, every round
-// loaded before any is processed. The token's position, slot, rotary row and
-// the norm weights are loaded once per block. Reductions (norm sum, e4m3
+// rows per round and the block's 8 warps cover 16 rows per round; the five
+// rounds of a Hy3 token (80 rows) are all loaded before any is processed, so
+// a block waits on memory once. The token's position, slot and rotary row are
+// loaded once per block, the norm weights per row from L1. Reductions (norm sum, e4m3
 // absolute max) take four xor-shuffle steps inside the half-warp, and the
 // rotation partner of dim d (d +- 64) lives in lane ^ 8. Row kinds (query,
 // key, value) are per-lane predicates, so all lanes run every shuffle.
@@ -21,7 +22,7 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 constexpr int kRowsPerRound = 2 * kWarpsPerBlock;  // one row per half-warp
-constexpr int kMaxRounds = 4;                        // rounds loaded before any is processed
+constexpr int kMaxRounds = 5;                        // rounds loaded before any is processed (80 rows)
 constexpr float kE4m3Max = 448.f;
 
 struct PrologueParams {
@@ -96,8 +97,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) rope_norm_kernel(const
         if (!rotate) atomicOr(p.err, (int)HPC_DEVERR_BAD_POSITION);
         if (slot >= 0 && !slot_ok) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
     }
-    // per-lane constants: rotation cos/sin, norm weights for dims [8*hl, 8*hl+8)
-    float c[8], sn[8], qw[8], kw[8];
+    // per-lane constants: rotation cos/sin for dims [8*hl, 8*hl+8) (the norm
+    // weights are read per row from L1, which keeps the registers for the rows
+    // in flight)
+    float c[8], sn[8];
     {
         const int i0 = (8 * hl) & 63;
         const float* cs = p.cos_sin + (long long)(rotate ? pos : 0) * kHeadDim;
@@ -106,17 +109,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) rope_norm_kernel(const
         const float4 s1 = *reinterpret_cast<const float4*>(cs + 64 + i0 + 4);
         const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
         const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const float4 q0 = *reinterpret_cast<const float4*>(p.qw + 8 * hl), q1 = *reinterpret_cast<const float4*>(p.qw + 8 * hl + 4);
-        const float4 k0 = *reinterpret_cast<const float4*>(p.kw + 8 * hl), k1 = *reinterpret_cast<const float4*>(p.kw + 8 * hl + 4);
-        const float qq[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const float kk[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
         const float sign = hl < 8 ? -1.f : 1.f;  // first half of the dims: x_i c - x_{i+64} s
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             c[k] = rotate ? cc[k] : 1.f;
             sn[k] = rotate ? sign * ss[k] : 0.f;
-            qw[k] = qq[k];
-            kw[k] = kk[k];
         }
     }
     for (int r0 = first; r0 < rounds; r0 += kMaxRounds) {
@@ -142,8 +139,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) rope_norm_kernel(const
             for (int k = 0; k < 8; ++k) s2 += y[k] * y[k];
             s2 = half_sum(s2);
             const float inv = is_qk ? rsqrtf(s2 * (1.f / kHeadDim) + p.eps) : 1.f;
+            if (is_qk) {
+                const float* wr = (is_q ? p.qw : p.kw) + 8 * hl;
+                const float4 w0 = __ldg(reinterpret_cast<const float4*>(wr));
+                const float4 w1 = __ldg(reinterpret_cast<const float4*>(wr + 4));
+                const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) y[k] *= is_qk ? inv * (is_q ? qw[k] : kw[k]) : 1.f;
+                for (int k = 0; k < 8; ++k) y[k] *= inv * ww[k];
+            }
             // rotary embedding on pairs (i, i + 64)
             float pr[8];
 #pragma unroll
