@@ -71,19 +71,19 @@ constexpr uint32_t kOCol = 64 * kSBufs;  // O tile g at column kOCol + 128 g
 static_assert(kOCol + 256 <= kTmemCols, "TMEM columns");
 constexpr float kRescaleLog2 = 8.0f;     // lazy rescale threshold: P <= 2^8
 constexpr int kSoftmaxThreads = 128;     // one warpgroup
-constexpr int kConvWarp0 = 11;           // first converter warp (e4m3 instances)
-constexpr int kConvThreads = 128;        // converter warpgroup
+constexpr int kSplitWarp = 11;           // e4m3: the warp that splits each descriptor's query
 
 template <bool FP8>
 struct TcCfg {
-    static constexpr int kStages = FP8 ? 6 : 4;                   // TMA ring depth
+    static constexpr int kStages = FP8 ? 5 : 4;                   // TMA ring depth
     static constexpr int kStageBytes = KvCfg<FP8>::kStageBytes;   // 17 KB e4m3, 32 KB bf16
     // operand slots the P . V product reads V from: the TMA stages themselves
-    // for bf16, three f16 V slots for e4m3 (conversion runs ahead of the MMAs)
-    static constexpr int kOpSlots = FP8 ? 3 : kStages;
+    // for bf16; for e4m3 one f16 V slot per P buffer, filled by the softmax
+    // warpgroup that writes that P
+    static constexpr int kOpSlots = FP8 ? kPBufs : kStages;
     static constexpr int kOpBytes = FP8 ? 16384 : 32768;
     static constexpr int kVOff = FP8 ? 0 : 16384;                 // V tile inside an operand slot
-    static constexpr int kWarps = FP8 ? 15 : 11;
+    static constexpr int kWarps = FP8 ? 12 : 11;
 };
 
 template <bool FP8>
@@ -98,9 +98,8 @@ struct TcLayout {
     static constexpr size_t kMeta = kML + 2 * 64 * 8;  // int [stage]: valid tokens of the staged chunk
     static constexpr size_t kBars = kMeta + 128;
     // full, empty (stages); qfull, qempty, published, consumed (2 each); sfull, sfree (one per S buffer);
-    // pfull, pvdone (one per P buffer); ofree; e4m3: cfull, cfree (op slots), q8full, qdone (2 each)
-    static constexpr int kNumBars =
-        2 * C::kStages + 8 + 2 * kSBufs + 2 * kPBufs + 1 + (FP8 ? 2 * C::kOpSlots + 4 : 0);
+    // pfull, pvdone (one per P buffer, with its V slot for e4m3); ofree; e4m3: q8full, qdone (2 each)
+    static constexpr int kNumBars = 2 * C::kStages + 8 + 2 * kSBufs + 2 * kPBufs + 1 + (FP8 ? 4 : 0);
     static constexpr size_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr size_t kFlag = kTmemSlot + 8;
     static constexpr size_t kTotal = kFlag + 8;
@@ -239,11 +238,10 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 // ------------------------------------------------------------------ kernel
 
 // Register cap per thread. The register file is four sub-partitions of 16384
-// registers and warp w runs on sub-partition w % 4: e4m3 (15 warps, four on
-// some sub-partitions) gets 16384 / (4 x 32) = 128; bf16 (11 warps, at most
-// three per sub-partition) could take 168, more than it needs.
+// registers and warp w runs on sub-partition w % 4: with at most three warps
+// on a sub-partition (11 warps bf16, 12 e4m3) a thread may hold 168.
 template <bool FP8>
-__global__ void __maxnreg__(FP8 ? 128 : 168)
+__global__ void __maxnreg__(168)
     decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ks,
                           const __grid_constant__ CUtensorMap tm_vs, const Params p) {
@@ -267,9 +265,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     uint64_t* published = pvdone + kPBufs;
     uint64_t* consumed = published + 2;
     uint64_t* ofree = consumed + 2;
-    uint64_t* cfull = ofree + 1;      // e4m3: op slot converted
-    uint64_t* cfree = cfull + NO;     // e4m3: op slot read by both MMAs
-    uint64_t* q8full = cfree + NO;    // e4m3: query row split into hi / lo e4m3 tiles and scales
+    uint64_t* q8full = ofree + 1;     // e4m3: query rows split into hi / lo e4m3 tiles and scales
     // e4m3: both softmax warpgroups finished a descriptor, so its query slot
     // (split in place) is free for the producer
     uint64_t* qdone = q8full + 2;
@@ -283,8 +279,6 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     // tiles are, the barrier that says they are ready, the one that frees them
     // and its valid-token count
     uint8_t* const opbase = FP8 ? smem + LY::kOps : smem;
-    uint64_t* const op_ready = FP8 ? cfull : full;
-    uint64_t* const op_free = FP8 ? cfree : empty;
     uint64_t* const q_ready = FP8 ? q8full : qfull;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -292,10 +286,10 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&full[i], 1);
-            // bf16: released by the P . V issuer's commit; e4m3: by the converter
-            // (V codes and scales read), the S issuer's commit (K codes read) and
-            // the chunk's softmax warpgroup (valid count and K scales read)
-            mbar_init(&empty[i], FP8 ? kConvThreads + 1 + kSoftmaxThreads : 1);
+            // bf16: released by the P . V issuer's commit; e4m3: by the S issuer's
+            // commit (K codes read) and the chunk's softmax warpgroup (valid count,
+            // scales and V codes read)
+            mbar_init(&empty[i], FP8 ? 1 + kSoftmaxThreads : 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
@@ -313,12 +307,8 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
         }
         mbar_init(ofree, kSoftmaxThreads);
         if constexpr (FP8) {
-            for (int i = 0; i < NO; ++i) {
-                mbar_init(&cfull[i], kConvThreads);
-                mbar_init(&cfree[i], 1);
-            }
             for (int i = 0; i < 2; ++i) {
-                mbar_init(&q8full[i], kConvThreads);
+                mbar_init(&q8full[i], 32);
                 mbar_init(&qdone[i], 2 * kSoftmaxThreads);
             }
         }
@@ -371,9 +361,8 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
                     const uint32_t sb = seq % kSBufs;
                     // bf16: the K tile of the chunk's stage; e4m3: its K codes
-                    const uint32_t ks_ = FP8 ? seq % NS : seq % NO;
-                    ok = wait_bounded(FP8 ? &full[ks_] : &op_ready[ks_], (seq / (FP8 ? NS : NO)) & 1, abort_flag,
-                                      kWaitLimitNs);
+                    const uint32_t ks_ = seq % NS;
+                    ok = wait_bounded(&full[ks_], (seq / NS) & 1, abort_flag, kWaitLimitNs);
                     if (ok && seq >= (uint32_t)kSBufs)
                         ok = wait_bounded(&sfree[sb], (seq / kSBufs - 1) & 1, abort_flag, kWaitLimitNs);
                     if (!ok) break;
@@ -391,7 +380,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                         umma_commit(&sfull[sb]);
                         umma_commit(&empty[ks_]);  // the K codes are read once S is done
                     } else {
-                        const uint32_t ka = smem_u32(opbase + (size_t)ks_ * C::kOpBytes);
+                        const uint32_t ka = smem_u32(smem + (size_t)ks_ * C::kStageBytes);
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t off = (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u;
@@ -430,24 +419,24 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                     if (!ok) break;
                 }
                 for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
-                    const uint32_t os = seq % NO;
+                    const uint32_t st = seq % NS;
                     const uint32_t g = seq & 1;
                     const uint32_t pb = 2 * g + ((seq >> 1) & 1);  // P buffer of the chunk
+                    // P (and, e4m3, the widened V in slot pb) written by the softmax
                     ok = wait_bounded(&pfull[pb], (seq >> 2) & 1, abort_flag, kWaitLimitNs);
-                    // e4m3: the converted V slot (bf16: the stage, waited by the softmax)
-                    if (FP8 && ok) ok = wait_bounded(&op_ready[os], (seq / NO) & 1, abort_flag, kWaitLimitNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t va = smem_u32(opbase + (size_t)os * C::kOpBytes + C::kVOff);
+                    // bf16: V of the chunk's stage; e4m3: the f16 V slot paired with P buffer pb
+                    const uint32_t va = smem_u32(FP8 ? opbase + (size_t)pb * C::kOpBytes : smem + (size_t)st * C::kStageBytes + C::kVOff);
                     const uint32_t pa = smem_u32(pbuf + pb * kPTile);
                     const bool first = cc - c0 < 2;  // the first chunk of this parity overwrites
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma_f16(tmem + kOCol + 128 * g, sdesc_sw128(pa + kk * 32, 16, 1024),
                                  sdesc_sw128(va + kk * 2048, 8192, 1024), kIdO, !first || kk > 0);
-                    umma_commit(&pvdone[pb]);
-                    // bf16: the stage (S_k finished before P_k was written); e4m3: the V slot
-                    umma_commit(&op_free[os]);
+                    umma_commit(&pvdone[pb]);  // P buffer pb and (e4m3) its V slot are free
+                    // bf16: the stage (S_k finished before P_k was written)
+                    if constexpr (!FP8) umma_commit(&empty[st]);
                 }
                 ++nd;
             }
@@ -457,12 +446,11 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
             }
         }
         __syncwarp();
-    } else if (warp >= kConvWarp0) {
-        // ============================ converter (e4m3 instances only): bf16 query
-        // tile -> hi / lo e4m3 tiles and row scales; V codes -> f16 V slot
+    } else if (warp == kSplitWarp) {
+        // ============================ query splitter (e4m3 instances only): each
+        // descriptor's bf16 query tile -> hi / lo e4m3 tiles in place, row scales
         if constexpr (FP8) {
-            const int ct = threadIdx.x - kConvWarp0 * 32;
-            uint32_t seq = 0;
+            float* qsc = reinterpret_cast<float*>(smem + LY::kQsc);
             int qd = 0;
             bool ok = true;
             for (int slot = list0; ok; ++slot) {
@@ -476,14 +464,15 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                 // finished the descriptor two back)
                 ok = wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs);
                 if (!ok) break;
-                {
-                    // In place: two threads per query row r, half hh reads bf16 dims
-                    // [64 hh, 64 hh + 64), which sit where row r of the hi tile (hh = 0)
-                    // or of the lo tile (hh = 1) goes; each thread writes the hi and lo
-                    // codes of its dims after both threads of the row have read.
-                    const int r = ct >> 1, hh = ct & 1;
+                uint8_t* qt = qbuf + qs * kQTile;
+                // Lane pair (2 j, 2 j + 1) takes query row r = j + 16 u, u < 4; half hh
+                // = lane & 1 reads bf16 dims [64 hh, 64 hh + 64), which sit where row r
+                // of the hi tile (hh = 0) or of the lo tile (hh = 1) goes; each lane
+                // writes the hi and lo codes of its dims once both lanes have read.
+#pragma unroll 1
+                for (int u = 0; u < 4; ++u) {
+                    const int r = (lane >> 1) + 16 * u, hh = lane & 1;
                     const bool in = r < kGroup * Q;
-                    uint8_t* qt = qbuf + qs * kQTile;
                     uint4 raw[8];
                     float amax = 0.f;
 #pragma unroll
@@ -497,7 +486,7 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                                                      fabsf(__uint_as_float(w[j] & 0xffff0000u))));
                     }
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-                    __syncwarp();  // the partner has read its half row
+                    __syncwarp();  // the partner lane has read its half row
                     // the smallest power of two 2^ex with amax / 2^ex <= 448: q / 2^ex is exact
                     float qscale = 1.f, qinv = 1.f;
                     if (amax > 0.f && amax <= 3.0e38f) {
@@ -507,83 +496,33 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                         qscale = ldexpf(1.f, ex);
                         qinv = ldexpf(1.f, -ex);
                     }
-                    if (hh == 0) reinterpret_cast<float*>(smem + LY::kQsc)[qs * 64 + r] = qscale;
+                    if (hh == 0) qsc[qs * 64 + r] = qscale;
 #pragma unroll
                     for (int c2 = 0; c2 < 4; ++c2) {
-                        // bf16 pieces c = 2 c2 + u (dims 64 hh + 8 c ...) -> bytes 8 u of the
+                        // bf16 pieces c = 2 c2 + v (dims 64 hh + 8 c ...) -> bytes 8 v of the
                         // e4m3 row's 16-byte piece 4 hh + c2
                         uint2 hp[2], lp[2];
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const uint4 v = raw[2 * c2 + u];
-                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                        for (int v = 0; v < 2; ++v) {
+                            const uint4 x4 = raw[2 * c2 + v];
+                            const uint32_t w[4] = {x4.x, x4.y, x4.z, x4.w};
                             float x[8];
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 x[2 * j] = __uint_as_float(w[j] << 16) * qinv;
                                 x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u) * qinv;
                             }
-                            split_e4m3x8(x, hp[u], lp[u]);
+                            split_e4m3x8(x, hp[v], lp[v]);
                         }
                         const int off = r * 128 + (((4 * hh + c2) ^ (r & 7)) << 4);
                         *reinterpret_cast<uint4*>(qt + off) = make_uint4(hp[0].x, hp[0].y, hp[1].x, hp[1].y);
                         *reinterpret_cast<uint4*>(qt + 8192 + off) = make_uint4(lp[0].x, lp[0].y, lp[1].x, lp[1].y);
                     }
+                    __syncwarp();
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&q8full[qs]);
                 ++qd;
-                for (int cc = c0; cc < c1 && ok; ++cc, ++seq) {
-                    const uint32_t st = seq % NS, os = seq % NO;
-                    ok = wait_bounded(&full[st], (seq / NS) & 1, abort_flag, kWaitLimitNs);
-                    if (ok && seq >= (uint32_t)NO)
-                        ok = wait_bounded(&cfree[os], ((seq / NO) - 1) & 1, abort_flag, kWaitLimitNs);
-                    if (!ok) break;
-                    const int nv = meta[st];  // 0: page id out of range (nothing loaded)
-                    const uint8_t* sb = smem + (size_t)st * C::kStageBytes;
-                    uint8_t* ob = opbase + (size_t)os * C::kOpBytes;
-                    const float* vs = reinterpret_cast<const float*>(sb + 16640);
-                    // Thread ct takes the 16-code V pieces c16 = (ct & 3) + 4 hf of rows
-                    // 32 rr + ct / 4: a warp's loads cover 8 rows x 4 pieces and its
-                    // stores 8 rows x 4 f16 pieces, each in the minimum of four 16-byte
-                    // bank-group passes.
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int row = 32 * rr + (ct >> 2);
-                        const bool in = row < nv;
-                        const float sv = in ? vs[row] : 0.f;
-                        const uint32_t s2 = pack_f16x2(sv, sv);
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const int c16 = (ct & 3) + 4 * hf;
-                            uint4 vl = make_uint4(0, 0, 0, 0), vh = vl;
-                            if (in) {
-                                const uint4 vw = *reinterpret_cast<const uint4*>(sb + 8192 + row * 128 +
-                                                                                ((c16 ^ (row & 7)) << 4));
-                                e4m3x4_to_f16x2x2(vw.x, vl.x, vl.y);
-                                e4m3x4_to_f16x2x2(vw.y, vl.z, vl.w);
-                                e4m3x4_to_f16x2x2(vw.z, vh.x, vh.y);
-                                e4m3x4_to_f16x2x2(vw.w, vh.z, vh.w);
-                                vl.x = hmul2_u32(vl.x, s2);
-                                vl.y = hmul2_u32(vl.y, s2);
-                                vl.z = hmul2_u32(vl.z, s2);
-                                vl.w = hmul2_u32(vl.w, s2);
-                                vh.x = hmul2_u32(vh.x, s2);
-                                vh.y = hmul2_u32(vh.y, s2);
-                                vh.z = hmul2_u32(vh.z, s2);
-                                vh.w = hmul2_u32(vh.w, s2);
-                            }
-                            // dims [16 c16, 16 c16 + 16) are f16 pieces f0 and f0 + 1 of dim
-                            // half hf, f0 = 2 (c16 & 3)
-                            const int f0 = 2 * (ct & 3);
-                            *reinterpret_cast<uint4*>(ob + hf * 8192 + row * 128 + ((f0 ^ (row & 7)) << 4)) = vl;
-                            *reinterpret_cast<uint4*>(ob + hf * 8192 + row * 128 + (((f0 + 1) ^ (row & 7)) << 4)) = vh;
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&empty[st]);  // V codes and scales read
-                    mbar_arrive(&cfull[os]);
-                }
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -656,7 +595,6 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                         sr[4 * m + 2] = __float_as_uint(__uint_as_float(sr[4 * m + 2]) * f.x);
                         sr[4 * m + 3] = __float_as_uint(__uint_as_float(sr[4 * m + 3]) * f.y);
                     }
-                    mbar_arrive(&empty[st]);
                 }
                 // valid tokens of this chunk for each row: the chunk's and the causal limit;
                 // tokens past it get -inf (after any scale, which is positive); full
@@ -755,8 +693,52 @@ __global__ void __maxnreg__(FP8 ? 128 : 168)
                     l_a += sa0 + sa1;
                     l_b += sb0 + sb1;
                 }
+                if constexpr (FP8) {
+                    // V codes of the stage -> f16 V slot 2 g + pj (code x scale, rounded; rows
+                    // past the live length zero). Thread tg takes the 16-code pieces
+                    // c16 = (tg & 3) + 4 hf of rows 32 rr + tg / 4: a warp's loads cover 8
+                    // rows x 4 pieces and its stores 8 rows x 4 f16 pieces, each in the
+                    // minimum of four 16-byte bank-group passes. The slot was last read by
+                    // the P . V of chunk k - 4, waited for above.
+                    const uint8_t* sbv = smem + (size_t)st * C::kStageBytes + 8192;
+                    const float* vs = reinterpret_cast<const float*>(smem + (size_t)st * C::kStageBytes + 16640);
+                    uint8_t* ob = opbase + (size_t)(2 * g + pj) * C::kOpBytes;
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int row = 32 * rr + (tg >> 2);
+                        const bool in = row < nv;
+                        const float sv = in ? vs[row] : 0.f;
+                        const uint32_t s2 = pack_f16x2(sv, sv);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const int c16 = (tg & 3) + 4 * hf;
+                            uint4 vl = make_uint4(0, 0, 0, 0), vh = vl;
+                            if (in) {
+                                const uint4 vw = *reinterpret_cast<const uint4*>(sbv + row * 128 + ((c16 ^ (row & 7)) << 4));
+                                e4m3x4_to_f16x2x2(vw.x, vl.x, vl.y);
+                                e4m3x4_to_f16x2x2(vw.y, vl.z, vl.w);
+                                e4m3x4_to_f16x2x2(vw.z, vh.x, vh.y);
+                                e4m3x4_to_f16x2x2(vw.w, vh.z, vh.w);
+                                vl.x = hmul2_u32(vl.x, s2);
+                                vl.y = hmul2_u32(vl.y, s2);
+                                vl.z = hmul2_u32(vl.z, s2);
+                                vl.w = hmul2_u32(vl.w, s2);
+                                vh.x = hmul2_u32(vh.x, s2);
+                                vh.y = hmul2_u32(vh.y, s2);
+                                vh.z = hmul2_u32(vh.z, s2);
+                                vh.w = hmul2_u32(vh.w, s2);
+                            }
+                            // dims [16 c16, 16 c16 + 16) are f16 pieces f0 and f0 + 1 of dim
+                            // half hf, f0 = 2 (c16 & 3)
+                            const int f0 = 2 * (tg & 3);
+                            *reinterpret_cast<uint4*>(ob + hf * 8192 + row * 128 + ((f0 ^ (row & 7)) << 4)) = vl;
+                            *reinterpret_cast<uint4*>(ob + hf * 8192 + row * 128 + (((f0 + 1) ^ (row & 7)) << 4)) = vh;
+                        }
+                    }
+                    mbar_arrive(&empty[st]);  // valid count, scales and V codes read
+                }
                 // rows of the last page past the live length may hold any bits: zero them
-                // in V (the e4m3 converter already wrote zeros there)
+                // in V (the e4m3 path wrote zeros there above)
                 if (!FP8 && nv < kChunk) {
                     uint8_t* vst = opbase + (size_t)st * C::kOpBytes + C::kVOff;  // bf16: the stage
                     const int nz = (kChunk - nv) * 16;  // 16-byte pieces over both dim halves
