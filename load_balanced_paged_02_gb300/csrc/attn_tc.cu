@@ -32,21 +32,22 @@
 //    is rare. At the descriptor's end warpgroup 1 publishes its (m, l) and
 //    warpgroup 0 merges both states and both O tiles into the partial rows and
 //    their LSEs.
-// e4m3 caches (one float32 scale per token and KV head), 15 warps, the same
+// e4m3 caches (one float32 scale per token and KV head), 12 warps, the same
 // roles with these changes:
-//  * warps 11-14, converter. Once per descriptor it splits each bf16 query row
-//    into two e4m3 tiles, Q = (Q_hi + Q_lo) x 2^e_r with a power-of-two row
-//    scale (exact to the bf16 input but for elements under 2^-11 of the row's
-//    maximum). Per chunk it widens the V codes of the e4m3 stage into an f16
-//    V slot (code x scale, rounded to f16; rows past the live length zero)
-//    and puts the chunk's K scales times log2(e)/sqrt(d) beside it. The
-//    dequantised V values must lie within the f16 range (|v| <= 65504).
+//  * warp 11, query splitter. Once per descriptor it splits each bf16 query
+//    row in place into two e4m3 tiles, Q = (Q_hi + Q_lo) x 2^e_r with a
+//    power-of-two row scale (exact to the bf16 input but for elements under
+//    2^-11 of the row's maximum).
 //  * S issuer: S = Q_hi . K^T + Q_lo . K^T as kind::f8f6f4 MMAs straight on
 //    the K codes of the stage (4 steps of 32 dims, each hi then lo), so K is
 //    never converted.
-//  * softmax: score column t is multiplied by its K scale factor in float32
-//    and the row by 2^e_r in the exponent, so the scores carry no rounding of
-//    the scales; P is f16 and P . V runs kind::f16 on the V slot.
+//  * softmax: score column t is multiplied by its K scale (read from the
+//    stage) in float32 and the row by 2^e_r log2(e)/sqrt(d) in the exponent,
+//    so the scores carry no rounding of the scales. The warpgroup that owns a
+//    chunk also widens its V codes into the f16 V slot paired with its P
+//    buffer (code x scale, rounded to f16; rows past the live length zero);
+//    P is f16 and P . V runs kind::f16 on that slot. The dequantised V values
+//    must lie within the f16 range (|v| <= 65504).
 // Every wait is bounded (2 s); on expiry the CTA records
 // HPC_DEVERR_WAIT_TIMEOUT and, after a bounded drain, frees its TMEM and
 // returns.
