@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="time eager launches only")
     ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue timing")
     ap.add_argument("--no-multi-token", action="store_true", help="skip the q_len > 1 timings")
+    ap.add_argument("--engine", choices=["auto", "mma_sync", "tcgen05"], default="auto",
+                    help="attention kernel for workloads with several new tokens per request "
+                         "(<workload>:qlen<N>); auto = the library's own choice")
     return ap.parse_args()
 
 
@@ -182,9 +185,12 @@ KERNEL_SOURCES = {
 }
 
 
-def attn_kernel_name(kv_dtype, q_len):
-    """The attention kernel the library's automatic engine choice launches."""
+def attn_kernel_name(kv_dtype, q_len, engine=None):
+    """The attention kernel launched for q_len new tokens: the pinned engine
+    (several new tokens only), else the library's automatic choice."""
     from load_balanced_paged_02_gb300 import binding as hb
+    if q_len > 1 and engine is not None:
+        return "decode_attn_tc_kernel" if engine == hb.ENGINE_TCGEN05 else "decode_attn_mt_kernel"
     if hb.auto_engine(kv_dtype, q_len) == hb.ENGINE_TCGEN05:
         return "decode_attn_tc_kernel"
     return "decode_attn_kernel" if q_len == 1 else "decode_attn_mt_kernel"
@@ -432,6 +438,9 @@ def run_ours(args):
     case = wl.make_case(w, device=dev)
     kvd = hb.kv_dtype_of(case["k_cache"])
     C = hb.default_num_ctas(kvd)
+    eng = {"auto": None, "mma_sync": hb.ENGINE_MMA_SYNC, "tcgen05": hb.ENGINE_TCGEN05}[args.engine]
+    if w.q_len == 1:
+        eng = None  # one new token: hpc_decode_attn's kernel
     Hkv = w.num_kv_heads
     lens = case["seq_lens"].cpu().numpy()
     stream = torch.cuda.current_stream(dev)
@@ -453,7 +462,7 @@ def run_ours(args):
             ev[1].record(stream)
         hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                            case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
-                           num_pages=case["num_pages"], q_scale=case["q_scale"])
+                           num_pages=case["num_pages"], q_scale=case["q_scale"], engine=eng)
         if ev is not None:
             ev[2].record(stream)
         hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
@@ -488,7 +497,7 @@ def run_ours(args):
         with torch.cuda.graph(layer_graph):
             hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                                case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
-                               num_pages=case["num_pages"], q_scale=case["q_scale"])
+                               num_pages=case["num_pages"], q_scale=case["q_scale"], engine=eng)
             hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
         for _ in range(3):
             graph.replay()
@@ -536,7 +545,7 @@ def run_ours(args):
     value = units_all / (ms_step * 1e-3) / 1e9
     attn_gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
 
-    kname = attn_kernel_name(kvd, w.q_len)
+    kname = attn_kernel_name(kvd, w.q_len, eng)
     result = None
     if rank == 0:
         clocks = clk.summary()
@@ -547,6 +556,7 @@ def run_ours(args):
             "dtype": "bf16" if kvd == hb.KV_BF16 else ("e4m3 (q and kv)" if w.q_dtype == "fp8" else "e4m3 kv, bf16 q"),
             "data": "synthetic",
             "config": {"workload": w.name, "detail": w.note, "num_ctas": C, "min_chunks": w.min_chunks,
+                       "engine": args.engine if w.q_len > 1 else "one-token kernel",
                        "live_tokens": int(lens.sum()), "splits": n_splits,
                        "bytes_per_step": byt, "l2": "inputs larger than L2 (no flush)",
                        "step": "cuda graph replay" if graph is not None else "eager launches",
@@ -572,7 +582,7 @@ def run_ours(args):
             hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits, plan=splan)
             hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                                case["seq_lens"], splan, sso, ssl, case["k_scale"], case["v_scale"],
-                               num_pages=case["num_pages"], q_scale=case["q_scale"])
+                               num_pages=case["num_pages"], q_scale=case["q_scale"], engine=eng)
             hb.hpc_decode_combine(splan, sso, ssl, out, lse, Hkv)
         for _ in range(3):
             sstep()
