@@ -157,6 +157,23 @@ def test_q_len_out_of_range_is_rejected():
 
 
 @pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
+def test_invalid_page_id_sets_error_and_skips(dtype, engine):
+    """A page id outside the pool sets the error bit and skips that chunk
+    (nothing is loaded from it); the other request's rows are untouched."""
+    case = case_for([200, 300], 3, hkv=1, dtype=dtype, seed=67)
+    bad = case["page_table"].clone()
+    bad[1, 2] = case["num_pages"] + 5
+    res = _gpu.run(dict(case, page_table=bad), num_ctas=4, min_chunks=1, engine=engine)
+    assert hb.hpc_decode_read_error(res["plan"]) & 4
+    host = wl.to_numpy_case(case, requests=[0])
+    rows = [(0, qi * 8 + h) for qi in range(3) for h in range(8)]
+    ro, rl = oracle.attn_rows(host, rows)
+    _gpu.assert_close(res["out"][0].float().cpu().numpy().reshape(-1, 128), res["lse"][0].cpu().numpy().reshape(-1),
+                      ro, rl, case, "request 0")
+    assert torch.isfinite(res["out"][1].float()).all()
+
+
+@pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
 def test_garbage_beyond_live_length_is_ignored(dtype, engine):
     """Slots past the live length of the last page hold NaN codes; the causal
     mask and the tail fill must keep them out of every row."""
