@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="time eager launches only")
     ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue timing")
     ap.add_argument("--no-multi-token", action="store_true", help="skip the q_len > 1 timings")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the plan -> prologue -> attention -> combine layer timing")
     ap.add_argument("--engine", choices=["auto", "mma_sync", "tcgen05"], default="auto",
                     help="attention kernel for workloads with several new tokens per request "
                          "(<workload>:qlen<N>); auto = the library's own choice")
@@ -317,6 +319,74 @@ def prologue_timing(w, dev, n_rep=200):
         gbs = byt / (us * 1e-6) / 1e9
         out[label] = {"tokens": T, "us": us, "bytes": byt, "GB/s": gbs, "frac": gbs / peak}
     return out
+
+
+def chained_layer_timing(w, case, C, dev, n_rep=200, rounds=5):
+    """One decode layer as a caller chains it: plan, the fused prologue writing
+    each request's new token (position L - 1) into the cache and emitting Q
+    (e4m3 with scales for an e4m3 cache), attention, combine; replayed from a
+    CUDA graph, with the attention kernel waiting for the prologue before any
+    load, and with HPC_ATTN_EARLY_KV (KV of chunks without the new token
+    gathered while the prologue runs). The two graphs alternate over
+    ``rounds`` blocks of ``n_rep`` replays; the medians of the blocks are
+    reported."""
+    import torch
+    from load_balanced_paged_02_gb300 import binding as hb
+    from load_balanced_paged_02_gb300 import workloads as wl
+    fp8 = w.kv_dtype == "fp8"
+    B, Hq, Hkv = w.batch, w.num_q_heads, w.num_kv_heads
+    lens = case["seq_lens"].cpu().numpy().astype(np.int64)
+    pt = case["page_table"].cpu().numpy()
+    pos = np.maximum(lens - 1, 0).astype(np.int32)
+    slots = np.where(lens > 0, pt[np.arange(B), pos // 64] * 64 + pos % 64, -1).astype(np.int32)
+    pc = wl.make_prologue_case(pos, Hq, Hkv, seed=91, device=dev, max_pos=int(pos.max()) + 1, slots=slots)
+    q = torch.empty((B, Hq, 128), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16, device=dev)
+    qs = torch.empty((B, Hq), dtype=torch.float32, device=dev) if fp8 else None
+    plan = hb.Plan(B, Hkv, C, dev)
+    so, sl = hb.split_buffers(plan)
+    out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+
+    def layer(early):
+        hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
+        hb.hpc_rope_norm(pc["qkv"], pc["positions"], pc["cos_sin"], pc["q_weight"], pc["k_weight"], pc["slots"],
+                         q, case["k_cache"], case["v_cache"], q_scale=qs, k_scale=case["k_scale"],
+                         v_scale=case["v_scale"], eps=pc["eps"], num_kv_heads=Hkv,
+                         num_pages=case["num_pages"])
+        hb.hpc_decode_attn(q, case["k_cache"], case["v_cache"], case["page_table"], case["seq_lens"], plan, so,
+                           sl, case["k_scale"], case["v_scale"], num_pages=case["num_pages"], q_scale=qs,
+                           early_kv=early)
+        hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+    graphs = {}
+    for early in (False, True):
+        for _ in range(3):
+            layer(early)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer(early)
+        g.replay()
+        graphs[early] = g
+    torch.cuda.synchronize()
+    if hb.hpc_decode_read_error(plan) != 0:
+        raise RuntimeError("chained layer: device error word set")
+    st = torch.cuda.current_stream(dev)
+    blocks = {False: [], True: []}
+    for _ in range(rounds):
+        for early in (False, True):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(n_rep):
+                graphs[early].replay()
+            b.record(st)
+            torch.cuda.synchronize()
+            blocks[early].append(1e3 * a.elapsed_time(b) / n_rep)
+    wait_us, early_us = float(np.median(blocks[False])), float(np.median(blocks[True]))
+    del graphs, so, sl
+    return {"layer": "plan -> hpc_rope_norm -> attention -> combine (cuda graph)",
+            "query": "e4m3 + scales" if fp8 else "bf16",
+            "us_wait_first": wait_us, "us_early_kv": early_us, "saved_us": wait_us - early_us,
+            "blocks_us": {"wait_first": blocks[False], "early_kv": blocks[True]}}
 
 
 # ---------------------------------------------------------------- arms
@@ -651,6 +721,10 @@ def run_ours(args):
     # ---- several new tokens per request on the same batch and cache (NEXT-4)
     if rank == 0 and not args.no_multi_token and w.q_len == 1 and w.q_dtype == "bf16":
         result["multi_token"] = multi_token_timing(w, case, plan, C, dev)
+
+    # ---- the layer chained with the prologue, KV gathered before Q is ready (NEXT-3)
+    if rank == 0 and not args.no_chain and w.q_len == 1 and w.q_dtype == "bf16":
+        result["chained_layer"] = chained_layer_timing(w, case, C, dev)
 
     # ---- CPU oracle baseline (rank 0 only, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -269,6 +269,43 @@ hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_
  * only, no device call. */
 int hpc_decode_attn_multi_auto_engine(int kv_dtype, int q_len);
 
+/* Flags of hpc_decode_attn_ex. */
+#define HPC_ATTN_EARLY_KV 1  /* gather KV before waiting for the predecessor kernel */
+
+/*
+ * Every attention form in one call: q_scale NULL takes a bf16 query
+ * [batch][q_len][num_q_heads][128] (hpc_decode_attn_multi_engine; q_len = 1
+ * is hpc_decode_attn), non-NULL an e4m3 query with per-(token, head) scales
+ * (hpc_decode_attn_q8: kv_dtype HPC_KV_FP8_E4M3, q_len 1, HPC_ENGINE_AUTO or
+ * HPC_ENGINE_MMA_SYNC). Outputs and errors as those calls, plus
+ * HPC_ERR_INVALID_ARG for an unknown flag bit.
+ *
+ * HPC_ATTN_EARLY_KV ([LL] "SGLang Low-Latency Mode: Kernels and Runtime",
+ * section "Low-Latency-Specific Optimizations", item 1: with programmatic
+ * dependent launch, attention starts gathering KV before it waits for the
+ * query). The kernel always waits for the kernel before it in the stream
+ * before it reads the query; with this flag each CTA's producer first issues
+ * the copies of the leading chunks of its task list that hold no new token
+ * (all 64 positions below seq_lens[b] - q_len), up to its ring depth, and
+ * only then waits. Results are bit-identical to the call without the flag.
+ * Contract, the caller's: the plan, seq_lens, page_table and every cache
+ * slot outside the last q_len tokens of each request are final before the
+ * kernel preceding this call in the stream triggers its dependents (the
+ * library's kernels trigger only after their own wait for their
+ * predecessor; a kernel launched without programmatic serialisation counts
+ * as triggering when it ends). That kernel may write the query and the new
+ * tokens' K and V (hpc_rope_norm does). Breaking the contract yields wrong
+ * outputs, never an out-of-bounds access: early copies are bounds-checked
+ * like the others and every copy lands before the CTA exits.
+ */
+hpc_status hpc_decode_attn_ex(const void* q, const float* q_scale, int q_len, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale,
+                              int kv_dtype, int num_pages, const int32_t* page_table,
+                              int page_table_stride, const int32_t* seq_lens, int batch,
+                              int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                              const hpc_plan* plan, float* split_o, float* split_lse, int engine,
+                              int flags, void* stream);
+
 /*
  * Combine ([SGL] the paragraph on execution; [VLLM] combine stage). For every
  * (request b, query head qh) with h = qh / 8, j = qh % 8 and the pair's

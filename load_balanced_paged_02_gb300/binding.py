@@ -18,6 +18,7 @@ from . import _build
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 ENGINE_AUTO, ENGINE_MMA_SYNC, ENGINE_TCGEN05 = 0, 1, 2
+ATTN_EARLY_KV = 1  # flag of hpc_decode_attn_ex
 HEAD_DIM = 128
 PAGE = 64
 GROUP = 8
@@ -59,6 +60,8 @@ SIGNATURES = {
                                    _P, _vp, _vp, _vp]),
     "hpc_decode_attn_multi_engine": (_i, [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i,
                                           _i, _P, _vp, _vp, _i, _vp]),
+    "hpc_decode_attn_ex": (_i, [_vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                                _P, _vp, _vp, _i, _i, _vp]),
     "hpc_decode_combine": (_i, [_P, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "hpc_decode_combine_multi": (_i, [_P, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "hpc_rope_norm": (_i, [_vp, _vp, _vp, _i, _vp, _vp, ctypes.c_float, _vp, _i, _i, _i, _i, _i, _vp, _vp,
@@ -216,12 +219,16 @@ def split_buffers(plan: Plan, device=None, q_len: int = 1):
 
 def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split_o, split_lse,
                     k_scale=None, v_scale=None, num_pages: int | None = None, stream=None,
-                    q_scale=None, engine: int | None = None):
+                    q_scale=None, engine: int | None = None, early_kv: bool = False):
     """Persistent attention over the task map; writes split_o / split_lse.
     A float8_e4m3fn q with its q_scale [B, Hq] goes to hpc_decode_attn_q8; a
     bf16 q of shape [B, q_len, Hq, 128] (several new tokens per request, causal)
-    goes to hpc_decode_attn_multi (or hpc_decode_attn_multi_engine when ``engine``
-    is given: ENGINE_AUTO, ENGINE_MMA_SYNC or ENGINE_TCGEN05)."""
+    goes to hpc_decode_attn_multi. A given ``engine`` (ENGINE_AUTO, ENGINE_MMA_SYNC
+    or ENGINE_TCGEN05) goes to hpc_decode_attn_multi_engine for a bf16 q of any
+    q_len (hpc_decode_attn_ex for an e4m3 q). ``early_kv`` goes
+    to hpc_decode_attn_ex with HPC_ATTN_EARLY_KV: the kernel gathers the KV of
+    chunks without a new token before it waits for the previous kernel (the
+    caller's contract is in the header)."""
     kvd = kv_dtype_of(k_cache)
     q_len = q.shape[1] if q.dim() == 4 else 1
     B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
@@ -236,16 +243,25 @@ def hpc_decode_attn(q, k_cache, v_cache, page_table, seq_lens, plan: Plan, split
     if split_o.numel() < need * HEAD_DIM or split_lse.numel() < need:
         raise HpcError("split buffers", detail=f"need {plan.split_capacity} x {q_len} x 8 rows")
     npages = int(num_pages if num_pages is not None else k_cache.shape[0])
-    if q.dtype in (torch.float8_e4m3fn, torch.uint8):
-        if q_scale is None:
-            raise HpcError("hpc_decode_attn_q8", detail="an e4m3 q needs q_scale")
+    q8 = q.dtype in (torch.float8_e4m3fn, torch.uint8)
+    if q8 and q_scale is None:
+        raise HpcError("hpc_decode_attn_q8", detail="an e4m3 q needs q_scale")
+    if early_kv or (q8 and engine is not None):
+        rc = lib().hpc_decode_attn_ex(
+            _ptr(q), _ptr(q_scale), q_len, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd,
+            npages, _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D,
+            int(k_cache.shape[1]), plan.ref(), _ptr(split_o), _ptr(split_lse),
+            ENGINE_AUTO if engine is None else int(engine), ATTN_EARLY_KV if early_kv else 0, _stream(stream))
+        _check("hpc_decode_attn_ex", rc)
+        return
+    if q8:
         rc = lib().hpc_decode_attn_q8(
             _ptr(q), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), npages,
             _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D,
             int(k_cache.shape[1]), plan.ref(), _ptr(split_o), _ptr(split_lse), _stream(stream))
         _check("hpc_decode_attn_q8", rc)
         return
-    if q.dim() == 4 and engine is not None:
+    if engine is not None:  # also for one new token ([B, Hq, 128] is [B, 1, Hq, 128])
         rc = lib().hpc_decode_attn_multi_engine(
             _ptr(q), q_len, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kvd, npages,
             _ptr(page_table), int(page_table.shape[1]), _ptr(seq_lens), B, Hq, Hkv, D, int(k_cache.shape[1]),

@@ -139,7 +139,7 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
                        const int32_t* page_table, int page_table_stride, const int32_t* seq_lens, int batch,
                        int num_q_heads, int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
                        float* split_o, float* split_lse, void* stream, int q_len = 1,
-                       int engine = HPC_ENGINE_AUTO) {
+                       int engine = HPC_ENGINE_AUTO, int flags = 0) {
     hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
     if (st != HPC_OK) return st;
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
@@ -157,6 +157,7 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     if (q_len < 1 || q_len > HPC_MAX_Q_LEN || (q_len > 1 && q_scale)) return HPC_ERR_INVALID_ARG;
     if (engine < HPC_ENGINE_AUTO || engine > HPC_ENGINE_TCGEN05) return HPC_ERR_INVALID_ARG;
+    if (flags & ~HPC_ATTN_EARLY_KV) return HPC_ERR_INVALID_ARG;
     AttnArgs a;
     a.q = q;
     a.q_scale = q_scale;
@@ -178,6 +179,7 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     a.split_cap = (long long)hpc_decode_split_capacity(batch, num_kv_heads, plan->num_ctas);
     a.split_o = split_o;
     a.split_lse = split_lse;
+    a.early_kv = (flags & HPC_ATTN_EARLY_KV) ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (engine == HPC_ENGINE_AUTO) engine = multi_engine_for(fp8, q_len);
     cudaError_t e;
@@ -241,6 +243,18 @@ hpc_status hpc_decode_attn_multi_engine(const void* q, int q_len, const void* k_
     return attn_common(q, nullptr, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
                        page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
                        split_o, split_lse, stream, q_len, engine);
+}
+
+hpc_status hpc_decode_attn_ex(const void* q, const float* q_scale, int q_len, const void* k_cache,
+                              const void* v_cache, const float* k_scale, const float* v_scale, int kv_dtype,
+                              int num_pages, const int32_t* page_table, int page_table_stride,
+                              const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                              int page_size, const hpc_plan* plan, float* split_o, float* split_lse, int engine,
+                              int flags, void* stream) {
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN) return HPC_ERR_INVALID_ARG;
+    return attn_common(q, q_scale, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
+                       page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, plan,
+                       split_o, split_lse, stream, q_len, engine, flags);
 }
 
 hpc_status hpc_decode_combine_multi(const hpc_plan* plan, int q_len, const float* split_o, const float* split_lse,

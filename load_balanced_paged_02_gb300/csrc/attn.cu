@@ -218,20 +218,22 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // Everything above overlaps the planner's tail; the task map, lengths and
-    // Q may come from earlier kernels, so wait for them here.
-    grid_dependency_wait();
-    grid_launch_dependents();
+    // Everything above overlaps the predecessor's tail. The task map, lengths
+    // and Q may come from earlier kernels: every warp waits for them here but
+    // the producer, which waits inside produce() (after its early loads, when
+    // the caller allows them). Each thread releases the next kernel only after
+    // its own wait.
     __syncthreads();
 
-    const int list0 = p.cta_off[blockIdx.x];
-
     if (warp == NCW) {
-        produce<FP8, STAGES, QF8 ? QStage::kE4m3 : QStage::kBf16>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, list0, lane, smem,
+        produce<FP8, STAGES, QF8 ? QStage::kE4m3 : QStage::kBf16>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, lane, smem,
                                                                   qbuf, kQSlotBytes, full, empty, qfull, qempty,
                                                                   meta, abort_flag);
         return;
     }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int list0 = p.cta_off[blockIdx.x];
 
     // ================================ consumer warps
     const int gi = warp >> 2, wq = warp & 3;
@@ -484,6 +486,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
         return cudaErrorInvalidValue;
     const PlanLayout L = plan_layout(a.batch, a.num_kv_heads, a.num_ctas);
     Params p;
+    memset(&p, 0, sizeof p);
     p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     p.q8 = reinterpret_cast<const uint8_t*>(a.q);
     p.q_scale = a.q_scale;
@@ -504,6 +507,8 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     p.split_o = a.split_o;
     p.split_lse = a.split_lse;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
+    p.early_kv = a.early_kv;
+    p.max_tasks = (int)L.max_tasks;
     const bool stat = a.mode == 1;
     if (a.fp8 && a.q_scale)
         return stat ? StaticFp8Q::launch(maps, p, a.num_ctas, s) : BalancedFp8Q::launch(maps, p, a.num_ctas, s);

@@ -50,6 +50,12 @@ struct Params {
     float* split_o;
     float* split_lse;
     float scale_log2;
+    // 1: the task map, page table, lengths and every cache slot but the last
+    // q_len tokens of each request were final before the preceding kernel
+    // released this one, so the producer may stream those chunks before it
+    // waits for that kernel
+    int early_kv;
+    int max_tasks;  // descriptor slots in the task map (bounds the early walk)
 };
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
@@ -189,7 +195,12 @@ enum class QStage {
 
 constexpr int kQRowsBytes = kGroup * kHeadDim * 2;  // 8 bf16 query rows
 
-// Producer warp of a decode attention CTA. It walks the CTA's descriptor list;
+// Producer warp of a decode attention CTA. It waits for the preceding kernel
+// itself (the kernel's other warps wait before they start): at once, or, with
+// p.early_kv, after issuing the TMA loads of the CTA's leading chunks that
+// hold no new token, up to a full ring, so the KV stream starts while the
+// predecessor (the prologue writing Q and the new tokens' K/V) is still
+// running. It walks the CTA's descriptor list;
 // for each descriptor it stages the query rows into a 2-slot ring (qfull /
 // qempty) and then streams every chunk (= page) of K and V, plus the page's
 // two e4m3 scale rows, into the STAGES-deep ring (full / empty) with TMA. The
@@ -198,14 +209,74 @@ constexpr int kQRowsBytes = kGroup * kHeadDim * 2;  // 8 bf16 query rows
 // Chunk k of the CTA goes to stage k % STAGES. Every wait is bounded; on
 // expiry it raises the abort flag, records HPC_DEVERR_WAIT_TIMEOUT and waits
 // (bounded) for its own copies in flight before returning.
+template <bool FP8, int STAGES>
+__device__ __forceinline__ void issue_chunk(const Params& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                            const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, uint8_t* sbuf,
+                                            uint64_t* full_st, int page, int h, uint64_t pol) {
+    using Cfg = KvCfg<FP8>;
+    mbar_arrive_expect_tx(full_st, Cfg::kTxBytes);
+    const int tok = page * kChunk;
+    if constexpr (FP8) {
+        // The 256-byte scale rows go through 2-D tensor maps: on GB300 that
+        // measured 6 % faster for the whole kernel than plain bulk copies of
+        // the same rows. Issued first, so they are not the last bytes of the
+        // stage to land.
+        const int srow = page * p.num_kv_heads + h;
+        tma_load_2d(sbuf + 16384, tm_ks, full_st, 0, srow, pol);
+        tma_load_2d(sbuf + 16640, tm_vs, full_st, 0, srow, pol);
+        tma_load_3d(sbuf, tm_k, full_st, 0, h, tok, pol);
+        tma_load_3d(sbuf + 8192, tm_v, full_st, 0, h, tok, pol);
+    } else {
+        tma_load_3d(sbuf, tm_k, full_st, 0, h, tok, pol);
+        tma_load_3d(sbuf + 8192, tm_k, full_st, 64, h, tok, pol);
+        tma_load_3d(sbuf + 16384, tm_v, full_st, 0, h, tok, pol);
+        tma_load_3d(sbuf + 24576, tm_v, full_st, 64, h, tok, pol);
+    }
+}
+
 template <bool FP8, int STAGES, QStage QM>
 __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                        const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, int list0, int lane,
+                                        const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, int lane,
                                         uint8_t* smem, uint8_t* qbuf, uint32_t q_slot_bytes, uint64_t* full,
                                         uint64_t* empty, uint64_t* qfull, uint64_t* qempty, volatile int* meta,
                                         volatile int* abort_flag, const CUtensorMap* tm_q = nullptr) {
     using Cfg = KvCfg<FP8>;
     const uint64_t pol = l2_evict_first_policy();
+    // Early phase: the leading chunks of the CTA's list that hold no new token
+    // (all 64 positions below seq_len - q_len), in list order, up to a full
+    // ring, stopping at the first other chunk. Each is issued exactly as the
+    // main loop would (stage npre of the first lap) and skipped there.
+    uint32_t npre = 0;
+    if (p.early_kv && lane == 0) {
+        // the walk stays inside the task map even if the caller broke the
+        // contract and the map is not yet written (wrong values, no fault)
+        const int l0 = p.cta_off[blockIdx.x];
+        for (int slot = max(l0, 0); slot < p.max_tasks && npre < (uint32_t)STAGES; ++slot) {
+            const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
+            const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
+            const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
+            if (h < 0 || !desc_ok(p, h, b, c0, c1, t1.x)) break;
+            const int L = __ldg(p.seq_lens + b);
+            const int32_t* prow = p.page_table + (long long)b * p.pt_stride;
+            bool stop = false;
+            for (int cc = c0; cc < c1 && npre < (uint32_t)STAGES; ++cc) {
+                const int page = __ldg(prow + cc);
+                if (kChunk * (cc + 1) > L - p.q_len || (unsigned)page >= (unsigned)p.num_pages) {
+                    stop = true;
+                    break;
+                }
+                meta[npre] = kChunk;
+                issue_chunk<FP8, STAGES>(p, tm_k, tm_v, tm_ks, tm_vs, smem + (size_t)npre * Cfg::kStageBytes,
+                                         &full[npre], page, h, pol);
+                ++npre;
+            }
+            if (stop) break;
+        }
+    }
+    npre = __shfl_sync(0xffffffffu, npre, 0);
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int list0 = p.cta_off[blockIdx.x];
     uint32_t seq = 0;
     int qd = 0;
     bool ok = true;
@@ -264,31 +335,14 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
                 const bool page_ok = (unsigned)page < (unsigned)p.num_pages;
                 const int st = (int)(seq % STAGES);
                 const uint32_t ph = (seq / STAGES) & 1;
-                if (lane == 0) {
+                if (lane == 0 && seq >= npre) {  // (the first npre chunks were issued early)
                     ok = wait_bounded(&empty[st], ph ^ 1, abort_flag, kWaitLimitNs);
                     if (ok) {
                         if (!page_ok) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
                         if (page_ok && nvalid > 0) {
                             meta[st] = nvalid;
-                            mbar_arrive_expect_tx(&full[st], Cfg::kTxBytes);
-                            uint8_t* sbuf = smem + (size_t)st * Cfg::kStageBytes;
-                            const int tok = page * kChunk;
-                            if constexpr (FP8) {
-                                // The 256-byte scale rows go through 2-D tensor maps: on
-                                // GB300 that measured 6 % faster for the whole kernel than
-                                // plain bulk copies of the same rows. Issued first, so
-                                // they are not the last bytes of the stage to land.
-                                const int srow = page * p.num_kv_heads + h;
-                                tma_load_2d(sbuf + 16384, tm_ks, &full[st], 0, srow, pol);
-                                tma_load_2d(sbuf + 16640, tm_vs, &full[st], 0, srow, pol);
-                                tma_load_3d(sbuf, tm_k, &full[st], 0, h, tok, pol);
-                                tma_load_3d(sbuf + 8192, tm_v, &full[st], 0, h, tok, pol);
-                            } else {
-                                tma_load_3d(sbuf, tm_k, &full[st], 0, h, tok, pol);
-                                tma_load_3d(sbuf + 8192, tm_k, &full[st], 64, h, tok, pol);
-                                tma_load_3d(sbuf + 16384, tm_v, &full[st], 0, h, tok, pol);
-                                tma_load_3d(sbuf + 24576, tm_v, &full[st], 64, h, tok, pol);
-                            }
+                            issue_chunk<FP8, STAGES>(p, tm_k, tm_v, tm_ks, tm_vs,
+                                                     smem + (size_t)st * Cfg::kStageBytes, &full[st], page, h, pol);
                         } else {
                             meta[st] = 0;
                             mbar_arrive(&full[st]);
@@ -309,6 +363,10 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
             wait_bounded(&full[k % STAGES], (k / STAGES) & 1, nullptr, kDrainLimitNs);
         if (qd > 0) wait_bounded(&qfull[(qd - 1) & 1], ((qd - 1) >> 1) & 1, nullptr, kDrainLimitNs);
     }
+    // Early copies the walk did not reach (an abort, or a task map that changed
+    // under the caller's contract) still land before the CTA may exit.
+    if (lane == 0)
+        for (uint32_t k = seq; k < npre; ++k) wait_bounded(&full[k], 0, nullptr, kDrainLimitNs);
 }
 
 }  // namespace attn

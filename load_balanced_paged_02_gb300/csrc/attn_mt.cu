@@ -234,18 +234,20 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
         *abort_flag = 0;
         fence_mbar_init();
     }
-    grid_dependency_wait();
-    grid_launch_dependents();
+    // every warp but the producer waits for the predecessor here (the producer
+    // waits inside produce(), after its early loads when the caller allows
+    // them); each thread releases the next kernel only after its own wait
     __syncthreads();
-
-    const int list0 = p.cta_off[blockIdx.x];
     const int Q = p.q_len;
 
     if (warp == NCW) {
-        produce<FP8, STAGES, QStage::kBf16Rows>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, list0, lane, smem, qbuf,
+        produce<FP8, STAGES, QStage::kBf16Rows>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, lane, smem, qbuf,
                                                 LY::kQSlot, full, empty, qfull, qempty, meta, abort_flag);
         return;
     }
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int list0 = p.cta_off[blockIdx.x];
 
     // ================================ consumer warps
     const int gi = warp / LY::kWPG, qw = (warp % LY::kWPG) / TS, ts = warp % TS;
@@ -526,6 +528,8 @@ cudaError_t launch_attn_mt(const AttnArgs& a, int q_len, cudaStream_t s) {
     p.split_o = a.split_o;
     p.split_lse = a.split_lse;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
+    p.early_kv = a.early_kv;
+    p.max_tasks = (int)L.max_tasks;
     return a.fp8 ? launch_set<true>(maps, p, a.num_ctas, s) : launch_set<false>(maps, p, a.num_ctas, s);
 }
 

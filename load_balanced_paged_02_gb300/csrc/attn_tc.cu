@@ -327,16 +327,22 @@ __global__ void __maxnreg__(168)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    grid_dependency_wait();
-    grid_launch_dependents();
+    // every warp but the producer waits for the predecessor here (the producer
+    // waits inside produce(), after its early loads when the caller allows
+    // them); each thread releases the next kernel only after its own wait
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int list0 = p.cta_off[blockIdx.x];
+    int list0 = 0;
+    if (warp != 8) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+        list0 = p.cta_off[blockIdx.x];
+    }
 
     if (warp == 8) {
-        produce<FP8, NS, QStage::kBf16Tile>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, list0, lane, smem, qbuf, kQTile, full,
+        produce<FP8, NS, QStage::kBf16Tile>(p, &tm_k, &tm_v, &tm_ks, &tm_vs, lane, smem, qbuf, kQTile, full,
                                             empty, qfull, FP8 ? qdone : qempty, meta, abort_flag, &tm_q);
     } else if (warp == 9) {
         // ============================ S issuer (one thread): S_k = Q . K_k^T
@@ -935,6 +941,8 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int q_len, cudaStream_t s) {
     p.split_o = a.split_o;
     p.split_lse = a.split_lse;
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
+    p.early_kv = a.early_kv;
+    p.max_tasks = (int)L.max_tasks;
     return a.fp8 ? launch_tc<true>(maps, p, a.num_ctas, s) : launch_tc<false>(maps, p, a.num_ctas, s);
 }
 

@@ -80,6 +80,7 @@ struct AttnArgs {
     long long split_cap;
     float* split_o;
     float* split_lse;
+    int early_kv;  // see Params::early_kv (attn_common.cuh)
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 int attn_default_ctas(int fp8);

@@ -14,7 +14,7 @@ FP8_MAX_ABS = 6e-2
 LSE_ABS = 1e-3
 
 
-def run(case, num_ctas=None, min_chunks=2, static_splits=None, plan=None, engine=None):
+def run(case, num_ctas=None, min_chunks=2, static_splits=None, plan=None, engine=None, early_kv=False):
     """plan -> attn -> combine on the case's device. Returns a dict of tensors."""
     Hkv = case["k_cache"].shape[2]
     if plan is None:
@@ -30,7 +30,8 @@ def run(case, num_ctas=None, min_chunks=2, static_splits=None, plan=None, engine
     sl.fill_(float("nan"))
     hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"],
                        case["seq_lens"], plan, so, sl, case["k_scale"], case["v_scale"],
-                       num_pages=case["num_pages"], q_scale=case.get("q_scale"), engine=engine)
+                       num_pages=case["num_pages"], q_scale=case.get("q_scale"), engine=engine,
+                       early_kv=early_kv)
     out = torch.full(case["q"].shape, float("nan"), dtype=torch.bfloat16, device=case["q"].device)
     lse = torch.full(case["q"].shape[:-1], float("nan"), dtype=torch.float32, device=case["q"].device)
     hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)

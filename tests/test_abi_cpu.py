@@ -114,6 +114,30 @@ def test_attn_q8_rejects_bad_arguments(L):
     assert call(D=64) == 2
 
 
+def test_attn_ex_rejects_bad_arguments(L):
+    """hpc_decode_attn_ex: unknown flag bits, q_len, engine and query-scale
+    combinations are refused on the host."""
+    plan = hb.PlanStruct(FAKE.value, 1 << 20, 2, 1, 4, 2, 0, 10)
+    args = dict(q=FAKE, qs=None, ql=1, k=FAKE, v=FAKE, ks=None, vs=None, dt=0, pages=16, pt=FAKE, stride=4,
+                sl=FAKE, B=2, Hq=8, Hkv=1, D=128, P=64, plan=ctypes.byref(plan), so=FAKE, slse=FAKE, eng=0,
+                flags=hb.ATTN_EARLY_KV)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.hpc_decode_attn_ex(a["q"], a["qs"], a["ql"], a["k"], a["v"], a["ks"], a["vs"], a["dt"],
+                                    a["pages"], a["pt"], a["stride"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["D"],
+                                    a["P"], a["plan"], a["so"], a["slse"], a["eng"], a["flags"], None)
+    assert call(flags=2) == 1
+    assert call(flags=-1) == 1
+    assert call(ql=0) == 1
+    assert call(ql=9) == 1
+    assert call(eng=3) == 1
+    assert call(qs=FAKE) == 2                            # a query scale with a bf16 cache
+    assert call(qs=FAKE, dt=1, ks=FAKE, vs=FAKE, ql=2) == 1  # e4m3 query is one token per request
+    assert call(q=None) == 1
+    assert call(D=64) == 2
+
+
 def test_plan_rejects_bad_arguments(L):
     p = hb.PlanStruct(FAKE.value, 1 << 20, 0, 0, 0, 0, 0, 0)
     assert L.hpc_decode_plan(None, 4, 1, 16, 2, ctypes.byref(p), None) == 1
