@@ -43,7 +43,10 @@ namespace {
 
 using namespace attn;
 
-constexpr int kQSlotBytes = kGroup * kHeadDim * 2;  // 2 KB of bf16 Q rows
+// one query slot: 8 bf16 rows at the padded pitch (the larger of the two forms;
+// e4m3: 8 code rows at their pitch, then 8 float32 scales)
+constexpr int kQSlotBytes = kGroup * kQPitchBf16;
+static_assert(kQScaleOffE4m3 + kGroup * 4 <= kQSlotBytes, "query slot");
 template <bool FP8, int STAGES, int NG>
 struct Layout {
     // Chunk k goes to group k % NG and to stage k % STAGES. With STAGES a
@@ -53,9 +56,12 @@ struct Layout {
     static_assert(STAGES % NG == 0, "stage ring must be a multiple of the consumer groups");
     static constexpr int kNCW = NG * 4;
     static constexpr size_t kQ = (size_t)STAGES * KvCfg<FP8>::kStageBytes;
+    // merge scratch and (m, l) words, two buffers: descriptor n uses buffer n % 2,
+    // so one barrier per descriptor orders the writes of n + 2 after the reads of n
+    static constexpr size_t kScratchFloats = (size_t)kNCW * kGroup * kScratchStride;
     static constexpr size_t kScratch = kQ + 2 * kQSlotBytes;
-    static constexpr size_t kML = kScratch + (size_t)kNCW * kGroup * kScratchStride * 4;
-    static constexpr size_t kMeta = kML + (size_t)kNCW * kGroup * 8;
+    static constexpr size_t kML = kScratch + 2 * kScratchFloats * 4;
+    static constexpr size_t kMeta = kML + 2 * (size_t)kNCW * kGroup * 8;
     static constexpr size_t kSink = kMeta + STAGES * 4;  // one word per consumer warp
     static constexpr size_t kBars = (kSink + kNCW * 4 + 7) / 8 * 8;
     static constexpr int kNumBars = 2 * STAGES + 5;
@@ -63,6 +69,7 @@ struct Layout {
     static constexpr size_t kTotal = kFlag + 16;
     static constexpr size_t kAlloc = kTotal + 1024;  // base is rounded up to 1 KB (128B swizzle)
     static constexpr int kThreads = (kNCW + 1) * 32;
+    static_assert(kAlloc <= 232448, "over the 227 KB shared-memory limit of a CTA");
 };
 
 template <bool FP8, bool QF8>
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], NCW);
         }
-        mbar_init(merge_bar, NCW * 32);
+        mbar_init(merge_bar, NCW);  // one arrival per consumer warp (lane 0, after __syncwarp)
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -233,7 +240,6 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
     }
     grid_dependency_wait();
     grid_launch_dependents();
-    const int list0 = p.cta_off[blockIdx.x];
 
     // ================================ consumer warps
     const int gi = warp >> 2, wq = warp & 3;
@@ -243,21 +249,21 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
     volatile uint32_t* q_sink = reinterpret_cast<volatile uint32_t*>(smem + LY::kSink);
     uint32_t seq = 0, mphase = 0;
     int qd = 0;
-    for (int slot = list0;; ++slot) {
-        const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-        const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
-        const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w, s = t1.x;
+    TaskAhead tw;
+    tw.start(p, p.cta_off[blockIdx.x]);
+    for (;;) {
+        const int h = tw.t0.x, b = tw.t0.y, c0 = tw.t0.z, c1 = tw.t0.w, s = tw.s;
         if (h < 0) break;
+        tw.next(p);
         if (!desc_ok(p, h, b, c0, c1, s)) continue;
-        (void)b;
 
         uint32_t qf[8][2];
         const int qs = qd & 1;
         if (!wait_bounded(&qfull[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs)) goto timeout;
-        load_q_frags<FP8, QF8>(smem_u32(qbuf + qs * kQSlotBytes), lane, qf);
+        load_q_frags<FP8, QF8, QF8 ? kQPitchE4m3 : kQPitchBf16>(smem_u32(qbuf + qs * kQSlotBytes), lane, qf);
         float qsc[2] = {1.f, 1.f};
         if constexpr (QF8) {
-            const float* qs_smem = reinterpret_cast<const float*>(qbuf + qs * kQSlotBytes + kGroup * kHeadDim);
+            const float* qs_smem = reinterpret_cast<const float*>(qbuf + qs * kQSlotBytes + kQScaleOffE4m3);
             qsc[0] = qs_smem[2 * c];
             qsc[1] = qs_smem[2 * c + 1];
         }
@@ -294,13 +300,16 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
                 if (lane == 0) mbar_arrive(&empty[st]);
             }
 
-            // ---- merge the NCW warps' states of this descriptor
+            // ---- merge the NCW warps' states of this descriptor (buffer mphase % 2;
+            // every warp read buffer mphase % 2 of two descriptors back before it
+            // arrived on the previous merge barrier, which this warp has passed)
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
                 l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
             }
-            float* scr = scratch + warp * kGroup * kScratchStride;
+            float* scr = scratch + (mphase & 1) * LY::kScratchFloats + warp * kGroup * kScratchStride;
+            float2* mlw = ml + (mphase & 1) * (NCW * kGroup);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 if constexpr (FP8) {
@@ -317,30 +326,32 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
                 }
             }
             if (g == 0) {
-                ml[warp * kGroup + 2 * c] = make_float2(m[0], l[0]);
-                ml[warp * kGroup + 2 * c + 1] = make_float2(m[1], l[1]);
+                mlw[warp * kGroup + 2 * c] = make_float2(m[0], l[0]);
+                mlw[warp * kGroup + 2 * c + 1] = make_float2(m[1], l[1]);
             }
         }
-        mbar_arrive(merge_bar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_bar);
         if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
-        ++mphase;
         {
+            const float* scr = scratch + (mphase & 1) * LY::kScratchFloats;
+            const float2* mlr = ml + (mphase & 1) * (NCW * kGroup);
             const int ct = warp * 32 + lane;
             for (int idx = ct; idx < kGroup * 32; idx += NCW * 32) {
                 const int qh = idx >> 5, d4 = idx & 31;
                 float M = kNegInf;
 #pragma unroll
-                for (int w = 0; w < NCW; ++w) M = fmaxf(M, ml[w * kGroup + qh].x);
+                for (int w = 0; w < NCW; ++w) M = fmaxf(M, mlr[w * kGroup + qh].x);
                 float lsum = 0.f;
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (M != kNegInf) {
 #pragma unroll
                     for (int w = 0; w < NCW; ++w) {
-                        const float2 v = ml[w * kGroup + qh];
+                        const float2 v = mlr[w * kGroup + qh];
                         const float f = fast_exp2(v.x - M);
                         lsum += v.y * f;
                         const float4 x = *reinterpret_cast<const float4*>(
-                            scratch + (w * kGroup + qh) * kScratchStride + 4 * d4);
+                            scr + (w * kGroup + qh) * kScratchStride + 4 * d4);
                         acc.x += f * x.x;
                         acc.y += f * x.y;
                         acc.z += f * x.z;
@@ -354,8 +365,6 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
                     p.split_lse[(long long)s * kGroup + qh] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : kNegInf;
             }
         }
-        mbar_arrive(merge_bar);
-        if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
         ++mphase;
     }
     return;

@@ -76,16 +76,90 @@ __device__ __forceinline__ bool desc_ok(const Params& p, int h, int b, int c0, i
            s >= 0 && s < p.split_cap;
 }
 
+// Walks a CTA's descriptor list one entry ahead. The entry after the current
+// one is in flight while the current one is processed, and (LEN) the live
+// length of its request and (PAGES) this lane's page id of its chunk c0 +
+// lane are loaded as soon as it becomes current, so a list of short
+// descriptors does not pay dependent global-memory round trips per
+// descriptor. Call next() right after copying the current fields, before the
+// descriptor's work. An entry past the current one is only read while the
+// current one is not the terminator, so every read stays inside the list.
+// len and pg are 0 for an entry outside the call's shapes (desc_ok false).
+template <bool LEN, bool PAGES>
+struct TaskWalker {
+    int4 t0, t1;  // current entry
+    int len;      // LEN: its request's live length
+    int pg;       // PAGES: page id of chunk t0.z + lane, when below t0.w
+    int4 n0, n1;  // the entry after it
+    int slot;
+
+    __device__ __forceinline__ static void fetch(const Params& p, int s, int4& a, int4& b) {
+        a = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)s * kTaskInts));
+        b = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)s * kTaskInts + 4));
+    }
+    __device__ __forceinline__ void side(const Params& p, int lane) {
+        len = 0;
+        pg = 0;
+        if ((LEN || PAGES) && t0.x >= 0 && desc_ok(p, t0.x, t0.y, t0.z, t0.w, t1.x)) {
+            if (LEN) len = __ldg(p.seq_lens + t0.y);
+            if (PAGES && t0.z + lane < t0.w) pg = __ldg(p.page_table + (long long)t0.y * p.pt_stride + t0.z + lane);
+        }
+    }
+    __device__ __forceinline__ void start(const Params& p, int list0, int lane) {
+        slot = list0;
+        fetch(p, slot, t0, t1);
+        side(p, lane);
+        n0 = make_int4(-1, -1, -1, -1);
+        n1 = n0;
+        if (t0.x >= 0) fetch(p, slot + 1, n0, n1);
+    }
+    __device__ __forceinline__ void next(const Params& p, int lane) {
+        if (t0.x < 0) return;
+        ++slot;
+        t0 = n0;
+        t1 = n1;
+        side(p, lane);
+        if (t0.x >= 0) fetch(p, slot + 1, n0, n1);
+    }
+};
+
+// The lighter form for loops that need only the entry itself: the next entry
+// (its kv head, request, chunk range and split index) is in flight while the
+// current descriptor is processed. Call next() right after copying the
+// current fields; the entry after the terminator is never read.
+struct TaskAhead {
+    int4 t0;  // current entry: kv head, request, first chunk, end chunk
+    int s;    // its split index
+    int slot;
+
+    __device__ __forceinline__ void fetch(const Params& p) {
+        t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
+        s = __ldg(p.tasks + (long long)slot * kTaskInts + 4);
+    }
+    __device__ __forceinline__ void start(const Params& p, int list0) {
+        slot = list0;
+        fetch(p);
+    }
+    __device__ __forceinline__ void next(const Params& p) {
+        if (t0.x < 0) return;
+        ++slot;
+        fetch(p);
+    }
+};
+
 // ------------------------------------------------------------------ consumer math
 
-template <bool FP8, bool QF8>
+// Query rows are staged PITCH bytes apart: 256 (bf16) or 128 (e4m3) packed,
+// or padded by 16 bytes (kQPitchBf16 / kQPitchE4m3) so that the 8 rows read
+// together fall into different shared-memory banks.
+template <bool FP8, bool QF8, uint32_t PITCH = (QF8 ? 128u : 256u)>
 __device__ __forceinline__ void load_q_frags(uint32_t qbase, int lane, uint32_t (&qf)[8][2]) {
     if constexpr (QF8) {
-        // e4m3 Q codes, rows of 128 bytes: thread (g, c) takes bytes [32c, 32c+32)
+        // e4m3 Q codes, 128 bytes per row: thread (g, c) takes bytes [32c, 32c+32)
         // of query g; k-step ks (32 dims) uses words 2ks and 2ks+1 of that slice,
         // matching the K words the same thread reads (see chunk_compute).
         const int g = lane >> 2, c = lane & 3;
-        const uint32_t base = qbase + (uint32_t)g * 128u + (uint32_t)c * 32u;
+        const uint32_t base = qbase + (uint32_t)g * PITCH + (uint32_t)c * 32u;
         const uint4 v0 = lds128(base), v1 = lds128(base + 16u);
         qf[0][0] = v0.x;
         qf[0][1] = v0.y;
@@ -102,7 +176,7 @@ __device__ __forceinline__ void load_q_frags(uint32_t qbase, int lane, uint32_t 
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
             uint32_t r[4];
-            ldsm_x4(r, qbase + (uint32_t)(lane & 7) * 256u + (uint32_t)(4 * kp + (lane >> 3)) * 16u);
+            ldsm_x4(r, qbase + (uint32_t)(lane & 7) * PITCH + (uint32_t)(4 * kp + (lane >> 3)) * 16u);
             qf[2 * kp][0] = r[0];
             qf[2 * kp][1] = r[1];
             qf[2 * kp + 1][0] = r[2];
@@ -112,7 +186,7 @@ __device__ __forceinline__ void load_q_frags(uint32_t qbase, int lane, uint32_t 
         // Thread (g, c) holds dims [32c, 32c+32) of query g; k-step ks uses
         // dims 32c+4ks+{0,1} (b0b1) and 32c+4ks+{2,3} (b2b3), widened to f16.
         const int g = lane >> 2, c = lane & 3;
-        const uint32_t base = qbase + (uint32_t)g * 256u + (uint32_t)c * 64u;
+        const uint32_t base = qbase + (uint32_t)g * PITCH + (uint32_t)c * 64u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint4 v = lds128(base + 16u * i);
@@ -186,14 +260,19 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int wq, int nv, int 
 
 // How the producer stages the query rows of a descriptor.
 enum class QStage {
-    kBf16,      // one new token: 8 bf16 rows (2 KB)
-    kE4m3,      // one new token: 8 rows of e4m3 codes, then their 8 float32 scales
+    kBf16,      // one new token: 8 bf16 rows, kQPitchBf16 bytes apart
+    kE4m3,      // one new token: 8 rows of e4m3 codes kQPitchE4m3 bytes apart, then their 8 float32 scales
     kBf16Rows,  // p.q_len new tokens: p.q_len blocks of 8 bf16 rows
     kBf16Tile,  // p.q_len new tokens as one 128-byte-swizzled tile [2 dim halves][8 q_len rows][128 B]
                 // by two 3-D TMA loads through tm_q (an MMA operand as it lands)
 };
 
 constexpr int kQRowsBytes = kGroup * kHeadDim * 2;  // 8 bf16 query rows
+// padded row pitches of the one-token query slot (one 16-byte piece per row
+// shifts the rows' banks: reads of all 8 rows at one column are conflict-free)
+constexpr uint32_t kQPitchBf16 = 256 + 16;
+constexpr uint32_t kQPitchE4m3 = 128 + 16;
+constexpr uint32_t kQScaleOffE4m3 = kGroup * kQPitchE4m3;  // the 8 float32 scales after the codes
 
 // Producer warp of a decode attention CTA. It waits for the preceding kernel
 // itself (the kernel's other warps wait before they start): at once, or, with
@@ -276,21 +355,21 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
     npre = __shfl_sync(0xffffffffu, npre, 0);
     grid_dependency_wait();
     grid_launch_dependents();
-    const int list0 = p.cta_off[blockIdx.x];
+    TaskWalker<true, true> tw;
+    tw.start(p, p.cta_off[blockIdx.x], lane);
     uint32_t seq = 0;
     int qd = 0;
     bool ok = true;
-    for (int slot = list0; ok; ++slot) {
-        const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-        const int4 t1 =
-            __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
+    while (ok) {
+        const int4 t0 = tw.t0, t1 = tw.t1;
+        const int L = tw.len, pg0 = tw.pg;
         const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
         if (h < 0) break;
+        tw.next(p, lane);
         if (!desc_ok(p, h, b, c0, c1, t1.x)) {
             if (lane == 0) atomicOr(p.err, (int)HPC_DEVERR_BAD_DESCRIPTOR);
             continue;
         }
-        const int L = __ldg(p.seq_lens + b);
         const int qs = qd & 1;
         if (lane == 0) {
             ok = wait_bounded(&qempty[qs], ((qd >> 1) & 1) ^ 1, abort_flag, kWaitLimitNs);
@@ -304,15 +383,22 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
                     tma_load_3d(qdst, tm_q, &qfull[qs], 0, h * kGroup, b * p.q_len, pol);
                     tma_load_3d(qdst + q_slot_bytes / 2, tm_q, &qfull[qs], 64, h * kGroup, b * p.q_len, pol);
                 } else if constexpr (QM == QStage::kE4m3) {
-                    // 8 rows of 128 e4m3 codes, then their 8 scales
+                    // 8 rows of 128 e4m3 codes (padded pitch), then their 8 scales
                     const long long qrow = (long long)b * p.num_q_heads + (long long)h * kGroup;
                     mbar_arrive_expect_tx(&qfull[qs], kGroup * kHeadDim + kGroup * 4);
-                    bulk_load_nohint(qdst, p.q8 + qrow * kHeadDim, kGroup * kHeadDim, &qfull[qs]);
-                    bulk_load_nohint(qdst + kGroup * kHeadDim, p.q_scale + qrow, kGroup * 4, &qfull[qs]);
+                    for (int r = 0; r < kGroup; ++r)
+                        bulk_load_nohint(qdst + r * kQPitchE4m3, p.q8 + (qrow + r) * kHeadDim, kHeadDim, &qfull[qs]);
+                    bulk_load_nohint(qdst + kQScaleOffE4m3, p.q_scale + qrow, kGroup * 4, &qfull[qs]);
+                } else if constexpr (QM == QStage::kBf16) {
+                    // 8 bf16 rows (padded pitch): query heads [8h, 8h + 8) of request b
+                    const long long qrow = (long long)b * p.num_q_heads + (long long)h * kGroup;
+                    mbar_arrive_expect_tx(&qfull[qs], kQRowsBytes);
+                    for (int r = 0; r < kGroup; ++r)
+                        bulk_load_nohint(qdst + r * kQPitchBf16, p.q + (qrow + r) * kHeadDim, kHeadDim * 2, &qfull[qs]);
                 } else {
                     // q_len blocks of 8 bf16 rows (2 KB each): new token i of request b,
                     // query heads [8h, 8h + 8)
-                    const int nq = QM == QStage::kBf16 ? 1 : p.q_len;
+                    const int nq = p.q_len;
                     mbar_arrive_expect_tx(&qfull[qs], (uint32_t)nq * kQRowsBytes);
                     for (int i = 0; i < nq; ++i) {
                         const long long qrow = ((long long)b * nq + i) * p.num_q_heads + (long long)h * kGroup;
@@ -326,7 +412,7 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
         const int32_t* prow = p.page_table + (long long)b * p.pt_stride;
         for (int cb = c0; cb < c1 && ok; cb += 32) {
             const int cl = cb + lane;
-            const int pg = cl < c1 ? __ldg(prow + cl) : 0;
+            const int pg = cb == c0 ? pg0 : (cl < c1 ? __ldg(prow + cl) : 0);
             const int n = min(32, c1 - cb);
             for (int j = 0; j < n; ++j, ++seq) {
                 const int page = __shfl_sync(0xffffffffu, pg, j);

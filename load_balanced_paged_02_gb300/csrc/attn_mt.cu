@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], NCW);
         }
-        mbar_init(merge_bar, NCW * 32);
+        mbar_init(merge_bar, NCW);  // one arrival per consumer warp (lane 0, after __syncwarp)
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -247,7 +247,6 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
     }
     grid_dependency_wait();
     grid_launch_dependents();
-    const int list0 = p.cta_off[blockIdx.x];
 
     // ================================ consumer warps
     const int gi = warp / LY::kWPG, qw = (warp % LY::kWPG) / TS, ts = warp % TS;
@@ -260,11 +259,12 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
     volatile uint32_t* q_sink = reinterpret_cast<volatile uint32_t*>(smem + LY::kSink);
     uint32_t seq = 0, mphase = 0;
     int qd = 0;
-    for (int slot = list0;; ++slot) {
-        const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-        const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
-        const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w, s = t1.x;
+    TaskAhead tw;
+    tw.start(p, p.cta_off[blockIdx.x]);
+    for (;;) {
+        const int h = tw.t0.x, b = tw.t0.y, c0 = tw.t0.z, c1 = tw.t0.w, s = tw.s;
         if (h < 0) break;
+        tw.next(p);
         if (!desc_ok(p, h, b, c0, c1, s)) continue;
         const int L = __ldg(p.seq_lens + b);
 
@@ -335,7 +335,8 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
                     dst[1] = make_float2(m[t][1], l[t][1]);
                 }
             }
-            mbar_arrive(merge_bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(merge_bar);
             if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
             ++mphase;
 
@@ -386,7 +387,8 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
                         }
                     }
                 }
-                mbar_arrive(merge_bar);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(merge_bar);
                 if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
                 ++mphase;
             }
@@ -416,7 +418,8 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
                 if (d4 == 0) p.split_lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : kNegInf;
             }
         }
-        mbar_arrive(merge_bar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(merge_bar);
         if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
         ++mphase;
     }

@@ -248,7 +248,7 @@ __global__ void __maxnreg__(168)
                           const __grid_constant__ CUtensorMap tm_vs, const Params p) {
     using LY = TcLayout<FP8>;
     using C = TcCfg<FP8>;
-    constexpr int NS = C::kStages, NO = C::kOpSlots;
+    constexpr int NS = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -353,12 +353,13 @@ __global__ void __maxnreg__(168)
             uint32_t seq = 0;  // chunks of this CTA
             int qd = 0;
             bool ok = true;
-            for (int slot = list0; ok; ++slot) {
-                const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-                const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
-                const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
+            TaskAhead tw;
+            tw.start(p, list0);
+            while (ok) {
+                const int h = tw.t0.x, b = tw.t0.y, c0 = tw.t0.z, c1 = tw.t0.w, sx = tw.s;
                 if (h < 0) break;
-                if (!desc_ok(p, h, b, c0, c1, t1.x)) continue;
+                tw.next(p);
+                if (!desc_ok(p, h, b, c0, c1, sx)) continue;
                 const int qs = qd & 1;
                 ok = wait_bounded(&q_ready[qs], (qd >> 1) & 1, abort_flag, kWaitLimitNs);
                 if (!ok) break;
@@ -413,12 +414,13 @@ __global__ void __maxnreg__(168)
             uint32_t seq = 0;
             int nd = 0;
             bool ok = true;
-            for (int slot = list0; ok; ++slot) {
-                const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-                const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
-                const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
+            TaskAhead tw;
+            tw.start(p, list0);
+            while (ok) {
+                const int h = tw.t0.x, b = tw.t0.y, c0 = tw.t0.z, c1 = tw.t0.w, sx = tw.s;
                 if (h < 0) break;
-                if (!desc_ok(p, h, b, c0, c1, t1.x)) continue;
+                tw.next(p);
+                if (!desc_ok(p, h, b, c0, c1, sx)) continue;
                 // the descriptor's first P . V overwrites the O tiles: the epilogue of
                 // the previous descriptor must have read them
                 if (nd > 0) {
@@ -460,12 +462,13 @@ __global__ void __maxnreg__(168)
             float* qsc = reinterpret_cast<float*>(smem + LY::kQsc);
             int qd = 0;
             bool ok = true;
-            for (int slot = list0; ok; ++slot) {
-                const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-                const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
-                const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w;
+            TaskAhead tw;
+            tw.start(p, list0);
+            while (ok) {
+                const int h = tw.t0.x, b = tw.t0.y, c0 = tw.t0.z, c1 = tw.t0.w, sx = tw.s;
                 if (h < 0) break;
-                if (!desc_ok(p, h, b, c0, c1, t1.x)) continue;
+                tw.next(p);
+                if (!desc_ok(p, h, b, c0, c1, sx)) continue;
                 const int qs = qd & 1;
                 // (the producer refills slot qs only after both softmax warpgroups
                 // finished the descriptor two back)
@@ -559,13 +562,14 @@ __global__ void __maxnreg__(168)
         float sc_a = p.scale_log2, sc_b = p.scale_log2;
         uint32_t seq = 0;
         int nd = 0;
-        for (int slot = list0;; ++slot) {
-            const int4 t0 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts));
-            const int4 t1 = __ldg(reinterpret_cast<const int4*>(p.tasks + (long long)slot * kTaskInts + 4));
-            const int h = t0.x, b = t0.y, c0 = t0.z, c1 = t0.w, s = t1.x;
+        TaskWalker<true, false> tw;
+        tw.start(p, list0, lane);
+        for (;;) {
+            const int h = tw.t0.x, b = tw.t0.y, c0 = tw.t0.z, c1 = tw.t0.w, s = tw.t1.x;
+            const int L = tw.len;
             if (h < 0) break;
+            tw.next(p, lane);
             if (!desc_ok(p, h, b, c0, c1, s)) continue;
-            const int L = __ldg(p.seq_lens + b);
             // reference maxima (log2 domain) and this thread's part of the row sums
             float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;
             if constexpr (FP8) {
