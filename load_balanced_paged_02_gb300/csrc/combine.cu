@@ -4,21 +4,29 @@
 // normalisation; vLLM x HPC-Ops blog, "解决方案：按步负载均衡的 decode 调度器",
 // the final combine into the BF16 output).
 //
-// One warp per output row (request b, new token i, query head qh); lane k
-// owns dims [4k, 4k+4). With n partials (o_i, lse_i) of pair (qh / 8, b):
-//   M = max lse_i, w_i = exp(lse_i - M), out = sum w_i o_i / sum w_i,
-//   out_lse = M + ln sum w_i.
-// A long request can leave a pair with ~100 partials, so the weights of a
-// tile of splits are staged in shared memory and eight partial rows per lane
-// are loaded before they are accumulated (the loop is latency bound).
+// Two forms, the same sums in the same order per output row (so the same bits):
+//  - rows: one warp per output row (request b, new token i, query head qh),
+//    lane k owning dims [4k, 4k+4); the weights of a tile of splits are staged
+//    in shared memory and eight partial rows per lane are loaded before they
+//    are accumulated (a long request can leave a pair with ~100 partials);
+//  - pairs: one warp per (KV-head pair, new token): the 8 query heads of the
+//    pair share its split range, so one lookup of (n, s0) serves 8 rows and
+//    each split contributes 8 independent row loads per lane.
+// The launcher takes the pair form when there are enough (pair, token) tasks
+// to fill the GPU with it (batches of many short requests), else the row form,
+// which spreads a pair's splits over 8 warps. With n partials (o_i, lse_i) of
+// a row: M = max lse_i, w_i = exp(lse_i - M), out = sum w_i o_i / sum w_i,
+// out_lse = M + ln sum w_i; weights lane-strided then reduced over the warp,
+// weighted rows summed split by split.
 #include "hpc_internal.cuh"
 
 namespace hpc {
 namespace {
 
 constexpr int kCombineWarps = 8;
-constexpr int kWTile = 256;  // split weights staged per warp at a time
-constexpr int kUnroll = 8;   // split rows in flight per lane
+constexpr int kWTile = 64;     // pair form: splits whose 8 weights are staged per warp at a time
+constexpr int kRowTile = 256;  // row form: split weights staged per warp at a time
+constexpr int kUnroll = 8;     // row form: split rows in flight per lane
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -34,11 +42,145 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__global__ void __launch_bounds__(kCombineWarps * 32)
-    combine_kernel(const int32_t* __restrict__ pair_nsplit, const int32_t* __restrict__ pair_split0,
+// The 8 LSEs of one split for rows jb .. jb + 7 (32 contiguous, 32-byte aligned bytes).
+__device__ __forceinline__ void load_lse8(const float* p, float (&l)[kGroup]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 c = *reinterpret_cast<const float4*>(p + 4);
+    l[0] = a.x, l[1] = a.y, l[2] = a.z, l[3] = a.w, l[4] = c.x, l[5] = c.y, l[6] = c.z, l[7] = c.w;
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32, 2)
+    combine_pairs_kernel(const int32_t* __restrict__ pair_nsplit, const int32_t* __restrict__ pair_split0,
                    const float* __restrict__ split_o, const float* __restrict__ split_lse,
                    __nv_bfloat16* __restrict__ out, float* __restrict__ out_lse, int B, int Hq, int Q) {
-    __shared__ float wsh[kCombineWarps][kWTile];
+    __shared__ float wsh[kCombineWarps][kWTile][kGroup];
+    grid_dependency_wait();  // the partials come from the attention kernel
+    grid_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = Hq / kGroup;
+    const long long task = (long long)blockIdx.x * kCombineWarps + warp;
+    if (task >= (long long)Hkv * B * Q) return;
+    const long long pair = task / Q;  // h * B + b
+    const int qi = (int)(task % Q);
+    const int h = (int)(pair / B), b = (int)(pair % B);
+    const int n = pair_nsplit[pair];
+    // partial rows of split s are [s][Q][8]: head j of new token qi in split s is
+    // row s * rs + jb + j
+    const long long s0 = pair_split0[pair];
+    const long long rs = (long long)Q * kGroup;
+    const int jb = qi * kGroup;
+
+    float4 acc[kGroup];
+    float lse[kGroup];
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        lse[j] = -INFINITY;
+    }
+    if (n == 1) {
+        const float* base = split_o + (s0 * rs + jb) * kHeadDim + 4 * lane;
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) acc[j] = *reinterpret_cast<const float4*>(base + j * kHeadDim);
+        load_lse8(split_lse + s0 * rs + jb, lse);
+    } else if (n > 1) {
+        float M[kGroup];
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) M[j] = -INFINITY;
+        for (int i = lane; i < n; i += 32) {
+            float l[kGroup];
+            load_lse8(split_lse + (s0 + i) * rs + jb, l);
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) M[j] = fmaxf(M[j], l[j]);
+        }
+        float wpart[kGroup];
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+            M[j] = warp_max(M[j]);
+            wpart[j] = 0.f;
+        }
+        for (int t0 = 0; t0 < n; t0 += kWTile) {
+            const int tn = min(kWTile, n - t0);
+            for (int i = lane; i < tn; i += 32) {
+                float l[kGroup];
+                load_lse8(split_lse + (s0 + t0 + i) * rs + jb, l);
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) {
+                    const float w = M[j] == -INFINITY ? 0.f : exp2f((l[j] - M[j]) * kLog2e);
+                    wsh[warp][i][j] = w;
+                    wpart[j] += w;
+                }
+            }
+            __syncwarp();
+            const float* base = split_o + ((s0 + t0) * rs + jb) * kHeadDim + 4 * lane;
+            int i = 0;
+            for (; i + 2 <= tn; i += 2) {
+                float4 x[2][kGroup];
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int j = 0; j < kGroup; ++j)
+                        x[u][j] = *reinterpret_cast<const float4*>(base + ((i + u) * rs + j) * kHeadDim);
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int j = 0; j < kGroup; ++j) {
+                        if (M[j] == -INFINITY) continue;
+                        const float w = wsh[warp][i + u][j];
+                        acc[j].x += w * x[u][j].x;
+                        acc[j].y += w * x[u][j].y;
+                        acc[j].z += w * x[u][j].z;
+                        acc[j].w += w * x[u][j].w;
+                    }
+            }
+            for (; i < tn; ++i) {
+#pragma unroll
+                for (int j = 0; j < kGroup; ++j) {
+                    const float4 x = *reinterpret_cast<const float4*>(base + (i * rs + j) * kHeadDim);
+                    if (M[j] == -INFINITY) continue;
+                    const float w = wsh[warp][i][j];
+                    acc[j].x += w * x.x;
+                    acc[j].y += w * x.y;
+                    acc[j].z += w * x.z;
+                    acc[j].w += w * x.w;
+                }
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+            const float wsum = warp_sum(wpart[j]);
+            if (M[j] == -INFINITY) continue;
+            const float inv = 1.f / wsum;
+            acc[j].x *= inv;
+            acc[j].y *= inv;
+            acc[j].z *= inv;
+            acc[j].w *= inv;
+            lse[j] = M[j] + log2f(wsum) * kLn2;
+        }
+    }
+    const long long row0 = ((long long)b * Q + qi) * Hq + (long long)h * kGroup;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x, acc[j].y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z, acc[j].w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + (row0 + j) * kHeadDim + 4 * lane) = packed;
+    }
+    if (out_lse && lane < kGroup) {
+        float v = lse[0];
+#pragma unroll
+        for (int j = 1; j < kGroup; ++j) v = lane == j ? lse[j] : v;
+        out_lse[row0 + lane] = v;
+    }
+}
+
+__global__ void __launch_bounds__(kCombineWarps * 32)
+    combine_rows_kernel(const int32_t* __restrict__ pair_nsplit, const int32_t* __restrict__ pair_split0,
+                   const float* __restrict__ split_o, const float* __restrict__ split_lse,
+                   __nv_bfloat16* __restrict__ out, float* __restrict__ out_lse, int B, int Hq, int Q) {
+    __shared__ float wsh[kCombineWarps][kRowTile];
     grid_dependency_wait();  // the partials come from the attention kernel
     grid_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -67,8 +209,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
         M = warp_max(M);
         if (M != -INFINITY) {
             float wpart = 0.f;
-            for (int t0 = 0; t0 < n; t0 += kWTile) {
-                const int tn = min(kWTile, n - t0);
+            for (int t0 = 0; t0 < n; t0 += kRowTile) {
+                const int tn = min(kRowTile, n - t0);
                 // weights of this tile, one per lane-strided split
                 for (int i = lane; i < tn; i += 32) {
                     const float w = exp2f((split_lse[(s0 + t0 + i) * rs + j] - M) * kLog2e);
@@ -126,9 +268,23 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o, const float* split_lse,
                            __nv_bfloat16* out, float* out_lse, int B, int Hq, int Hkv, int q_len, cudaStream_t s) {
     const PlanLayout L = plan_layout(B, Hkv, C);
-    const long long rows = (long long)B * q_len * Hq;
+    const long long tasks = (long long)Hkv * B * q_len;  // (pair, new token)
+    // one wave of the pair form: 2 blocks of 8 warps per SM (its register bound)
+    static const long long full_wave = [] {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 0;
+        return (long long)(sms > 0 ? sms : 152) * 2 * kCombineWarps;
+    }();
+    if (tasks >= full_wave) {
+        const long long blocks = (tasks + kCombineWarps - 1) / kCombineWarps;
+        return launch_pdl(combine_pairs_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+                          plan + L.pair_nsplit, plan + L.pair_split0, split_o, split_lse, out, out_lse, B, Hq, q_len);
+    }
+    const long long rows = tasks * kGroup;
     const long long blocks = (rows + kCombineWarps - 1) / kCombineWarps;
-    return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+    return launch_pdl(combine_rows_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
                       plan + L.pair_nsplit, plan + L.pair_split0, split_o, split_lse, out, out_lse, B, Hq, q_len);
 }
 
