@@ -24,7 +24,9 @@
  *   - Pointers named d_* or documented as "device" are device pointers; h_*
  *     are host pointers. The caller owns all memory. The library never
  *     allocates, frees or synchronises inside these calls (except
- *     hpc_decode_read_error, which synchronises by design).
+ *     hpc_decode_read_error, which synchronises by design, and
+ *     hpc_decode_step_graph_create / _destroy, which allocate and free a
+ *     captured step).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Work is enqueued asynchronously on it.
  *   - Supported shapes: head_dim == 128, page_size == 64 (one chunk is one
@@ -378,13 +380,19 @@ size_t hpc_decode_step_workspace_bytes(int batch, int num_q_heads, int num_kv_he
                                        int page_table_stride, int num_ctas);
 
 /*
- * One decode step from host buffers: copies h_q, h_seq_lens and h_page_table
- * into d_workspace (cudaMemcpyAsync, host -> device), plans with num_ctas and
- * min_chunks_per_cta, runs attention over the device-resident caches,
- * combines, and copies out (and out_lse, if h_out_lse is non-NULL) back to the
- * host. Everything is enqueued on `stream`; the caller synchronises the
- * stream before reading h_out. Host buffers should be pinned for the copies
- * to be asynchronous. Same errors as the calls it chains.
+ * One decode step from host buffers: brings h_q, h_seq_lens and h_page_table
+ * into d_workspace, plans with num_ctas and min_chunks_per_cta, runs attention
+ * over the device-resident caches, combines, and delivers out (and out_lse,
+ * if h_out_lse is non-NULL) to the host. Everything is enqueued on `stream`;
+ * the caller synchronises the stream before reading h_out.
+ * When all the host buffers are page-locked and mapped into the device's
+ * address space (cudaHostAlloc, or cudaHostRegister with
+ * cudaHostRegisterMapped; cudaPointerGetAttributes reports them as host
+ * memory with a device pointer), one staging kernel reads the inputs over the
+ * host link and the combine writes the outputs straight into h_out and
+ * h_out_lse (h_out 8-byte aligned). Otherwise the inputs and outputs go
+ * through cudaMemcpyAsync (synchronous for pageable memory). Same errors as
+ * the calls it chains.
  */
 hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens,
                                 const int32_t* h_page_table, int page_table_stride,
@@ -394,6 +402,41 @@ hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens,
                                 int head_dim, int page_size, int num_ctas, int min_chunks_per_cta,
                                 void* d_workspace, size_t workspace_bytes, void* h_out,
                                 float* h_out_lse, void* stream);
+
+/* One hpc_decode_step_host call captured as a CUDA graph (opaque). */
+typedef struct hpc_step_graph hpc_step_graph;
+
+/*
+ * Captures the work of hpc_decode_step_host (the three host -> device copies,
+ * plan, attention, combine and the copies back into h_out and h_out_lse) as a
+ * CUDA graph, so that each step is one graph launch instead of eight
+ * enqueues. Every pointer and size is fixed at capture: the caller refills
+ * the host input buffers in place and reads the output buffers after each
+ * launch. Host buffers must be pinned (capture of a copy from pageable memory
+ * fails). Capture runs on a stream of its own, so this call performs no step;
+ * it sets the kernels' one-time attributes first and allocates the graph and
+ * its handle (host and driver memory) until hpc_decode_step_graph_destroy.
+ * Errors: as hpc_decode_step_host; HPC_ERR_INVALID_ARG for graph == NULL;
+ * HPC_ERR_CUDA if capture or instantiation fails (*graph is then NULL).
+ */
+hpc_status hpc_decode_step_graph_create(const void* h_q, const int32_t* h_seq_lens,
+                                        const int32_t* h_page_table, int page_table_stride,
+                                        const void* d_k_cache, const void* d_v_cache,
+                                        const float* d_k_scale, const float* d_v_scale,
+                                        int kv_dtype, int num_pages, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int page_size, int num_ctas,
+                                        int min_chunks_per_cta, void* d_workspace,
+                                        size_t workspace_bytes, void* h_out, float* h_out_lse,
+                                        hpc_step_graph** graph);
+
+/* Enqueues one captured step on `stream`; synchronise the stream before
+ * reading the outputs. Launches on one graph are ordered by the stream; two
+ * launches of the same graph must not overlap (they share the workspace and
+ * the host buffers). Errors: HPC_ERR_INVALID_ARG, HPC_ERR_CUDA. */
+hpc_status hpc_decode_step_graph_launch(hpc_step_graph* graph, void* stream);
+
+/* Frees a captured step (NULL is a no-op). Its launches must have completed. */
+hpc_status hpc_decode_step_graph_destroy(hpc_step_graph* graph);
 
 /*
  * One decode step (plan -> attention -> combine) that allocates nothing. The

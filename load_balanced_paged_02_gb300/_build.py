@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "hpcdecode")
 LIB_PATH = os.path.join(HERE, "libhpcdecode.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cu", "attn.cu", "attn_mt.cu", "attn_tc.cu", "combine.cu", "prologue.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["plan.cu", "attn.cu", "attn_mt.cu", "attn_tc.cu", "combine.cu", "prologue.cu", "api.cu", "noalloc.cu",
+           "stage.cu"]
 
 
 def nvcc() -> str:

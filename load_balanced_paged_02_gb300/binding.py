@@ -69,6 +69,10 @@ SIGNATURES = {
     "hpc_decode_step_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "hpc_decode_step_host": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                   _i, _i, _vp, _sz, _vp, _vp, _vp]),
+    "hpc_decode_step_graph_create": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                                          _i, _vp, _sz, _vp, _vp, ctypes.POINTER(_vp)]),
+    "hpc_decode_step_graph_launch": (_i, [_vp, _vp]),
+    "hpc_decode_step_graph_destroy": (_i, [_vp]),
     "hpc_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                 _i, _vp, _vp, _vp]),
     "hpc_decode_read_error": (_i, [_P, ctypes.POINTER(_i)]),
@@ -348,6 +352,48 @@ def hpc_decode_step_host(h_q, h_seq_lens, h_page_table, k_cache, v_cache, worksp
         int(k_cache.shape[1]), num_ctas, min_chunks_per_cta, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(h_out), _ptr(h_out_lse), _stream(stream))
     _check("hpc_decode_step_host", rc)
+
+
+class StepGraph:
+    """hpc_decode_step_host captured once as a CUDA graph (hpc_decode_step_graph_*).
+    The tensors given here are fixed: refill the pinned host inputs in place,
+    call launch(), synchronise the stream, then read h_out / h_out_lse."""
+
+    def __init__(self, h_q, h_seq_lens, h_page_table, k_cache, v_cache, workspace, h_out, h_out_lse=None,
+                 k_scale=None, v_scale=None, num_ctas=None, min_chunks_per_cta: int = 2, num_pages=None):
+        B, Hq, D = h_q.shape
+        Hkv = k_cache.shape[2]
+        if num_ctas is None:
+            num_ctas = default_num_ctas(kv_dtype_of(k_cache))
+        # keep every tensor the graph points into alive as long as the graph
+        self._keep = (h_q, h_seq_lens, h_page_table, k_cache, v_cache, workspace, h_out, h_out_lse, k_scale,
+                      v_scale)
+        handle = _vp()
+        rc = lib().hpc_decode_step_graph_create(
+            _ptr(h_q), _ptr(h_seq_lens), _ptr(h_page_table), int(h_page_table.shape[1]),
+            _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), kv_dtype_of(k_cache),
+            int(num_pages if num_pages is not None else k_cache.shape[0]), B, Hq, Hkv, D,
+            int(k_cache.shape[1]), num_ctas, min_chunks_per_cta, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(h_out), _ptr(h_out_lse), ctypes.byref(handle))
+        _check("hpc_decode_step_graph_create", rc)
+        self._handle = handle
+
+    def launch(self, stream=None):
+        if not self._handle:
+            raise HpcError("hpc_decode_step_graph_launch", detail="the graph was closed")
+        _check("hpc_decode_step_graph_launch", lib().hpc_decode_step_graph_launch(self._handle, _stream(stream)))
+
+    def close(self):
+        if self._handle:
+            rc = lib().hpc_decode_step_graph_destroy(self._handle)
+            self._handle = _vp()
+            _check("hpc_decode_step_graph_destroy", rc)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def hpc_rope_norm(qkv, positions, cos_sin, q_weight, k_weight, slot_mapping, q_out, k_cache, v_cache,

@@ -2,6 +2,8 @@
 // host-side argument checks, then the launches in plan.cu, attn.cu and
 // combine.cu. Nothing here allocates device memory or synchronises, except
 // hpc_decode_read_error.
+#include <new>
+
 #include "hpc_internal.cuh"
 
 using namespace hpc;
@@ -35,6 +37,17 @@ hpc_status plan_check(const hpc_plan* plan, int batch, int num_kv_heads) {
     if (plan->num_ctas < 1 || plan->bytes < plan_bytes_ll(batch, num_kv_heads, plan->num_ctas))
         return HPC_ERR_INVALID_ARG;
     return HPC_OK;
+}
+
+// The device address of page-locked, device-mapped host memory; nullptr for
+// anything else (pageable or device memory, or a failed query).
+void* mapped_host(const void* h) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, h) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
 struct StepWorkspace {
@@ -344,12 +357,28 @@ hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     const size_t q_bytes = (size_t)batch * num_q_heads * kHeadDim * 2;
-    if (cudaMemcpyAsync(ws + w.q, h_q, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-        cudaMemcpyAsync(ws + w.seq_lens, h_seq_lens, (size_t)batch * 4, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(ws + w.page_table, h_page_table, (size_t)batch * page_table_stride * 4,
-                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+    const size_t pt_bytes = (size_t)batch * page_table_stride * 4;
+    // Page-locked, device-mapped host buffers are read and written by the
+    // kernels themselves (one staging kernel in, the combine out); any other
+    // host memory goes through the copy engine.
+    void* m_q = mapped_host(h_q);
+    void* m_sl = mapped_host(h_seq_lens);
+    void* m_pt = mapped_host(h_page_table);
+    void* m_out = mapped_host(h_out);
+    void* m_lse = h_out_lse ? mapped_host(h_out_lse) : nullptr;
+    const bool zero_copy = m_q && m_sl && m_pt && m_out && (!h_out_lse || m_lse) && aligned(m_out, 8);
+    if (zero_copy) {
+        const StageCopy cq{static_cast<const uint8_t*>(m_q), ws + w.q, q_bytes};
+        const StageCopy csl{static_cast<const uint8_t*>(m_sl), ws + w.seq_lens, (size_t)batch * 4};
+        const StageCopy cpt{static_cast<const uint8_t*>(m_pt), ws + w.page_table, pt_bytes};
+        if (launch_stage_in(cq, csl, cpt, s) != cudaSuccess) return HPC_ERR_CUDA;
+    } else if (cudaMemcpyAsync(ws + w.q, h_q, q_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+               cudaMemcpyAsync(ws + w.seq_lens, h_seq_lens, (size_t)batch * 4, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess ||
+               cudaMemcpyAsync(ws + w.page_table, h_page_table, pt_bytes, cudaMemcpyHostToDevice, s) !=
+                   cudaSuccess) {
         return HPC_ERR_CUDA;
+    }
     hpc_plan plan{};
     plan.buf = reinterpret_cast<int32_t*>(ws + w.plan);
     plan.bytes = hpc_decode_plan_bytes(batch, num_kv_heads, num_ctas);
@@ -364,6 +393,10 @@ hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens, cons
         HPC_OK)
         return st;
     float* d_lse = reinterpret_cast<float*>(ws + w.out_lse);
+    if (zero_copy) {
+        return hpc_decode_combine(&plan, so, sl, m_out, static_cast<float*>(m_lse), batch, num_q_heads,
+                                  num_kv_heads, head_dim, stream);
+    }
     if ((st = hpc_decode_combine(&plan, so, sl, ws + w.out, d_lse, batch, num_q_heads, num_kv_heads, head_dim,
                                  stream)) != HPC_OK)
         return st;
@@ -372,6 +405,80 @@ hpc_status hpc_decode_step_host(const void* h_q, const int32_t* h_seq_lens, cons
         cudaMemcpyAsync(h_out_lse, d_lse, (size_t)batch * num_q_heads * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return HPC_ERR_CUDA;
     return HPC_OK;
+}
+
+}  // extern "C"
+
+struct hpc_step_graph {
+    cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+hpc_status hpc_decode_step_graph_create(const void* h_q, const int32_t* h_seq_lens, const int32_t* h_page_table,
+                                        int page_table_stride, const void* d_k_cache, const void* d_v_cache,
+                                        const float* d_k_scale, const float* d_v_scale, int kv_dtype,
+                                        int num_pages, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int page_size, int num_ctas, int min_chunks_per_cta, void* d_workspace,
+                                        size_t workspace_bytes, void* h_out, float* h_out_lse,
+                                        hpc_step_graph** graph) {
+    if (!graph) return HPC_ERR_INVALID_ARG;
+    *graph = nullptr;
+    // the checks of hpc_decode_step_host, before any CUDA call
+    hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
+    if (st != HPC_OK) return st;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+    if (!h_q || !h_seq_lens || !h_page_table || !d_workspace || !h_out) return HPC_ERR_INVALID_ARG;
+    if (!sizes_ok(batch, num_kv_heads, num_ctas) || page_table_stride < 1 || !aligned(d_workspace, 256))
+        return HPC_ERR_INVALID_ARG;
+    if (workspace_bytes < step_workspace(batch, num_q_heads, num_kv_heads, page_table_stride, num_ctas).total)
+        return HPC_ERR_WORKSPACE_TOO_SMALL;
+    // one-time launcher setup (kernel attributes) outside the capture
+    if (attn_default_ctas(kv_dtype == HPC_KV_FP8_E4M3) <= 0) return HPC_ERR_CUDA;
+    cudaStream_t cs = nullptr;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return HPC_ERR_CUDA;
+    cudaGraph_t g = nullptr;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return HPC_ERR_CUDA;
+    }
+    st = hpc_decode_step_host(h_q, h_seq_lens, h_page_table, page_table_stride, d_k_cache, d_v_cache, d_k_scale,
+                              d_v_scale, kv_dtype, num_pages, batch, num_q_heads, num_kv_heads, head_dim,
+                              page_size, num_ctas, min_chunks_per_cta, d_workspace, workspace_bytes, h_out,
+                              h_out_lse, cs);
+    const cudaError_t ce = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (st != HPC_OK || ce != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        (void)cudaGetLastError();
+        return st != HPC_OK ? st : HPC_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ie = cudaGraphInstantiate(&exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ie != cudaSuccess) {
+        (void)cudaGetLastError();
+        return HPC_ERR_CUDA;
+    }
+    hpc_step_graph* out = new (std::nothrow) hpc_step_graph{exec};
+    if (!out) {
+        cudaGraphExecDestroy(exec);
+        return HPC_ERR_CUDA;
+    }
+    *graph = out;
+    return HPC_OK;
+}
+
+hpc_status hpc_decode_step_graph_launch(hpc_step_graph* graph, void* stream) {
+    if (!graph || !graph->exec) return HPC_ERR_INVALID_ARG;
+    return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
+}
+
+hpc_status hpc_decode_step_graph_destroy(hpc_step_graph* graph) {
+    if (!graph) return HPC_OK;
+    const cudaError_t e = graph->exec ? cudaGraphExecDestroy(graph->exec) : cudaSuccess;
+    delete graph;
+    return e == cudaSuccess ? HPC_OK : HPC_ERR_CUDA;
 }
 
 hpc_status hpc_decode_read_error(const hpc_plan* plan, int* device_error_word) {

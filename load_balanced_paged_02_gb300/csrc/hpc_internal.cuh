@@ -115,6 +115,14 @@ struct RopeNormArgs {
 cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s);
 
 // q_len new tokens per request (1 for plain decode): rows (b, i, qh) of out.
+// One byte range for the zero-copy staging kernel (stage.cu).
+struct StageCopy {
+    const uint8_t* src;  // device-mapped host address
+    uint8_t* dst;        // device address
+    size_t bytes;
+};
+cudaError_t launch_stage_in(const StageCopy& a, const StageCopy& b, const StageCopy& c, cudaStream_t s);
+
 cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o,
                            const float* split_lse, __nv_bfloat16* out, float* out_lse, int B,
                            int Hq, int Hkv, int q_len, cudaStream_t s);

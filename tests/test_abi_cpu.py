@@ -138,6 +138,26 @@ def test_attn_ex_rejects_bad_arguments(L):
     assert call(D=64) == 2
 
 
+def test_step_graph_rejects_bad_arguments(L):
+    """hpc_decode_step_graph_*: argument checks before any CUDA call."""
+    handle = ctypes.c_void_p(1234)
+    args = [FAKE, FAKE, FAKE, 4, FAKE, FAKE, None, None, 0, 16, 2, 8, 1, 128, 64, 4, 2, FAKE, 1 << 30, FAKE, None]
+
+    def create(*over, graph=ctypes.byref(handle)):
+        a = list(args)
+        for i, v in over:
+            a[i] = v
+        return L.hpc_decode_step_graph_create(*a, graph)
+    assert create(graph=None) == 1
+    assert create((0, None)) == 1 and handle.value is None           # no h_q; *graph cleared
+    assert create((13, 64)) == 2                                       # head_dim
+    assert create((8, 7)) == 2                                         # kv dtype
+    assert create((17, FAKE_ODD)) == 1                                 # workspace alignment
+    assert create((18, 16)) == 3                                       # workspace too small
+    assert L.hpc_decode_step_graph_launch(None, None) == 1
+    assert L.hpc_decode_step_graph_destroy(None) == 0
+
+
 def test_plan_rejects_bad_arguments(L):
     p = hb.PlanStruct(FAKE.value, 1 << 20, 0, 0, 0, 0, 0, 0)
     assert L.hpc_decode_plan(None, 4, 1, 16, 2, ctypes.byref(p), None) == 1

@@ -270,6 +270,71 @@ def test_step_host_matches_device_path():
     assert torch.equal(h_lse, res["lse"].cpu())
 
 
+def test_step_host_pageable_buffers_take_the_copy_path():
+    """Pageable host buffers go through cudaMemcpyAsync (the mapped ones
+    through the staging kernel and the combine): same bytes either way."""
+    lens = [500, 64, 1300, 7]
+    case = case_for(lens, 2, seed=14)
+    res = _gpu.run(case, num_ctas=10)
+    B, Hq, D = case["q"].shape
+    ws = torch.empty(hb.step_workspace_bytes(B, Hq, 2, case["page_table"].shape[1], 10), dtype=torch.uint8,
+                     device=DEV)
+    for pinned in (False, True):
+        h = [case[k].cpu() for k in ("q", "seq_lens", "page_table")]
+        h_out = torch.full_like(h[0], float("nan"))
+        h_lse = torch.full((B, Hq), float("nan"), dtype=torch.float32)
+        if pinned:
+            h = [t.pin_memory() for t in h]
+            h_out, h_lse = h_out.pin_memory(), h_lse.pin_memory()
+        hb.hpc_decode_step_host(h[0], h[1], h[2], case["k_cache"], case["v_cache"], ws, h_out, h_lse,
+                                num_ctas=10, num_pages=case["num_pages"])
+        torch.cuda.synchronize()
+        assert torch.equal(h_out, res["out"].cpu()), f"pinned={pinned}"
+        assert torch.equal(h_lse, res["lse"].cpu()), f"pinned={pinned}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_step_graph_matches_step_host(dtype):
+    """The captured step (hpc_decode_step_graph_*) gives the bytes of
+    hpc_decode_step_host, and picks up new inputs written in place into its
+    pinned host buffers (new query, new lengths, so a new task map)."""
+    lens = [500, 64, 1300, 7, 0, 65]
+    case = case_for(lens, 2, dtype=dtype, seed=17)
+    B, Hq, D = case["q"].shape
+    C = 12
+    ws_bytes = hb.step_workspace_bytes(B, Hq, 2, case["page_table"].shape[1], C)
+    ws_a = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    ws_b = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    h_q = case["q"].cpu().pin_memory()
+    h_sl = case["seq_lens"].cpu().pin_memory()
+    h_pt = case["page_table"].cpu().pin_memory()
+    outs = [torch.empty_like(h_q).pin_memory() for _ in range(2)]
+    lses = [torch.empty((B, Hq), dtype=torch.float32).pin_memory() for _ in range(2)]
+    kw = dict(k_scale=case["k_scale"], v_scale=case["v_scale"], num_ctas=C, num_pages=case["num_pages"])
+    g = hb.StepGraph(h_q, h_sl, h_pt, case["k_cache"], case["v_cache"], ws_b, outs[1], lses[1], **kw)
+    try:
+        for step in range(3):
+            if step > 0:  # new inputs, in place
+                h_q.copy_(torch.randn(h_q.shape, generator=torch.Generator().manual_seed(step)).to(h_q.dtype))
+                # (each new length within the request's pages)
+                h_sl.copy_(torch.tensor([500 - 150 * step, 64 - step, 1300 - 200 * step, 7 - 2 * step, 0,
+                                         65 - 30 * step], dtype=torch.int32))
+            outs[1].fill_(float("nan"))
+            hb.hpc_decode_step_host(h_q, h_sl, h_pt, case["k_cache"], case["v_cache"], ws_a, outs[0], lses[0],
+                                    **kw)
+            g.launch()
+            torch.cuda.synchronize()
+            assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16)), f"step {step}"
+            assert torch.equal(lses[0].view(torch.int32), lses[1].view(torch.int32)), f"step {step}"
+        # and the last step against the oracle
+        host = wl.to_numpy_case(dict(case, q=h_q.to(DEV), seq_lens=h_sl.to(DEV)))
+        ro, rl = oracle.attn_rows(host)
+        _gpu.assert_close(outs[1].float().numpy(), lses[1].numpy(), ro.reshape(B, Hq, 128), rl.reshape(B, Hq),
+                          case, "captured step")
+    finally:
+        g.close()
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_cuda_graph_replay_recomputes_from_device_inputs(dtype):
     """The step (plan -> attn -> combine, chained with programmatic dependent
