@@ -178,17 +178,27 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) rope_norm_kernel(const
                 if (p.kv_fp8) scale_dst = (is_qk ? p.k_scale : p.v_scale) + ((size_t)page * p.Hkv + h) * kChunk + off;
             }
             if (fp8_row) {
-                // x / scale with a correctly rounded division: bf16 inputs often land
-                // exactly on e4m3 rounding midpoints, where a reciprocal's last-bit
-                // error would break the tie the other way
+                // x / scale correctly rounded: bf16 inputs often land exactly on e4m3
+                // rounding midpoints, where a last-bit error would break the tie the
+                // other way. Markstein's correction step (P. Markstein, "Computation
+                // of elementary functions on the IBM RISC System/6000 processor",
+                // IBM J. Res. Dev. 34(1), 1990): with y = RN(1 / scale), q = RN(x y)
+                // and the exact residual r = x - scale q (one FMA), RN(q + r y) is
+                // the correctly rounded quotient while nothing over- or underflows
+                // (|x / scale| <= 448 here).
                 const float scale = am > 0.f ? am / kE4m3Max : 1.f;
+                const float rcp = __frcp_rn(scale);
+                auto qdiv = [scale, rcp](float x) {
+                    const float q = x * rcp;
+                    return fmaf(fmaf(-q, scale, x), rcp, q);
+                };
                 uint32_t codes[2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                        make_float2(y[4 * k] / scale, y[4 * k + 1] / scale), __NV_SATFINITE, __NV_E4M3);
+                        make_float2(qdiv(y[4 * k]), qdiv(y[4 * k + 1])), __NV_SATFINITE, __NV_E4M3);
                     const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                        make_float2(y[4 * k + 2] / scale, y[4 * k + 3] / scale), __NV_SATFINITE, __NV_E4M3);
+                        make_float2(qdiv(y[4 * k + 2]), qdiv(y[4 * k + 3])), __NV_SATFINITE, __NV_E4M3);
                     codes[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
                 }
                 *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + dst_elem) = make_uint2(codes[0], codes[1]);
