@@ -69,7 +69,11 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&y)[8]) {
     }
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, 3) rope_norm_kernel(const PrologueParams p) {
+// MINB resident blocks per SM: 3 for decode-size calls (a few blocks, latency
+// bound), 4 for many tokens, where more blocks in flight keep more rows
+// loading (8192 tokens at 64/8 heads: 89.7 -> 81.5 us with bf16 outputs).
+template <int MINB>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(const PrologueParams p) {
     grid_dependency_wait();  // the QKV projection may still be finishing
     grid_launch_dependents();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -245,7 +249,10 @@ cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s) {
     const int rounds = (a.num_q_heads + 2 * a.num_kv_heads + kRowsPerRound - 1) / kRowsPerRound;
     p.rounds_per_block = (long long)a.num_tokens * rounds < 8LL * 152 ? 1 : rounds;
     const unsigned splits = (unsigned)((rounds + p.rounds_per_block - 1) / p.rounds_per_block);
-    return launch_pdl(rope_norm_kernel, dim3((unsigned)a.num_tokens, splits), dim3(kWarpsPerBlock * 32), 0, s, p);
+    const dim3 grid((unsigned)a.num_tokens, splits);
+    if ((long long)a.num_tokens * splits >= 4LL * 152 * 4)
+        return launch_pdl(rope_norm_kernel<4>, grid, dim3(kWarpsPerBlock * 32), 0, s, p);
+    return launch_pdl(rope_norm_kernel<3>, grid, dim3(kWarpsPerBlock * 32), 0, s, p);
 }
 
 }  // namespace hpc
