@@ -58,9 +58,10 @@ class Workload:
     extra: dict = field(default_factory=dict)
 
 
-# The five workloads the scope names, and the six length mixes of the pages'
-# decode-latency table (vLLM x HPC-Ops blog, Table 3), at the TP8-shard head
-# shape (8 query heads, 1 KV head) and at the full Hy3 shape.
+# The five workloads the scope names (plus a batch of many short requests),
+# and the six length mixes of the pages' decode-latency table (vLLM x HPC-Ops
+# blog, Table 3), at the TP8-shard head shape (8 query heads, 1 KV head) and
+# at the full Hy3 shape.
 WORKLOADS = {
     "tiny": Workload("tiny", 4, 8, 1, "bf16", 0, lens=[37, 128, 300, 1000], pool_pages=64,
                      num_ctas=16, min_chunks=2,
@@ -77,6 +78,11 @@ WORKLOADS = {
     "fp8q": Workload("fp8q", 64, 64, 8, "fp8", 4, loguniform=(512, 262144), total_cap=FOUR_M,
                      q_dtype="fp8",
                      note="the fp8 batch with e4m3 Q and a per-(request, head) Q scale"),
+    # many short requests: every (KV head, request) pair is one two-chunk
+    # descriptor, so per-descriptor costs (query staging, merge, partial
+    # write) and the combine's per-pair work dominate instead of the KV stream
+    "short": Workload("short", 1024, 64, 8, "bf16", 5, lens=[128] * 1024,
+                      note="batch 1024 x 128 tokens, 64 Q / 8 KV heads, bf16 (8192 two-chunk descriptors)"),
 }
 
 TABLE3_MIXES = {

@@ -423,7 +423,7 @@ def test_uniform_workload_full():
     _gpu.check_split_invariants(case, res)
 
 
-@pytest.mark.parametrize("name", ["mixed", "skew", "fp8", "fp8q"])
+@pytest.mark.parametrize("name", ["mixed", "skew", "fp8", "fp8q", "short"])
 def test_full_size_workload_sampled(name):
     w = wl.WORKLOADS[name]
     case = wl.make_case(w, device=DEV)
