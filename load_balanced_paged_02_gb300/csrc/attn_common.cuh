@@ -262,7 +262,7 @@ __device__ __forceinline__ void zero_v_tail(uint8_t* stage, int wq, int nv, int 
 enum class QStage {
     kBf16,      // one new token: 8 bf16 rows, kQPitchBf16 bytes apart
     kE4m3,      // one new token: 8 rows of e4m3 codes kQPitchE4m3 bytes apart, then their 8 float32 scales
-    kBf16Rows,  // p.q_len new tokens: p.q_len blocks of 8 bf16 rows
+    kBf16Rows,  // p.q_len new tokens: p.q_len blocks of 8 bf16 rows, kQPitchBf16 bytes apart
     kBf16Tile,  // p.q_len new tokens as one 128-byte-swizzled tile [2 dim halves][8 q_len rows][128 B]
                 // by two 3-D TMA loads through tm_q (an MMA operand as it lands)
 };
@@ -396,18 +396,24 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
                     for (int r = 0; r < kGroup; ++r)
                         bulk_load_nohint(qdst + r * kQPitchBf16, p.q + (qrow + r) * kHeadDim, kHeadDim * 2, &qfull[qs]);
                 } else {
-                    // q_len blocks of 8 bf16 rows (2 KB each): new token i of request b,
-                    // query heads [8h, 8h + 8)
-                    const int nq = p.q_len;
-                    mbar_arrive_expect_tx(&qfull[qs], (uint32_t)nq * kQRowsBytes);
-                    for (int i = 0; i < nq; ++i) {
-                        const long long qrow = ((long long)b * nq + i) * p.num_q_heads + (long long)h * kGroup;
-                        bulk_load_nohint(qdst + i * kQRowsBytes, p.q + qrow * kHeadDim, kQRowsBytes, &qfull[qs]);
-                    }
+                    // q_len blocks of 8 bf16 rows: row (i, j) = new token i of request
+                    // b, query head 8h + j, at the padded pitch; the warp's lanes issue
+                    // the copies below, after this expectation is set
+                    mbar_arrive_expect_tx(&qfull[qs], (uint32_t)p.q_len * kQRowsBytes);
                 }
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
+        if constexpr (QM == QStage::kBf16Rows) {
+            if (ok) {
+                uint8_t* qdst = qbuf + qs * q_slot_bytes;
+                for (int r = lane; r < p.q_len * kGroup; r += 32) {
+                    const int i = r / kGroup, j = r % kGroup;
+                    const long long qrow = ((long long)b * p.q_len + i) * p.num_q_heads + (long long)h * kGroup + j;
+                    bulk_load_nohint(qdst + r * kQPitchBf16, p.q + qrow * kHeadDim, kHeadDim * 2, &qfull[qs]);
+                }
+            }
+        }
         ++qd;
         const int32_t* prow = p.page_table + (long long)b * p.pt_stride;
         for (int cb = c0; cb < c1 && ok; cb += 32) {

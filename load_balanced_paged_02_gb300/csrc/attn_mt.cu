@@ -50,7 +50,7 @@ struct MtLayout {
     static constexpr int kNCW = NG * kWPG;
     static constexpr int kOwners = NG * TS;  // partial states per (new token, head)
     static constexpr int kQCap = NTW * QS;   // new tokens per descriptor
-    static constexpr int kQSlot = kQCap * kQRowsBytes;
+    static constexpr int kQSlot = kQCap * kGroup * (int)kQPitchBf16;  // rows at the padded pitch
     static constexpr size_t kQ = (size_t)STAGES * KvCfg<FP8>::kStageBytes;
     static constexpr size_t kScratch = kQ + 2 * (size_t)kQSlot;
     static constexpr size_t kML = kScratch + (size_t)kQCap * kGroup * kScratchStride * 4;
@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
 #pragma unroll
         for (int t = 0; t < NTW; ++t) {
             if (t < ntl) {
-                load_q_frags<FP8, false>(smem_u32(qbuf + qs * LY::kQSlot + (j0 + t) * kQRowsBytes), lane, qf[t]);
+                load_q_frags<FP8, false, kQPitchBf16>(
+                    smem_u32(qbuf + qs * LY::kQSlot + (j0 + t) * kGroup * kQPitchBf16), lane, qf[t]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) qf[t][i][0] = qf[t][i][1] = 0u;
