@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--no-multi-token", action="store_true", help="skip the q_len > 1 timings")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the plan -> prologue -> attention -> combine layer timing")
+    ap.add_argument("--num-ctas", type=int, default=0,
+                    help="CTAs the task map is planned for (0: the workload's stated count, else one "
+                         "wave of the deep attention instance)")
     ap.add_argument("--engine", choices=["auto", "mma_sync", "tcgen05"], default="auto",
                     help="attention kernel for workloads with several new tokens per request "
                          "(<workload>:qlen<N>); auto = the library's own choice")
@@ -507,7 +510,9 @@ def run_ours(args):
     w = rank_workload(wl.by_name(args.workload), rank)
     case = wl.make_case(w, device=dev)
     kvd = hb.kv_dtype_of(case["k_cache"])
-    C = hb.default_num_ctas(kvd)
+    # the CTA count a workload states (tiny: 16, uniform: 148), else one wave of the
+    # deep attention instance; --num-ctas overrides both
+    C = args.num_ctas if args.num_ctas > 0 else (w.num_ctas or hb.default_num_ctas(kvd))
     eng = {"auto": None, "mma_sync": hb.ENGINE_MMA_SYNC, "tcgen05": hb.ENGINE_TCGEN05}[args.engine]
     if w.q_len == 1:
         eng = None  # one new token: hpc_decode_attn's kernel

@@ -137,7 +137,10 @@ size_t hpc_decode_split_capacity(int batch, int num_kv_heads, int num_ctas);
 
 /* Persistent CTA count for the attention kernel on the current device:
  * SM count x resident CTAs per SM of the kernel instance for `kv_dtype`.
- * Returns 0 if the device cannot be queried. */
+ * Returns 0 if the device cannot be queried. A plan for more CTAs than this
+ * runs a shallower instance that keeps two CTAs per SM resident (up to twice
+ * this count in one wave): finer buckets for batches of many short requests,
+ * at the price of more partials for long ones. */
 int hpc_decode_default_num_ctas(int kv_dtype);
 
 /*

@@ -468,8 +468,9 @@ struct Inst {
 using BalancedBf16 = Inst<false, false, 4, 2>;
 using BalancedFp8 = Inst<true, false, 8, 2>;
 using BalancedFp8Q = Inst<true, true, 8, 2>;
-// Static split-KV instances: one descriptor per CTA, shallow rings so that
-// several CTAs share an SM, as a non-persistent split-KV grid would.
+// Shallow instances: static split-KV maps (one descriptor per CTA, several
+// CTAs per SM, as a non-persistent split-KV grid would) and balanced maps
+// planned for more CTAs than the deep instance keeps resident.
 using StaticBf16 = Inst<false, false, 2, 1>;
 using StaticFp8 = Inst<true, false, 4, 1>;
 using StaticFp8Q = Inst<true, true, 4, 1>;
@@ -518,7 +519,17 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
     p.early_kv = a.early_kv;
     p.max_tasks = (int)L.max_tasks;
-    const bool stat = a.mode == 1;
+    // A static map, or a balanced map planned for more CTAs than the deep
+    // instance keeps resident (SMs x its CTAs per SM), runs the shallow
+    // instance, which holds two CTAs per SM: a caller can plan a batch of many
+    // short requests over 2 x SMs CTAs without a second wave of CTAs.
+    static std::atomic<int> deep_cap[2] = {{0}, {0}};
+    int cap = deep_cap[a.fp8 ? 1 : 0].load(std::memory_order_relaxed);
+    if (cap == 0) {
+        cap = attn_default_ctas(a.fp8);
+        deep_cap[a.fp8 ? 1 : 0].store(cap, std::memory_order_relaxed);
+    }
+    const bool stat = a.mode == 1 || (cap > 0 && a.num_ctas > cap);
     if (a.fp8 && a.q_scale)
         return stat ? StaticFp8Q::launch(maps, p, a.num_ctas, s) : BalancedFp8Q::launch(maps, p, a.num_ctas, s);
     if (a.fp8)
