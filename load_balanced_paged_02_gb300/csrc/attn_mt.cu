@@ -53,8 +53,15 @@ struct MtLayout {
     static constexpr int kQSlot = kQCap * kGroup * (int)kQPitchBf16;  // rows at the padded pitch
     static constexpr size_t kQ = (size_t)STAGES * KvCfg<FP8>::kStageBytes;
     static constexpr size_t kScratch = kQ + 2 * (size_t)kQSlot;
-    static constexpr size_t kML = kScratch + (size_t)kQCap * kGroup * kScratchStride * 4;
-    static constexpr size_t kMeta = kML + (size_t)kOwners * kQCap * kGroup * 8;
+    // Merge scratch: one accumulator row set (owners add in turn), or, where
+    // shared memory allows, one row set per owner (every owner writes at once
+    // and all warps merge after one barrier).
+    static constexpr size_t kScratchOne = (size_t)kQCap * kGroup * kScratchStride * 4;
+    static constexpr size_t kMLBytes = (size_t)kOwners * kQCap * kGroup * 8;
+    static constexpr size_t kTail = STAGES * 4 + (size_t)kNCW * 4 + 8 + (2 * STAGES + 5) * 8 + 16 + 1024;
+    static constexpr bool kParMerge = kScratch + kOwners * kScratchOne + kMLBytes + kTail <= 232448;
+    static constexpr size_t kML = kScratch + (kParMerge ? kOwners : 1) * kScratchOne;
+    static constexpr size_t kMeta = kML + kMLBytes;
     static constexpr size_t kSink = kMeta + STAGES * 4;
     static constexpr size_t kBars = (kSink + kNCW * 4 + 7) / 8 * 8;
     static constexpr int kNumBars = 2 * STAGES + 5;
@@ -321,70 +328,35 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
                 if (lane == 0) mbar_arrive(&empty[st]);
             }
 
-            // ---- phase 1: publish (m, l) of each (owner, new token, head)
+            if constexpr (LY::kParMerge) {
+                // ---- every owner writes its (m, l) and its unnormalised rows at once
 #pragma unroll
-            for (int t = 0; t < NTW; ++t) {
-                if (t >= ntl) continue;
+                for (int t = 0; t < NTW; ++t) {
+                    if (t >= ntl) continue;
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    l[t][0] += __shfl_xor_sync(0xffffffffu, l[t][0], off);
-                    l[t][1] += __shfl_xor_sync(0xffffffffu, l[t][1], off);
-                }
-                if (g == 0) {
-                    float2* dst = ml + (own * QCAP + j0 + t) * kGroup + 2 * c;
-                    dst[0] = make_float2(m[t][0], l[t][0]);
-                    dst[1] = make_float2(m[t][1], l[t][1]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(merge_bar);
-            if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
-            ++mphase;
-
-            // ---- phase 2: owner k adds its rescaled outputs, k = 0 .. OWN-1
-            for (int k = 0; k < OWN; ++k) {
-                if (own == k) {
+                    for (int off = 4; off < 32; off <<= 1) {
+                        l[t][0] += __shfl_xor_sync(0xffffffffu, l[t][0], off);
+                        l[t][1] += __shfl_xor_sync(0xffffffffu, l[t][1], off);
+                    }
+                    if (g == 0) {
+                        float2* dst = ml + (own * QCAP + j0 + t) * kGroup + 2 * c;
+                        dst[0] = make_float2(m[t][0], l[t][0]);
+                        dst[1] = make_float2(m[t][1], l[t][1]);
+                    }
+                    float* r0 = scratch + ((own * QCAP + j0 + t) * kGroup + 2 * c) * kScratchStride;
+                    float* r1 = r0 + kScratchStride;
 #pragma unroll
-                    for (int t = 0; t < NTW; ++t) {
-                        if (t >= ntl) continue;
-                        const int j = j0 + t;
-                        float f[2];
-#pragma unroll
-                        for (int col = 0; col < 2; ++col) {
-                            float M = kNegInf;
-#pragma unroll
-                            for (int gg = 0; gg < OWN; ++gg) M = fmaxf(M, ml[(gg * QCAP + j) * kGroup + 2 * c + col].x);
-                            f[col] = m[t][col] == kNegInf ? 0.f : fast_exp2(m[t][col] - M);
-                        }
-                        float* r0 = scratch + (j * kGroup + 2 * c) * kScratchStride;
-                        float* r1 = r0 + kScratchStride;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            int d00, d01, d10, d11;  // dims of o[t][i][0..3]
-                            if constexpr (FP8) {
-                                d00 = 16 * g + 2 * i;  // regs 0, 1: dim d; regs 2, 3: dim d + 1
-                                d01 = d00;
-                                d10 = d00 + 1;
-                                d11 = d00 + 1;
-                            } else {
-                                d00 = 16 * i + g;  // regs 0, 1: dim d; regs 2, 3: dim d + 8
-                                d01 = d00;
-                                d10 = d00 + 8;
-                                d11 = d00 + 8;
-                            }
-                            const float a0 = o[t][i][0] * f[0], a1 = o[t][i][1] * f[1];
-                            const float a2 = o[t][i][2] * f[0], a3 = o[t][i][3] * f[1];
-                            if (k == 0) {
-                                r0[d00] = a0;
-                                r1[d01] = a1;
-                                r0[d10] = a2;
-                                r1[d11] = a3;
-                            } else {
-                                r0[d00] += a0;
-                                r1[d01] += a1;
-                                r0[d10] += a2;
-                                r1[d11] += a3;
-                            }
+                    for (int i = 0; i < 8; ++i) {
+                        if constexpr (FP8) {
+                            const int d = 16 * g + 2 * i;  // regs 0, 1: dim d; regs 2, 3: dim d + 1
+                            *reinterpret_cast<float2*>(r0 + d) = make_float2(o[t][i][0], o[t][i][2]);
+                            *reinterpret_cast<float2*>(r1 + d) = make_float2(o[t][i][1], o[t][i][3]);
+                        } else {
+                            const int d = 16 * i + g;  // regs 0, 1: dim d; regs 2, 3: dim d + 8
+                            r0[d] = o[t][i][0];
+                            r1[d] = o[t][i][1];
+                            r0[d + 8] = o[t][i][2];
+                            r1[d + 8] = o[t][i][3];
                         }
                     }
                 }
@@ -392,9 +364,113 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
                 if (lane == 0) mbar_arrive(merge_bar);
                 if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
                 ++mphase;
+            } else {
+                // ---- phase 1: publish (m, l) of each (owner, new token, head)
+#pragma unroll
+                for (int t = 0; t < NTW; ++t) {
+                    if (t >= ntl) continue;
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        l[t][0] += __shfl_xor_sync(0xffffffffu, l[t][0], off);
+                        l[t][1] += __shfl_xor_sync(0xffffffffu, l[t][1], off);
+                    }
+                    if (g == 0) {
+                        float2* dst = ml + (own * QCAP + j0 + t) * kGroup + 2 * c;
+                        dst[0] = make_float2(m[t][0], l[t][0]);
+                        dst[1] = make_float2(m[t][1], l[t][1]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(merge_bar);
+                if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                ++mphase;
+
+                // ---- phase 2: owner k adds its rescaled outputs, k = 0 .. OWN-1
+                for (int k = 0; k < OWN; ++k) {
+                    if (own == k) {
+#pragma unroll
+                        for (int t = 0; t < NTW; ++t) {
+                            if (t >= ntl) continue;
+                            const int j = j0 + t;
+                            float f[2];
+#pragma unroll
+                            for (int col = 0; col < 2; ++col) {
+                                float M = kNegInf;
+#pragma unroll
+                                for (int gg = 0; gg < OWN; ++gg) M = fmaxf(M, ml[(gg * QCAP + j) * kGroup + 2 * c + col].x);
+                                f[col] = m[t][col] == kNegInf ? 0.f : fast_exp2(m[t][col] - M);
+                            }
+                            float* r0 = scratch + (j * kGroup + 2 * c) * kScratchStride;
+                            float* r1 = r0 + kScratchStride;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                int d00, d01, d10, d11;  // dims of o[t][i][0..3]
+                                if constexpr (FP8) {
+                                    d00 = 16 * g + 2 * i;  // regs 0, 1: dim d; regs 2, 3: dim d + 1
+                                    d01 = d00;
+                                    d10 = d00 + 1;
+                                    d11 = d00 + 1;
+                                } else {
+                                    d00 = 16 * i + g;  // regs 0, 1: dim d; regs 2, 3: dim d + 8
+                                    d01 = d00;
+                                    d10 = d00 + 8;
+                                    d11 = d00 + 8;
+                                }
+                                const float a0 = o[t][i][0] * f[0], a1 = o[t][i][1] * f[1];
+                                const float a2 = o[t][i][2] * f[0], a3 = o[t][i][3] * f[1];
+                                if (k == 0) {
+                                    r0[d00] = a0;
+                                    r1[d01] = a1;
+                                    r0[d10] = a2;
+                                    r1[d11] = a3;
+                                } else {
+                                    r0[d00] += a0;
+                                    r1[d01] += a1;
+                                    r0[d10] += a2;
+                                    r1[d11] += a3;
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(merge_bar);
+                    if (!wait_bounded(merge_bar, mphase & 1, abort_flag, kWaitLimitNs)) goto timeout;
+                    ++mphase;
+                }
             }
         }
-        {
+        if constexpr (LY::kParMerge) {
+            // ---- all warps: rows (s * q_len + j) * 8 + head from every owner's state
+            const int ct = warp * 32 + lane;
+            for (int idx = ct; idx < Q * kGroup * 32; idx += NCW * 32) {
+                const int row = idx >> 5, d4 = idx & 31;
+                const int j = row >> 3, qh = row & 7;
+                float M = kNegInf;
+#pragma unroll
+                for (int gg = 0; gg < OWN; ++gg) M = fmaxf(M, ml[(gg * QCAP + j) * kGroup + qh].x);
+                float lsum = 0.f;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (M != kNegInf) {
+#pragma unroll
+                    for (int gg = 0; gg < OWN; ++gg) {
+                        const float2 v = ml[(gg * QCAP + j) * kGroup + qh];
+                        const float f = fast_exp2(v.x - M);
+                        lsum += v.y * f;
+                        const float4 x = *reinterpret_cast<const float4*>(
+                            scratch + ((gg * QCAP + j) * kGroup + qh) * kScratchStride + 4 * d4);
+                        acc.x += f * x.x;
+                        acc.y += f * x.y;
+                        acc.z += f * x.z;
+                        acc.w += f * x.w;
+                    }
+                }
+                const float inv = lsum > 0.f ? 1.f / (lsum * Cfg::kPScale) : 0.f;
+                const long long orow = ((long long)s * Q + j) * kGroup + qh;
+                *reinterpret_cast<float4*>(p.split_o + orow * kHeadDim + 4 * d4) =
+                    make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                if (d4 == 0) p.split_lse[orow] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : kNegInf;
+            }
+        } else {
             // ---- phase 3: normalise and write rows (s * q_len + j) * 8 + head
             const int ct = warp * 32 + lane;
             for (int idx = ct; idx < Q * kGroup * 32; idx += NCW * 32) {
