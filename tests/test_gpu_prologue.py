@@ -139,6 +139,35 @@ def test_many_rows_path_matches_oracle():
     check_e4m3_rows(vc, vsc, rv, "v")
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_large_call_instance_matches_oracle(fp8):
+    """A call of at least four waves of blocks (2600 tokens x 80 rows) runs the
+    prologue's 64-register instance (four blocks per SM)."""
+    T = 2600
+    rng = np.random.default_rng(12)
+    pos = rng.integers(0, 4000, size=T).astype(np.int32)
+    pc = wl.make_prologue_case(pos, 64, 8, seed=12, device=DEV, max_pos=4096,
+                               slots=np.arange(T, dtype=np.int32))
+    pages = (T + 63) // 64
+    q, qs, k, v, ks, vs = run_prologue(pc, fp8, fp8, num_pages=pages)
+    rq, rk, rv = _oracle(pc)
+    if fp8:
+        check_e4m3_rows(q.view(torch.uint8).cpu().numpy(), qs.cpu().numpy(), rq, "q")
+        kc = k.view(torch.uint8).cpu().numpy().reshape(pages * 64, 8, 128)[:T]
+        ksc = ks.cpu().numpy().transpose(0, 2, 1).reshape(pages * 64, 8)[:T]
+        check_e4m3_rows(kc, ksc, rk, "k")
+        vc = v.view(torch.uint8).cpu().numpy().reshape(pages * 64, 8, 128)[:T]
+        vsc = vs.cpu().numpy().transpose(0, 2, 1).reshape(pages * 64, 8)[:T]
+        check_e4m3_rows(vc, vsc, rv, "v")
+    else:
+        tol = lambda r: 2.0 ** -8 * np.abs(r) + 2e-5  # noqa: E731
+        assert np.all(np.abs(q.float().cpu().numpy() - rq) <= tol(rq))
+        kc = k.float().cpu().numpy().reshape(pages * 64, 8, 128)[:T]
+        vc = v.float().cpu().numpy().reshape(pages * 64, 8, 128)[:T]
+        assert np.all(np.abs(kc - rk) <= tol(rk))
+        assert np.array_equal(vc, rv.astype(np.float32))
+
+
 def test_bad_position_sets_error_bit():
     pc = wl.make_prologue_case([3, 9000, 5], 8, 1, seed=3, device=DEV, max_pos=16)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
