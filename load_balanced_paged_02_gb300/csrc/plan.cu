@@ -21,31 +21,54 @@ constexpr int kPlanWarps = kPlanThreads / 32;
 
 // Exclusive scan of one value per thread across the block. All threads must
 // call it. Returns the exclusive prefix; *total receives the block sum.
-__device__ long long block_exclusive_scan(long long v, long long* total, long long* warp_sums) {
+template <typename V>
+__device__ V block_exclusive_scan(V v, V* total, V* warp_sums) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    long long x = v;
+    V x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        V y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
     if (lane == 31) warp_sums[wid] = x;
     __syncthreads();
     if (wid == 0) {
-        long long w = warp_sums[lane];
+        V w = warp_sums[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            long long y = __shfl_up_sync(0xffffffffu, w, o);
+            V y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o) w += y;
         }
         warp_sums[lane] = w;
     }
     __syncthreads();
-    long long prefix = (wid > 0 ? warp_sums[wid - 1] : 0) + x - v;
+    V prefix = (wid > 0 ? warp_sums[wid - 1] : 0) + x - v;
     *total = warp_sums[kPlanWarps - 1];
     __syncthreads();
     return prefix;
 }
+
+// Division of 32-bit unsigned integers by a divisor fixed for the launch, as a
+// multiply and shifts (T. Granlund and P. L. Montgomery, "Division by invariant
+// integers using multiplication", PLDI 1994, section 4): with l = ceil(log2 d)
+// and m = floor(2^32 (2^l - d) / d) + 1, the quotient is
+// (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0), t = high half of m * n, for
+// 1 <= d < 2^32 and every 32-bit n. The planner is one block and issue bound,
+// and the per-pair divisions by the bucket and the batch were most of its work.
+struct FastDiv {
+    uint32_t m;
+    int s1, s2;
+    __device__ __forceinline__ explicit FastDiv(uint32_t d) {
+        const int l = 32 - __clz((int)(d - 1u));  // ceil(log2 d); 0 for d = 1
+        m = (uint32_t)(((((uint64_t)1 << l) - d) << 32) / d + 1);
+        s1 = l < 1 ? l : 1;
+        s2 = l > 0 ? l - 1 : 0;
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const {
+        const uint32_t t = __umulhi(m, n);
+        return (t + ((n - t) >> s1)) >> s2;
+    }
+};
 
 __device__ __forceinline__ void write_row(int32_t* row, int a, int b, int c, int d, int e, int f,
                                           int g) {
@@ -76,7 +99,7 @@ __device__ long long chunk_prefix(const int32_t* __restrict__ seq_lens, int B, i
             n = (L + kChunk - 1) / kChunk;
         }
         long long tot;
-        long long ex = block_exclusive_scan(n, &tot, warp_sums);
+        long long ex = block_exclusive_scan<long long>(n, &tot, warp_sums);
         if (b < B) pre[b] = (int32_t)(running + ex);
         running += tot;
     }
@@ -117,6 +140,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
                          int32_t* __restrict__ buf) {
     extern __shared__ int32_t pre[];  // [B + 1]
     __shared__ long long warp_sums[32];
+    __shared__ unsigned warp_sums32[32];
     __shared__ int s_err;
     const int tid = threadIdx.x;
     if (tid == 0) s_err = 0;
@@ -138,60 +162,64 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     const long long used = T ? (T + bucket - 1) / bucket : 0;
     const long long P = (long long)Hkv * B;
 
-    // Chunk indices stay below T <= INT32_MAX (checked in chunk_prefix), so the
-    // per-pair divisions run in 32 bits; products that can pass 2^31 stay 64-bit.
-    const unsigned ubucket = (unsigned)bucket;
-    const unsigned uB = (unsigned)B;
+    // Chunk indices stay below T <= INT32_MAX (checked in chunk_prefix), and so do
+    // split and task-row indices (P + 2C rows), so the per-pair work runs in 32-bit
+    // unsigned arithmetic: the planner is one block and bound by instruction issue.
+    // A CTA range ends below T + bucket < 2^32.
+    const unsigned ubucket = (unsigned)bucket, uB = (unsigned)B, uN = (unsigned)N, uT = (unsigned)T;
+    const FastDiv by_bucket(ubucket), by_batch(uB);
+    const int Pi = (int)P;  // P <= HPC_MAX_CTAS
 
     // split count of every (kv head, request) pair, then its first split index
-    long long running = 0;
-    for (long long base = 0; base < P; base += kPlanThreads) {
-        const long long p = base + tid;
-        long long ns = 0;
-        if (p < P) {
-            const unsigned up = (unsigned)p;
-            const unsigned h = up / uB, b = up - h * uB;
+    unsigned running = 0;
+    for (int base = 0; base < Pi; base += kPlanThreads) {
+        const int p = base + tid;
+        unsigned ns = 0;
+        if (p < Pi) {
+            const unsigned h = by_batch.div((unsigned)p), b = (unsigned)p - h * uB;
             const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
-            const unsigned g0 = h * (unsigned)N + (unsigned)pre[b];
-            ns = nb ? (long long)((g0 + nb - 1) / ubucket - g0 / ubucket + 1) : 0;
+            const unsigned g0 = h * uN + (unsigned)pre[b];
+            ns = nb ? by_bucket.div(g0 + nb - 1) - by_bucket.div(g0) + 1 : 0;
         }
-        long long tot;
-        long long ex = block_exclusive_scan(ns, &tot, warp_sums);
-        if (p < P) {
+        unsigned tot;
+        const unsigned ex = block_exclusive_scan<unsigned>(ns, &tot, warp_sums32);
+        if (p < Pi) {
             nsplit[p] = (int32_t)ns;
             split0[p] = (int32_t)(running + ex);
         }
         running += tot;
     }
     const long long total = running;
-    __syncthreads();
 
-    // descriptors, and the first task row of every used CTA
-    for (long long p = tid; p < P; p += kPlanThreads) {
-        const unsigned up = (unsigned)p;
-        const int h = (int)(up / uB), b = (int)(up - (unsigned)h * uB);
-        const long long nb = pre[b + 1] - pre[b];
+    // Descriptors, by the thread that scanned the pair (its split0 write is its own).
+    // Descriptor k of a pair lies in CTA first + k; the one that reaches the end of
+    // its CTA's range [cta*bucket, min((cta+1)*bucket, T)) is the CTA's last, and the
+    // CTA's terminator row follows it.
+    for (int p = tid; p < Pi; p += kPlanThreads) {
+        const unsigned h = by_batch.div((unsigned)p), b = (unsigned)p - h * uB;
+        const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
         if (!nb) continue;
-        const long long g0 = (long long)h * N + pre[b];
-        const long long first = (unsigned)g0 / ubucket;
-        const int ns = nsplit[p];
-        const long long s0 = split0[p];
-        for (int k = 0; k < ns; ++k) {
-            const long long cta = first + k;
-            const long long lo = cta * bucket, hi = lo + bucket;
-            const long long cs = g0 > lo ? g0 : lo;
-            const long long ce = (g0 + nb) < hi ? (g0 + nb) : hi;
-            const long long s = s0 + k;
-            const long long slot = s + cta;
-            write_row(tasks + slot * kTaskInts, h, b, (int)(cs - g0), (int)(ce - g0), (int)s, k, ns);
+        const unsigned g0 = h * uN + (unsigned)pre[b], end = g0 + nb;
+        const unsigned first = by_bucket.div(g0);
+        const unsigned ns = by_bucket.div(end - 1) - first + 1;
+        const unsigned s0 = (unsigned)split0[p];
+        for (unsigned k = 0; k < ns; ++k) {
+            const unsigned cta = first + k;
+            const unsigned lo = cta * ubucket, hi = lo + ubucket;
+            const unsigned cs = g0 > lo ? g0 : lo;
+            const unsigned ce = end < hi ? end : hi;
+            const unsigned s = s0 + k, slot = s + cta;
+            int32_t* row = tasks + (size_t)slot * kTaskInts;
+            write_row(row, (int)h, (int)b, (int)(cs - g0), (int)(ce - g0), (int)s, (int)k, (int)ns);
             if (cs == lo) cta_off[cta] = (int32_t)slot;
+            if (ce == hi || ce == uT) write_term(row + kTaskInts);
         }
     }
+
+    // unused CTAs: an empty task list each, then terminators up to the row capacity
     for (long long j = used + tid; j <= C; j += kPlanThreads) cta_off[j] = (int32_t)(total + j);
     for (long long i = L.cta_off + C + 1 + tid; i < L.tasks; i += kPlanThreads) buf[i] = 0;
-    __syncthreads();
-    for (long long j = tid; j < C; j += kPlanThreads) write_term(tasks + (cta_off[j + 1] - 1) * kTaskInts);
-    for (long long r = total + C + tid; r < L.max_tasks; r += kPlanThreads) write_term(tasks + r * kTaskInts);
+    for (long long r = total + used + tid; r < L.max_tasks; r += kPlanThreads) write_term(tasks + r * kTaskInts);
     if (tid == 0)
         write_header(buf, T, bucket, used, total, C, B, Hkv, m, L.max_tasks, 0, N, s_err);
 }
@@ -217,6 +245,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 
     const long long N = chunk_prefix(seq_lens, B, Hkv, pre, warp_sums, &s_err);
     const long long P = (long long)Hkv * B;
+    const FastDiv by_batch((unsigned)B);
 
     // non-empty splits of a pair: s*q < n_b  <=>  s < ceil(n_b / q), q = ceil(n_b / S)
     long long running = 0;
@@ -224,7 +253,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
         const long long p = base + tid;
         long long ns = 0;
         if (p < P) {
-            const unsigned b = (unsigned)p % (unsigned)B;
+            const unsigned b = (unsigned)p - by_batch.div((unsigned)p) * (unsigned)B;
             const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
             const unsigned q = (nb + (unsigned)S - 1) / (unsigned)S;
             ns = q ? (long long)((nb + q - 1) / q) : 0;
@@ -241,11 +270,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
     __syncthreads();
 
     const unsigned uS = (unsigned)S, uB = (unsigned)B;
+    const FastDiv by_splits(uS);
     for (long long j = tid; j < C; j += kPlanThreads) {
         const unsigned uj = (unsigned)j;  // C <= HPC_MAX_CTAS < 2^31
-        const unsigned up = uj / uS;
+        const unsigned up = by_splits.div(uj);
         const int s = (int)(uj - up * uS);
-        const int h = (int)(up / uB), b = (int)(up - (unsigned)h * uB);
+        const int h = (int)by_batch.div(up), b = (int)(up - (unsigned)h * uB);
         const long long p = up;
         const long long nb = pre[b + 1] - pre[b];
         const long long q = ((unsigned)nb + uS - 1) / uS;

@@ -56,6 +56,11 @@ def test_plan_bit_exact_random_and_edges():
         B = int(rng.integers(1, 60))
         cases.append((rng.integers(0, 6000, size=B).tolist(), int(rng.integers(1, 9)),
                       int(rng.integers(1, 400)), int(rng.integers(0, 6))))
+    # batch sizes and buckets at and next to powers of two: the planner divides by
+    # both with a precomputed multiplier, whose shifts change at those points
+    for B in (2, 3, 4, 5, 127, 128, 129, 1023, 1024, 1025):
+        for C, m in ((1, 0), (B, 0), (3 * B + 1, 1), (256, 4)):
+            cases.append((rng.integers(0, 5000, size=B).tolist(), int(rng.integers(1, 9)), C, m))
     # more than 1024 requests / pairs: several scan tiles in the planner
     cases.append((rng.integers(0, 3000, size=3000).tolist(), 8, 304, 2))
     cases.append((rng.integers(0, 300, size=HB_MAX_B).tolist(), 1, 1000, 1))
