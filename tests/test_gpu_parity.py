@@ -156,20 +156,23 @@ def test_static_split_full(dtype):
     _gpu.check_full(case, res)
 
 
-@pytest.mark.parametrize("dtype,q_len", [("bf16", 1), ("fp8", 1), ("bf16", 3)])
-def test_many_short_requests_full(dtype, q_len):
+@pytest.mark.parametrize("dtype,q_len,B,hkv", [
+    ("bf16", 1, 400, 8), ("fp8", 1, 400, 8), ("bf16", 3, 140, 8),
+    # more than two waves of the pair form; an odd q_len, whose consecutive
+    # units change pair mid-warp-block; one KV head and an odd unit count
+    ("bf16", 1, 700, 8), ("fp8", 1, 700, 8), ("bf16", 5, 130, 8), ("bf16", 1, 4865, 1)])
+def test_many_short_requests_full(dtype, q_len, B, hkv):
     """Enough (KV-head pair, new token) tasks that the combine takes its
     one-warp-per-pair form (at least two blocks of 8 warps per SM on 152 SMs),
     with empty, one-chunk and multi-split pairs among them; every row and
     every split partial against the oracle."""
-    rng = np.random.default_rng(80 + q_len)
-    B = 400 if q_len == 1 else 140
+    rng = np.random.default_rng(80 + q_len + B)
     lens = rng.integers(0, 300, size=B)
     lens[::37] = 0
     lens[5] = 20000  # one request long enough to leave a multi-split pair
-    w = wl.Workload("t", B, 64, 8, dtype, 81, lens=[int(x) for x in lens], q_len=q_len)
+    w = wl.Workload("t", B, 8 * hkv, hkv, dtype, 81, lens=[int(x) for x in lens], q_len=q_len)
     case = wl.make_case(w, device=DEV)
-    assert 8 * B * q_len >= 152 * 2 * 8
+    assert hkv * B * q_len >= 152 * 2 * 8
     res = _gpu.run(case, num_ctas=152, min_chunks=2)
     _gpu.check_plan_exact(res, case, min_chunks=2)
     _gpu.check_full(case, res)
