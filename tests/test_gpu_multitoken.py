@@ -55,6 +55,16 @@ def test_ragged_full(dtype, engine, q_len):
 
 
 @pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
+def test_max_kv_heads(dtype, engine):
+    """256 KV heads (the library's limit), 2048 query heads, three new tokens."""
+    case = case_for([1, 100, 700, 0, 64], 3, hkv=256, dtype=dtype, seed=93)
+    res = _gpu.run(case, num_ctas=152, min_chunks=2, engine=engine)
+    _gpu.check_plan_exact(res, case, min_chunks=2)
+    _gpu.check_full(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
+
+
+@pytest.mark.parametrize("dtype,engine", ENGINES, ids=ENGINE_IDS)
 @pytest.mark.parametrize("C,m", [(1, 0), (7, 1), (300, 4)])
 def test_cta_budgets(dtype, engine, C, m):
     case = case_for(RAGGED, 6, hkv=1, dtype=dtype, seed=50 + C)

@@ -179,6 +179,35 @@ def test_many_short_requests_full(dtype, q_len, B, hkv):
     assert hb.hpc_decode_read_error(res["plan"]) == 0
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_max_batch_full(dtype):
+    """HPC_MAX_BATCH requests (short, ragged, every eleventh empty, one long)
+    with one KV head: several scan tiles in the planner, ~15K descriptors over
+    152 CTAs and the pair-form combine; every row and every split partial."""
+    rng = np.random.default_rng(90)
+    B = HB_MAX_B
+    lens = rng.integers(0, 200, size=B)
+    lens[::11] = 0
+    lens[7] = 9000
+    w = wl.Workload("t", B, 8, 1, dtype, 91, lens=[int(x) for x in lens])
+    case = wl.make_case(w, device=DEV)
+    res = _gpu.run(case, num_ctas=152, min_chunks=2)
+    _gpu.check_plan_exact(res, case, min_chunks=2)
+    _gpu.check_full(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
+
+
+@pytest.mark.parametrize("dtype,q_dtype", [("bf16", "bf16"), ("fp8", "bf16"), ("fp8", "fp8")])
+def test_max_kv_heads_full(dtype, q_dtype):
+    """HPC_MAX_KV_HEADS (256) KV heads, 2048 query heads: the KV tensor maps'
+    head dimension and row stride at their largest, every row and split."""
+    case = case_for([1, 100, 700, 0, 64], 256, dtype, seed=92, q_dtype=q_dtype)
+    res = _gpu.run(case, num_ctas=152, min_chunks=2)
+    _gpu.check_plan_exact(res, case, min_chunks=2)
+    _gpu.check_full(case, res)
+    assert hb.hpc_decode_read_error(res["plan"]) == 0
+
+
 def test_all_lengths_zero():
     case = case_for([0, 0, 0], 1, seed=6, pool=4)
     res = _gpu.run(case, num_ctas=8)
