@@ -7,14 +7,17 @@
 // per token and head). One pass over the QKV output; no intermediate tensors.
 //
 // One block per token. A half-warp owns one (token, head) row, lane k of the
-// half owning dims [8k, 8k+8) (16-byte loads and stores); a warp covers two
-// rows per round and the block's 8 warps cover 16 rows per round; the five
-// rounds of a Hy3 token (80 rows) are all loaded before any is processed, so
-// a block waits on memory once. The token's position, slot and rotary row are
-// loaded once per block, the norm weights per row from L1. Reductions (norm sum, e4m3
-// absolute max) take four xor-shuffle steps inside the half-warp, and the
-// rotation partner of dim d (d +- 64) lives in lane ^ 8. Row kinds (query,
-// key, value) are per-lane predicates, so all lanes run every shuffle.
+// half owning dims [4k, 4k+4) and their rotation partners [64+4k, 64+4k+4)
+// (two 8-byte loads and stores, each half-warp-wide access 128 contiguous
+// bytes), so the rotary embedding needs no data from other lanes; a warp
+// covers two rows per round and the block's 8 warps cover 16 rows per round;
+// the five rounds of a Hy3 token (80 rows) are all loaded before any is
+// processed, so a block waits on memory once. The token's position, slot and
+// rotary row are loaded once per block, the norm weights per row from L1. The
+// reductions (norm sum; e4m3 absolute max, only when a call writes e4m3) take
+// four xor-shuffle steps inside the half-warp. Row kinds (query, key, value)
+// are per-lane predicates, so all lanes run every shuffle. The kernel is bound
+// by instruction issue for prefill-sized calls, so per-row work is kept small.
 #include "hpc_internal.cuh"
 
 namespace hpc {
@@ -59,6 +62,13 @@ __device__ __forceinline__ float half_max(float v) {
     return v;
 }
 
+// Dims [4k, 4k+4) and [64+4k, 64+4k+4) of a row that starts at `row` + 4k.
+__device__ __forceinline__ uint4 load_pair(const __nv_bfloat16* row) {
+    const uint2 a = *reinterpret_cast<const uint2*>(row);
+    const uint2 b = *reinterpret_cast<const uint2*>(row + 64);
+    return make_uint4(a.x, a.y, b.x, b.y);
+}
+
 __device__ __forceinline__ void unpack8(const uint4& r, float (&y)[8]) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -82,7 +92,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
     const int H3 = p.Hq + 2 * p.Hkv;
     const int t = blockIdx.x;
     // the first rounds' rows load first: they do not depend on the position
-    const __nv_bfloat16* src = p.qkv + (size_t)t * H3 * kHeadDim + 8 * hl;
+    const __nv_bfloat16* src = p.qkv + (size_t)t * H3 * kHeadDim + 4 * hl;
     const int all_rounds = (H3 + kRowsPerRound - 1) / kRowsPerRound;
     const int first = blockIdx.y * p.rounds_per_block;
     const int rounds = min(all_rounds, first + p.rounds_per_block);
@@ -91,7 +101,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
     for (int r = 0; r < kMaxRounds; ++r) {
         const int j = (first + r) * kRowsPerRound + 2 * warp + half;
         raw[r] = make_uint4(0u, 0u, 0u, 0u);
-        if (first + r < rounds && j < H3) raw[r] = *reinterpret_cast<const uint4*>(src + (size_t)j * kHeadDim);
+        if (first + r < rounds && j < H3) raw[r] = load_pair(src + (size_t)j * kHeadDim);
     }
     const int pos = p.pos[t];
     const int slot = p.slots[t];
@@ -101,32 +111,30 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
         if (!rotate) atomicOr(p.err, (int)HPC_DEVERR_BAD_POSITION);
         if (slot >= 0 && !slot_ok) atomicOr(p.err, (int)HPC_DEVERR_PAGE_OUT_OF_RANGE);
     }
-    // per-lane constants: rotation cos/sin for dims [8*hl, 8*hl+8) (the norm
-    // weights are read per row from L1, which keeps the registers for the rows
-    // in flight)
-    float c[8], sn[8];
+    // per-lane constants: rotation cos/sin of pair indices [4*hl, 4*hl+4) (the
+    // norm weights are read per row from L1, which keeps the registers for the
+    // rows in flight); cos 1, sin 0 without a valid position
+    float c[4], sn[4];
     {
-        const int i0 = (8 * hl) & 63;
-        const float* cs = p.cos_sin + (long long)(rotate ? pos : 0) * kHeadDim;
-        const float4 c0 = *reinterpret_cast<const float4*>(cs + i0), c1 = *reinterpret_cast<const float4*>(cs + i0 + 4);
-        const float4 s0 = *reinterpret_cast<const float4*>(cs + 64 + i0);
-        const float4 s1 = *reinterpret_cast<const float4*>(cs + 64 + i0 + 4);
-        const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-        const float sign = hl < 8 ? -1.f : 1.f;  // first half of the dims: x_i c - x_{i+64} s
+        const float* cs = p.cos_sin + (long long)(rotate ? pos : 0) * kHeadDim + 4 * hl;
+        const float4 c0 = *reinterpret_cast<const float4*>(cs);
+        const float4 s0 = *reinterpret_cast<const float4*>(cs + 64);
+        const float cc[4] = {c0.x, c0.y, c0.z, c0.w};
+        const float ss[4] = {s0.x, s0.y, s0.z, s0.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
             c[k] = rotate ? cc[k] : 1.f;
-            sn[k] = rotate ? sign * ss[k] : 0.f;
+            sn[k] = rotate ? ss[k] : 0.f;
         }
     }
+    const bool any_fp8 = p.q_scale != nullptr || p.kv_fp8 != 0;  // uniform over the grid
     for (int r0 = first; r0 < rounds; r0 += kMaxRounds) {
         if (r0 != first) {
 #pragma unroll
             for (int r = 0; r < kMaxRounds; ++r) {
                 const int j = (r0 + r) * kRowsPerRound + 2 * warp + half;
                 raw[r] = make_uint4(0u, 0u, 0u, 0u);
-                if (r0 + r < rounds && j < H3) raw[r] = *reinterpret_cast<const uint4*>(src + (size_t)j * kHeadDim);
+                if (r0 + r < rounds && j < H3) raw[r] = load_pair(src + (size_t)j * kHeadDim);
             }
         }
 #pragma unroll
@@ -144,40 +152,43 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
             s2 = half_sum(s2);
             const float inv = is_qk ? rsqrtf(s2 * (1.f / kHeadDim) + p.eps) : 1.f;
             if (is_qk) {
-                const float* wr = (is_q ? p.qw : p.kw) + 8 * hl;
+                const float* wr = (is_q ? p.qw : p.kw) + 4 * hl;
                 const float4 w0 = __ldg(reinterpret_cast<const float4*>(wr));
-                const float4 w1 = __ldg(reinterpret_cast<const float4*>(wr + 4));
+                const float4 w1 = __ldg(reinterpret_cast<const float4*>(wr + 64));
                 const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
                 for (int k = 0; k < 8; ++k) y[k] *= inv * ww[k];
             }
-            // rotary embedding on pairs (i, i + 64)
-            float pr[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) pr[k] = __shfl_xor_sync(0xffffffffu, y[k], 8);
+            // rotary embedding on pairs (i, i + 64), both in this lane: y[k] and y[k + 4]
             if (is_qk) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) y[k] = y[k] * c[k] + pr[k] * sn[k];
+                for (int k = 0; k < 4; ++k) {
+                    const float a = y[k], b = y[k + 4];
+                    y[k] = a * c[k] + b * -sn[k];
+                    y[k + 4] = b * c[k] + a * sn[k];
+                }
             }
             // output format of this row
             const bool fp8_row = is_q ? (p.q_scale != nullptr) : (p.kv_fp8 != 0);
             float am = 0.f;
+            if (any_fp8) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(y[k]));
-            am = half_max(am);
+                for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(y[k]));
+                am = half_max(am);
+            }
             if (!valid || (!is_q && !slot_ok)) continue;
             size_t dst_elem;
             void* dst;
             float* scale_dst = nullptr;
             if (is_q) {
                 const size_t qrow = (size_t)t * p.Hq + j;
-                dst_elem = qrow * kHeadDim + 8 * hl;
+                dst_elem = qrow * kHeadDim + 4 * hl;
                 dst = p.q_out;
                 scale_dst = p.q_scale ? p.q_scale + qrow : nullptr;
             } else {
                 const int h = is_qk ? j - p.Hq : j - p.Hq - p.Hkv;
                 const int page = slot / kChunk, off = slot % kChunk;
-                dst_elem = (((size_t)page * kChunk + off) * p.Hkv + h) * kHeadDim + 8 * hl;
+                dst_elem = (((size_t)page * kChunk + off) * p.Hkv + h) * kHeadDim + 4 * hl;
                 dst = is_qk ? p.k_cache : p.v_cache;
                 if (p.kv_fp8) scale_dst = (is_qk ? p.k_scale : p.v_scale) + ((size_t)page * p.Hkv + h) * kChunk + off;
             }
@@ -205,15 +216,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
                         make_float2(qdiv(y[4 * k + 2]), qdiv(y[4 * k + 3])), __NV_SATFINITE, __NV_E4M3);
                     codes[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
                 }
-                *reinterpret_cast<uint2*>(static_cast<uint8_t*>(dst) + dst_elem) = make_uint2(codes[0], codes[1]);
+                uint8_t* d8 = static_cast<uint8_t*>(dst) + dst_elem;
+                *reinterpret_cast<uint32_t*>(d8) = codes[0];        // dims [4k, 4k+4)
+                *reinterpret_cast<uint32_t*>(d8 + 64) = codes[1];   // dims [64+4k, 64+4k+4)
                 if (hl == 0) *scale_dst = scale;
             } else {
-                uint4 packed;
-                packed.x = pack_bf16x2(y[0], y[1]);
-                packed.y = pack_bf16x2(y[2], y[3]);
-                packed.z = pack_bf16x2(y[4], y[5]);
-                packed.w = pack_bf16x2(y[6], y[7]);
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + dst_elem) = packed;
+                __nv_bfloat16* d16 = static_cast<__nv_bfloat16*>(dst) + dst_elem;
+                *reinterpret_cast<uint2*>(d16) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+                *reinterpret_cast<uint2*>(d16 + 64) = make_uint2(pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
             }
         }
     }
