@@ -80,8 +80,10 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&y)[8]) {
 }
 
 // MINB resident blocks per SM: 3 for decode-size calls (a few blocks, latency
-// bound), 4 for many tokens, where more blocks in flight keep more rows
-// loading (8192 tokens at 64/8 heads: 89.7 -> 81.5 us with bf16 outputs).
+// bound); for many tokens more blocks in flight keep more rows loading: 5 with
+// bf16 outputs (8192 tokens at 64/8 heads: 70.2 -> 66.8 us, at the cost of a
+// 64-byte spill), 4 when an output is e4m3, whose per-row quantisation gains
+// nothing from a fifth block (81.9 -> 82.0 us).
 template <int MINB>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(const PrologueParams p) {
     grid_dependency_wait();  // the QKV projection may still be finishing
@@ -260,8 +262,11 @@ cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s) {
     p.rounds_per_block = (long long)a.num_tokens * rounds < 8LL * 152 ? 1 : rounds;
     const unsigned splits = (unsigned)((rounds + p.rounds_per_block - 1) / p.rounds_per_block);
     const dim3 grid((unsigned)a.num_tokens, splits);
-    if ((long long)a.num_tokens * splits >= 4LL * 152 * 4)
+    if ((long long)a.num_tokens * splits >= 4LL * 152 * 4) {
+        if (!a.q_scale && !a.kv_fp8)
+            return launch_pdl(rope_norm_kernel<5>, grid, dim3(kWarpsPerBlock * 32), 0, s, p);
         return launch_pdl(rope_norm_kernel<4>, grid, dim3(kWarpsPerBlock * 32), 0, s, p);
+    }
     return launch_pdl(rope_norm_kernel<3>, grid, dim3(kWarpsPerBlock * 32), 0, s, p);
 }
 
