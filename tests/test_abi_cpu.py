@@ -189,3 +189,30 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(hb._build, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(hb.HpcError):
         hb.lib()
+
+
+def test_rope_norm_rejects_bad_arguments(L):
+    """Every call here is refused on the host (or has no tokens), so nothing
+    is launched with the fake pointers."""
+    def call(**kw):
+        a = dict(qkv=FAKE, positions=FAKE, cos_sin=FAKE, max_pos=4096, q_weight=FAKE, k_weight=FAKE, eps=1e-6,
+                 slots=FAKE, num_tokens=4, num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64,
+                 q_out=FAKE, q_scale=None, k_cache=FAKE, v_cache=FAKE, k_scale=None, v_scale=None,
+                 kv_dtype=hb.KV_BF16, num_pages=16, err=None)
+        a.update(kw)
+        return L.hpc_rope_norm(a["qkv"], a["positions"], a["cos_sin"], a["max_pos"], a["q_weight"],
+                               a["k_weight"], a["eps"], a["slots"], a["num_tokens"], a["num_q_heads"],
+                               a["num_kv_heads"], a["head_dim"], a["page_size"], a["q_out"], a["q_scale"],
+                               a["k_cache"], a["v_cache"], a["k_scale"], a["v_scale"], a["kv_dtype"],
+                               a["num_pages"], a["err"], None)
+    assert call(head_dim=64) == 2
+    assert call(page_size=32) == 2
+    assert call(kv_dtype=7) == 2
+    for bad in (dict(num_tokens=-1), dict(num_q_heads=0), dict(num_kv_heads=0), dict(num_kv_heads=257),
+                dict(max_pos=0), dict(num_pages=0), dict(eps=float("nan")), dict(eps=-1.0), dict(qkv=None),
+                dict(positions=None), dict(slots=None), dict(k_cache=None), dict(qkv=FAKE_ODD),
+                dict(q_out=FAKE_ODD), dict(kv_dtype=hb.KV_FP8_E4M3), dict(kv_dtype=hb.KV_FP8_E4M3, k_scale=FAKE)):
+        assert call(**bad) == 1, bad
+    # no tokens: valid and nothing to do
+    assert call(num_tokens=0) == 0
+    assert call(num_tokens=0, kv_dtype=hb.KV_FP8_E4M3, k_scale=FAKE, v_scale=FAKE) == 0
