@@ -276,6 +276,7 @@ int hpc_decode_attn_multi_auto_engine(int kv_dtype, int q_len);
 
 /* Flags of hpc_decode_attn_ex. */
 #define HPC_ATTN_EARLY_KV 1  /* gather KV before waiting for the predecessor kernel */
+#define HPC_ATTN_TEST_WAIT_EXPIRY 2  /* failure-path test: make a bounded wait run out */
 
 /*
  * Every attention form in one call: q_scale NULL takes a bf16 query
@@ -302,6 +303,19 @@ int hpc_decode_attn_multi_auto_engine(int kv_dtype, int q_len);
  * tokens' K and V (hpc_rope_norm does). Breaking the contract yields wrong
  * outputs, never an out-of-bounds access: early copies are bounds-checked
  * like the others and every copy lands before the CTA exits.
+ *
+ * HPC_ATTN_TEST_WAIT_EXPIRY exists to test the failure path without a fault
+ * (the pages have no counterpart). Every wait inside the attention kernels is
+ * bounded (2 s); when one runs out, the CTA sets HPC_DEVERR_WAIT_TIMEOUT in
+ * the task map's error word, waits (bounded) for its own copies in flight
+ * and returns, leaving the device usable. With this flag the consumer warps
+ * of every CTA first wait, with a 1 ms limit, on a barrier that nothing
+ * completes, so every CTA takes that path: the call computes no partial
+ * (split_o / split_lse keep their contents) and hpc_decode_read_error then
+ * reports HPC_DEVERR_WAIT_TIMEOUT. Plan again before the next use of the
+ * task map (the planner clears the error word). One new token per request on
+ * the warp-level kernel only (q_len 1, engine AUTO or MMA_SYNC); other forms
+ * return HPC_ERR_UNSUPPORTED.
  */
 hpc_status hpc_decode_attn_ex(const void* q, const float* q_scale, int q_len, const void* k_cache,
                               const void* v_cache, const float* k_scale, const float* v_scale,
@@ -456,9 +470,15 @@ hpc_status hpc_decode_step_graph_destroy(hpc_step_graph* graph);
  *     hpc_decode_split_capacity rows of 4128 bytes (each part rounded up to
  *     256 bytes) must fit in 8 MiB, about 2000 split rows; larger sizes return
  *     HPC_ERR_WORKSPACE_TOO_SMALL before any work is enqueued.
+ *   - Every argument check of hpc_decode_plan, hpc_decode_attn and
+ *     hpc_decode_combine runs before the first launch: a refused call
+ *     enqueues nothing and leaves the array as it was.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept with the ID of the
+ *     context it was found in: after a device reset (or the primary context
+ *     released and created again) the next call looks it up again, so make
+ *     that call outside stream capture too.
  *   - Every call on a device shares the array: calls whose work overlaps on
  *     the GPU (other streams, no ordering between them) race on it. Nothing in
  *     the array needs to start at zero; each call rewrites what it reads.

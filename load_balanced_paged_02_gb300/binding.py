@@ -18,7 +18,8 @@ from . import _build
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 ENGINE_AUTO, ENGINE_MMA_SYNC, ENGINE_TCGEN05 = 0, 1, 2
-ATTN_EARLY_KV = 1  # flag of hpc_decode_attn_ex
+ATTN_EARLY_KV = 1  # flags of hpc_decode_attn_ex
+ATTN_TEST_WAIT_EXPIRY = 2
 HEAD_DIM = 128
 PAGE = 64
 GROUP = 8

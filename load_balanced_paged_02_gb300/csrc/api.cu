@@ -145,6 +145,27 @@ int multi_engine_for(bool fp8, int q_len) {
     return q_len >= 3 ? HPC_ENGINE_TCGEN05 : HPC_ENGINE_MMA_SYNC;
 }
 
+// The checks of an attention call on everything but the task map and the
+// split buffers.
+hpc_status attn_inputs_check(const void* q, const float* q_scale, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale, int kv_dtype, int num_pages,
+                             const int32_t* page_table, int page_table_stride, const int32_t* seq_lens,
+                             int num_q_heads, int num_kv_heads, int head_dim, int page_size) {
+    hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
+    if (st != HPC_OK) return st;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens) return HPC_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return HPC_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return HPC_ERR_INVALID_ARG;
+    if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) return HPC_ERR_INVALID_ARG;
+    if (num_pages < 1 || (long long)num_pages * kChunk > 2147483647LL || page_table_stride < 1)
+        return HPC_ERR_INVALID_ARG;
+    if (fp8 && (long long)num_pages * num_kv_heads > 2147483647LL) return HPC_ERR_INVALID_ARG;
+    if (q_scale && (!fp8 || !aligned(q_scale, 16))) return fp8 ? HPC_ERR_INVALID_ARG : HPC_ERR_UNSUPPORTED;
+    return HPC_OK;
+}
+
 // Shared by hpc_decode_attn (bf16 Q), hpc_decode_attn_q8 (e4m3 Q + scales)
 // and hpc_decode_attn_multi (q_len bf16 query rows per request).
 hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache, const void* v_cache,
@@ -153,24 +174,16 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
                        int num_q_heads, int num_kv_heads, int head_dim, int page_size, const hpc_plan* plan,
                        float* split_o, float* split_lse, void* stream, int q_len = 1,
                        int engine = HPC_ENGINE_AUTO, int flags = 0) {
-    hpc_status st = shape_check(num_q_heads, num_kv_heads, head_dim, page_size);
+    hpc_status st = attn_inputs_check(q, q_scale, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages,
+                                      page_table, page_table_stride, seq_lens, num_q_heads, num_kv_heads,
+                                      head_dim, page_size);
     if (st != HPC_OK) return st;
-    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return HPC_ERR_UNSUPPORTED;
     const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
-    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !split_o || !split_lse)
-        return HPC_ERR_INVALID_ARG;
-    if (fp8 && (!k_scale || !v_scale)) return HPC_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(split_o, 16))
-        return HPC_ERR_INVALID_ARG;
-    if (fp8 && (!aligned(k_scale, 16) || !aligned(v_scale, 16))) return HPC_ERR_INVALID_ARG;
-    if (num_pages < 1 || (long long)num_pages * kChunk > 2147483647LL || page_table_stride < 1)
-        return HPC_ERR_INVALID_ARG;
-    if (fp8 && (long long)num_pages * num_kv_heads > 2147483647LL) return HPC_ERR_INVALID_ARG;
-    if (q_scale && (!fp8 || !aligned(q_scale, 16))) return fp8 ? HPC_ERR_INVALID_ARG : HPC_ERR_UNSUPPORTED;
+    if (!split_o || !split_lse || !aligned(split_o, 16)) return HPC_ERR_INVALID_ARG;
     if ((st = plan_check(plan, batch, num_kv_heads)) != HPC_OK) return st;
     if (q_len < 1 || q_len > HPC_MAX_Q_LEN || (q_len > 1 && q_scale)) return HPC_ERR_INVALID_ARG;
     if (engine < HPC_ENGINE_AUTO || engine > HPC_ENGINE_TCGEN05) return HPC_ERR_INVALID_ARG;
-    if (flags & ~HPC_ATTN_EARLY_KV) return HPC_ERR_INVALID_ARG;
+    if (flags & ~(HPC_ATTN_EARLY_KV | HPC_ATTN_TEST_WAIT_EXPIRY)) return HPC_ERR_INVALID_ARG;
     AttnArgs a;
     a.q = q;
     a.q_scale = q_scale;
@@ -193,8 +206,11 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
     a.split_o = split_o;
     a.split_lse = split_lse;
     a.early_kv = (flags & HPC_ATTN_EARLY_KV) ? 1 : 0;
+    a.test_wait_expiry = (flags & HPC_ATTN_TEST_WAIT_EXPIRY) ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (engine == HPC_ENGINE_AUTO) engine = multi_engine_for(fp8, q_len);
+    // the failure-path test exists in the one-token kernel only
+    if (a.test_wait_expiry && (q_len != 1 || engine == HPC_ENGINE_TCGEN05)) return HPC_ERR_UNSUPPORTED;
     cudaError_t e;
     if (engine == HPC_ENGINE_TCGEN05)
         e = launch_attn_tc(a, q_len, cs);
@@ -205,6 +221,24 @@ hpc_status attn_common(const void* q, const float* q_scale, const void* k_cache,
 }
 
 }  // namespace
+
+// Every host-side check that hpc_decode_plan, hpc_decode_attn and
+// hpc_decode_combine make for one step with one new token per request, except
+// those on the task map and split buffers the caller does not provide.
+hpc_status hpc::step_args_check(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                                const float* v_scale, int kv_dtype, int num_pages, const int32_t* page_table,
+                                int page_table_stride, const int32_t* seq_lens, int batch, int num_q_heads,
+                                int num_kv_heads, int head_dim, int page_size, int num_ctas,
+                                int min_chunks_per_cta, const void* out) {
+    if (min_chunks_per_cta < 0 || !sizes_ok(batch, num_kv_heads, num_ctas)) return HPC_ERR_INVALID_ARG;
+    if ((long long)num_kv_heads * batch > HPC_MAX_CTAS) return HPC_ERR_INVALID_ARG;
+    hpc_status st = attn_inputs_check(q, nullptr, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages,
+                                      page_table, page_table_stride, seq_lens, num_q_heads, num_kv_heads,
+                                      head_dim, page_size);
+    if (st != HPC_OK) return st;
+    if (!out || !aligned(out, 8)) return HPC_ERR_INVALID_ARG;
+    return HPC_OK;
+}
 
 extern "C" {
 

@@ -31,7 +31,8 @@
 //    conflicts; the permutation is undone when the merge writes dims back.
 // Every wait is bounded (2 s by %globaltimer); on expiry the CTA records
 // HPC_DEVERR_WAIT_TIMEOUT, the producer waits (bounded) for its copies in
-// flight, and the CTA returns.
+// flight, and the CTA returns. HPC_ATTN_TEST_WAIT_EXPIRY makes the consumers
+// take that path on purpose, for tests of it.
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -64,7 +65,7 @@ struct Layout {
     static constexpr size_t kMeta = kML + 2 * (size_t)kNCW * kGroup * 8;
     static constexpr size_t kSink = kMeta + STAGES * 4;  // one word per consumer warp
     static constexpr size_t kBars = (kSink + kNCW * 4 + 7) / 8 * 8;
-    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kNumBars = 2 * STAGES + 6;  // full, empty, qfull x2, qempty x2, merge, unset
     static constexpr size_t kFlag = kBars + kNumBars * 8;
     static constexpr size_t kTotal = kFlag + 16;
     static constexpr size_t kAlloc = kTotal + 1024;  // base is rounded up to 1 KB (128B swizzle)
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
     uint64_t* qfull = empty + STAGES;
     uint64_t* qempty = qfull + 2;
     uint64_t* merge_bar = qempty + 2;
+    uint64_t* unset_bar = merge_bar + 1;  // never completed (failure-path test)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kFlag);
     volatile int* meta = reinterpret_cast<volatile int*>(smem + LY::kMeta);
     uint8_t* qbuf = smem + LY::kQ;
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
             mbar_init(&qempty[i], NCW);
         }
         mbar_init(merge_bar, NCW);  // one arrival per consumer warp (lane 0, after __syncwarp)
+        mbar_init(unset_bar, 1);    // nothing arrives on it
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -249,6 +252,10 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
     volatile uint32_t* q_sink = reinterpret_cast<volatile uint32_t*>(smem + LY::kSink);
     uint32_t seq = 0, mphase = 0;
     int qd = 0;
+    // Failure-path test: a wait on a barrier that nothing completes runs out
+    // after kTestWaitLimitNs, and the CTA leaves through its timeout path
+    // (the producer then drains its copies in flight).
+    if (p.test_wait_expiry && !wait_bounded(unset_bar, 0, abort_flag, kTestWaitLimitNs)) goto timeout;
     TaskAhead tw;
     tw.start(p, p.cta_off[blockIdx.x]);
     for (;;) {
@@ -519,6 +526,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)kHeadDim);
     p.early_kv = a.early_kv;
     p.max_tasks = (int)L.max_tasks;
+    p.test_wait_expiry = a.test_wait_expiry;
     // A static map, or a balanced map planned for more CTAs than the deep
     // instance keeps resident (SMs x its CTAs per SM), runs the shallow
     // instance, which holds two CTAs per SM: a caller can plan a batch of many

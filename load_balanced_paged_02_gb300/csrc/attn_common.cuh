@@ -14,6 +14,8 @@ namespace attn {
 constexpr int kScratchStride = 132;  // floats per (query) merge row
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
+// limit of the failure-path test's wait (HPC_ATTN_TEST_WAIT_EXPIRY)
+constexpr uint64_t kTestWaitLimitNs = 1000000ull;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kNegInf = -__builtin_huge_valf();
 
@@ -56,6 +58,10 @@ struct Params {
     // waits for that kernel
     int early_kv;
     int max_tasks;  // descriptor slots in the task map (bounds the early walk)
+    // 1: failure-path test (one-token kernel): the consumers first wait, with
+    // kTestWaitLimitNs, on a barrier that nothing completes, so the CTA takes
+    // its timeout path
+    int test_wait_expiry;
 };
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
@@ -286,8 +292,8 @@ constexpr uint32_t kQScaleOffE4m3 = kGroup * kQPitchE4m3;  // the 8 float32 scal
 // lanes fetch 32 page ids at a time; lane 0 issues the copies. meta[stage]
 // carries the chunk's valid token count (0: skip, page id out of range).
 // Chunk k of the CTA goes to stage k % STAGES. Every wait is bounded; on
-// expiry it raises the abort flag, records HPC_DEVERR_WAIT_TIMEOUT and waits
-// (bounded) for its own copies in flight before returning.
+// expiry it raises the abort flag and records HPC_DEVERR_WAIT_TIMEOUT. On any
+// exit it waits (bounded) for its own copies in flight before returning.
 template <bool FP8, int STAGES>
 __device__ __forceinline__ void issue_chunk(const Params& p, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                             const CUtensorMap* tm_ks, const CUtensorMap* tm_vs, uint8_t* sbuf,
@@ -404,17 +410,16 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
         if constexpr (QM == QStage::kBf16Rows) {
-            if (ok) {
-                uint8_t* qdst = qbuf + qs * q_slot_bytes;
-                for (int r = lane; r < p.q_len * kGroup; r += 32) {
-                    const int i = r / kGroup, j = r % kGroup;
-                    const long long qrow = ((long long)b * p.q_len + i) * p.num_q_heads + (long long)h * kGroup + j;
-                    bulk_load_nohint(qdst + r * kQPitchBf16, p.q + qrow * kHeadDim, kHeadDim * 2, &qfull[qs]);
-                }
+            uint8_t* qdst = qbuf + qs * q_slot_bytes;
+            for (int r = lane; r < p.q_len * kGroup; r += 32) {
+                const int i = r / kGroup, j = r % kGroup;
+                const long long qrow = ((long long)b * p.q_len + i) * p.num_q_heads + (long long)h * kGroup + j;
+                bulk_load_nohint(qdst + r * kQPitchBf16, p.q + qrow * kHeadDim, kHeadDim * 2, &qfull[qs]);
             }
         }
-        ++qd;
+        ++qd;  // query copies issued
         const int32_t* prow = p.page_table + (long long)b * p.pt_stride;
         for (int cb = c0; cb < c1 && ok; cb += 32) {
             const int cl = cb + lane;
@@ -449,16 +454,24 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
     if (!ok && lane == 0) {
         *abort_flag = 1;
         atomicOr(p.err, (int)HPC_DEVERR_WAIT_TIMEOUT);
-        // wait (bounded) for the copies this warp may still have in flight
+    }
+    // Every copy this warp issued lands before it returns, whichever way the
+    // walk ended: after an abort the consumers may have left already, and a CTA
+    // must not exit while copies into its shared memory are in flight. (On the
+    // normal path they have landed or are about to: consumers wait for each.)
+    // Chunk k < seq went to stage k % STAGES in lap k / STAGES, and every chunk
+    // before the last STAGES was consumed before its stage was issued again;
+    // query copy d < qd went to slot d % 2 in lap d / 2. Early copies the walk
+    // did not reach (an abort, or a task map that changed under the caller's
+    // contract) sit in stages [seq, npre) of the first lap.
+    if (lane == 0) {
         const uint32_t first = seq > (uint32_t)STAGES ? seq - STAGES : 0u;
         for (uint32_t k = first; k < seq; ++k)
             wait_bounded(&full[k % STAGES], (k / STAGES) & 1, nullptr, kDrainLimitNs);
-        if (qd > 0) wait_bounded(&qfull[(qd - 1) & 1], ((qd - 1) >> 1) & 1, nullptr, kDrainLimitNs);
-    }
-    // Early copies the walk did not reach (an abort, or a task map that changed
-    // under the caller's contract) still land before the CTA may exit.
-    if (lane == 0)
+        for (int d = qd > 2 ? qd - 2 : 0; d < qd; ++d)
+            wait_bounded(&qfull[d & 1], (d >> 1) & 1, nullptr, kDrainLimitNs);
         for (uint32_t k = seq; k < npre; ++k) wait_bounded(&full[k], 0, nullptr, kDrainLimitNs);
+    }
 }
 
 }  // namespace attn

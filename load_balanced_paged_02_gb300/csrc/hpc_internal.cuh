@@ -81,9 +81,20 @@ struct AttnArgs {
     float* split_o;
     float* split_lse;
     int early_kv;  // see Params::early_kv (attn_common.cuh)
+    int test_wait_expiry = 0;  // see Params::test_wait_expiry (one-token kernel only)
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 int attn_default_ctas(int fp8);
+
+// Host-side checks of one decode step's arguments (api.cu): those that
+// hpc_decode_plan, hpc_decode_attn and hpc_decode_combine make, minus the ones
+// on a task map and split buffers, for entry points that provide those
+// themselves. Enqueues nothing and makes no CUDA call.
+hpc_status step_args_check(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, int kv_dtype, int num_pages, const int32_t* page_table,
+                           int page_table_stride, const int32_t* seq_lens, int batch, int num_q_heads,
+                           int num_kv_heads, int head_dim, int page_size, int num_ctas, int min_chunks_per_cta,
+                           const void* out);
 
 // Several new tokens per request (attn_mt.cu): q is bf16 [B][q_len][Hq][128],
 // split rows are [split][q_len][8]; 2 <= q_len <= kMaxQLen.

@@ -11,36 +11,91 @@
 //
 // The array is a file-scope __device__ symbol. In host code its name is only a
 // host-side stand-in, not a device address, so the entry point looks the
-// address up with cudaGetSymbolAddress, once per device, with that device
-// current, on its first call on the device, and passes that address on.
+// address up with cudaGetSymbolAddress, with the device current, on its first
+// call on the device, and passes that address on. The address belongs to the
+// device's current context: a device reset (or a primary context released and
+// created again) loads the module again, maybe elsewhere. So the lookup is
+// cached per device together with the context's unique ID, and a call that
+// finds another context current looks the address up again.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "hpc_internal.cuh"
 
 namespace {
 
+using hpc::kGroup;
+using hpc::kHeadDim;
+
 // 8 MiB: the task map plus split_o / split_lse rows. A split row takes
-// 8 * 128 * 4 + 8 * 4 = 4128 bytes, so about 2000 rows fit, e.g.
-// 64 requests x 8 KV heads on 152 CTAs (663 rows, 2.8 MB).
+// kGroup * kHeadDim * 4 + kGroup * 4 = 4128 bytes, so about 2000 rows fit,
+// e.g. 64 requests x 8 KV heads on 152 CTAs (663 rows, 2.8 MB).
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+    unsigned long long ctx_id;  // the context the address was looked up in
+    void* addr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+// cuCtxGetCurrent and cuCtxGetId through the runtime's driver entry points
+// (the library does not link libcuda).
+struct CtxFns {
+    PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxFns& ctx_fns() {
+    static CtxFns f;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    return f;
+}
+
+// Unique ID of the calling thread's current context; 0 if none is current.
+bool current_ctx_id(unsigned long long* id) {
+    const CtxFns& f = ctx_fns();
+    if (!f.get_current || !f.get_id) return false;
+    CUcontext ctx = nullptr;
+    if (f.get_current(&ctx) != CUDA_SUCCESS) return false;
+    *id = 0;
+    return !ctx || f.get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 hpc_status scratch_base(void** base) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return HPC_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return HPC_ERR_UNSUPPORTED;
+    unsigned long long id = 0;
+    if (!current_ctx_id(&id)) return HPC_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& c = g_scratch[dev];
+    if (!c.addr || id == 0 || c.ctx_id != id) {
+        // set-up: the device address of the array in this device's current
+        // context (the lookup also makes the primary context current when none
+        // was, so the ID is read again afterwards)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return HPC_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+        if (!current_ctx_id(&id) || id == 0) return HPC_ERR_CUDA;
+        c.addr = p;
+        c.ctx_id = id;
     }
-    *base = g_scratch_addr[dev];
+    *base = c.addr;
     return HPC_OK;
 }
 
@@ -58,13 +113,18 @@ extern "C" hpc_status hpc_decode_noalloc(const void* q, const void* k_cache, con
     const size_t cap = hpc_decode_split_capacity(batch, num_kv_heads, num_ctas);
     if (!plan_bytes || !cap) return HPC_ERR_INVALID_ARG;
     const size_t off_o = round256(plan_bytes);
-    const size_t off_lse = off_o + round256(cap * 8 * 128 * sizeof(float));
-    const size_t need = off_lse + round256(cap * 8 * sizeof(float));
+    const size_t off_lse = off_o + round256(cap * kGroup * kHeadDim * sizeof(float));
+    const size_t need = off_lse + round256(cap * kGroup * sizeof(float));
     if (need > kNoAllocScratchBytes) return HPC_ERR_WORKSPACE_TOO_SMALL;
+    // every check the three calls below make, before any of them enqueues work
+    // into the shared array
+    hpc_status st = hpc::step_args_check(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, num_pages, page_table,
+                                         page_table_stride, seq_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                                         page_size, num_ctas, min_chunks_per_cta, out);
+    if (st != HPC_OK) return st;
 
     void* base = nullptr;
-    hpc_status st = scratch_base(&base);
-    if (st != HPC_OK) return st;
+    if ((st = scratch_base(&base)) != HPC_OK) return st;
     unsigned char* s = static_cast<unsigned char*>(base);
     float* split_o = reinterpret_cast<float*>(s + off_o);
     float* split_lse = reinterpret_cast<float*>(s + off_lse);

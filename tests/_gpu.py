@@ -74,35 +74,28 @@ def check_plan_exact(res, case, num_ctas=None, min_chunks=2, static_splits=None)
     return ref
 
 
-def check_full(case, res, check_splits=True):
-    """Compare every output row (and every split partial) with the oracle."""
-    host = wl.to_numpy_case(case)
+def check_full(case, res, check_splits=True, host=None, rows=None, what=""):
+    """Compare every output row (and every split partial) with the oracle.
+
+    ``host`` (a host copy of the case) and ``rows`` (the oracle's full-sequence
+    rows of it) may be given when several runs share one case. Returns the
+    largest and mean absolute output errors and the largest LSE error."""
+    if host is None:
+        host = wl.to_numpy_case(case)
     shape = host["q"].shape[:-1]  # [B, Hq] or [B, q_len, Hq]
-    ro, rl = oracle.attn_rows(host)
-    assert_close(res["out"].float().cpu().numpy(), res["lse"].cpu().numpy(), ro.reshape(shape + (128,)),
-                 rl.reshape(shape), case, "output")
+    ro, rl = oracle.attn_rows(host) if rows is None else rows
+    tag = f"{what} " if what else ""
+    err = assert_close(res["out"].float().cpu().numpy(), res["lse"].cpu().numpy(), ro.reshape(shape + (128,)),
+                       rl.reshape(shape), case, tag + "output")
+    fin = np.isfinite(rl)
+    lerr = float(np.abs(res["lse"].cpu().numpy().reshape(-1)[fin] - rl[fin]).max()) if fin.any() else 0.0
     if check_splits:
         pb = res["plan"].buf.cpu().numpy()
         so, sl = oracle.attn_splits(pb, host)
         n = so.shape[0]
         assert_close(res["split_o"][:n].cpu().numpy(), res["split_lse"][:n].cpu().numpy(), so, sl,
-                     case, "split partials")
-
-
-def check_sampled(case, res, requests, heads=None):
-    """Compare rows of the given requests (all query heads, or `heads`) with the
-    oracle run on a host copy of just those requests' pages."""
-    host = wl.to_numpy_case(case, requests=requests)
-    Hq = host["q"].shape[-2]
-    Q = host["q"].shape[1] if host["q"].ndim == 4 else 1
-    heads = list(range(Hq)) if heads is None else list(heads)
-    rows = [(i, qi * Hq + h) for i in range(len(requests)) for qi in range(Q) for h in heads]
-    ro, rl = oracle.attn_rows(host, rows)
-    out = res["out"].float().cpu().numpy().reshape(len(case["seq_lens"]), Q, Hq, 128)
-    lse = res["lse"].cpu().numpy().reshape(len(case["seq_lens"]), Q, Hq)
-    got_o = np.stack([out[requests[i], r // Hq, r % Hq] for i, r in rows])
-    got_l = np.array([lse[requests[i], r // Hq, r % Hq] for i, r in rows])
-    return assert_close(got_o, got_l, ro, rl, case, f"sampled rows of requests {list(requests)}")
+                     case, tag + "split partials")
+    return float(err.max()), float(err.mean()), lerr
 
 
 def check_split_invariants(case, res):

@@ -127,8 +127,12 @@ def test_attn_ex_rejects_bad_arguments(L):
         return L.hpc_decode_attn_ex(a["q"], a["qs"], a["ql"], a["k"], a["v"], a["ks"], a["vs"], a["dt"],
                                     a["pages"], a["pt"], a["stride"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["D"],
                                     a["P"], a["plan"], a["so"], a["slse"], a["eng"], a["flags"], None)
-    assert call(flags=2) == 1
+    assert call(flags=4) == 1
     assert call(flags=-1) == 1
+    # the failure-path test flag: one new token on the warp-level kernel only
+    assert call(flags=hb.ATTN_TEST_WAIT_EXPIRY, ql=2) == 2
+    assert call(flags=hb.ATTN_TEST_WAIT_EXPIRY, ql=3) == 2
+    assert call(flags=hb.ATTN_TEST_WAIT_EXPIRY, eng=hb.ENGINE_TCGEN05) == 2
     assert call(ql=0) == 1
     assert call(ql=9) == 1
     assert call(eng=3) == 1
@@ -216,3 +220,24 @@ def test_rope_norm_rejects_bad_arguments(L):
     # no tokens: valid and nothing to do
     assert call(num_tokens=0) == 0
     assert call(num_tokens=0, kv_dtype=hb.KV_FP8_E4M3, k_scale=FAKE, v_scale=FAKE) == 0
+
+
+def test_noalloc_refuses_before_any_work(L):
+    """hpc_decode_noalloc runs every check of plan, attention and combine
+    before its first launch (fake pointers: nothing may be enqueued)."""
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ks=None, vs=None, dt=0, pages=1000, pt=FAKE, stride=8, sl=FAKE, B=24,
+                 Hq=64, Hkv=8, D=128, P=64, C=152, m=2, out=FAKE, lse=None)
+        a.update(kw)
+        return L.hpc_decode_noalloc(a["q"], a["k"], a["v"], a["ks"], a["vs"], a["dt"], a["pages"], a["pt"],
+                                    a["stride"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], a["C"],
+                                    a["m"], a["out"], a["lse"], None)
+    assert call(B=4096) == 3                      # beyond the fixed array
+    assert call(D=64) == 2
+    assert call(P=32) == 2
+    assert call(Hq=32) == 2
+    assert call(dt=7) == 2
+    for bad in (dict(q=None), dict(sl=None), dict(pt=None), dict(out=None), dict(q=FAKE_ODD),
+                dict(out=ctypes.c_void_p(0x10002)), dict(m=-1), dict(pages=0), dict(stride=0),
+                dict(dt=1), dict(dt=1, ks=FAKE), dict(B=0), dict(C=0)):
+        assert call(**bad) == 1, bad

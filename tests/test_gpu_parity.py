@@ -2,9 +2,9 @@
 
 Task maps must match byte for byte. Outputs: BF16 KV max abs <= 2e-2 and mean
 abs <= 2e-3; e4m3 KV max abs <= 6e-2; LSE <= 1e-3 abs. Small cases compare
-every output row and every split partial; the full-size workloads compare all
-query heads of sampled requests (the longest, the shortest and seeded others)
-plus size-independent properties of the partials.
+every output row and every split partial, and so do the full-size workloads
+(tiny, uniform, mixed, skew, e4m3, e4m3 query, many short requests), for the
+balanced map and for the static split-KV map of the same kernel.
 """
 import numpy as np
 import pytest
@@ -441,39 +441,36 @@ def test_many_steps_chained_without_sync():
 
 # ------------------------------------------------------------------ full-size workloads
 
-def _sample_requests(lens, k, seed):
-    lens = np.asarray(lens)
-    order = np.argsort(lens)
-    pick = {int(order[-1]), int(order[0])}
-    rng = np.random.default_rng(seed)
-    while len(pick) < min(k, len(lens)):
-        pick.add(int(rng.integers(0, len(lens))))
-    return sorted(pick)
-
-
 def test_uniform_workload_full():
     w = wl.WORKLOADS["uniform"]
     case = wl.make_case(w, device=DEV)
     res = _gpu.run(case, num_ctas=w.num_ctas, min_chunks=w.min_chunks)
     _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
-    _gpu.check_full(case, res, check_splits=False)
+    _gpu.check_full(case, res, check_splits=True, what="uniform")
     _gpu.check_split_invariants(case, res)
 
 
 @pytest.mark.parametrize("name", ["mixed", "skew", "fp8", "fp8q", "short"])
-def test_full_size_workload_sampled(name):
+def test_full_size_workload_every_row(name):
+    """The full batch in the launch configuration the benchmark times: every
+    output row and LSE and every split partial of the balanced map against the
+    float64 oracle; then the static split-KV schedule of the same kernel
+    (S = 16), again every row (and every split partial on the bf16 batches)."""
     w = wl.WORKLOADS[name]
     case = wl.make_case(w, device=DEV)
+    host = wl.to_numpy_case(case)
+    rows = oracle.attn_rows(host)
     C = hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"]))
     res = _gpu.run(case, num_ctas=C, min_chunks=w.min_chunks)
     _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
-    lens = case["seq_lens"].cpu().numpy()
-    _gpu.check_sampled(case, res, _sample_requests(lens, 5, seed=w.seed))
+    _gpu.check_full(case, res, host=host, rows=rows, what=f"{name} balanced (C={C})")
     _gpu.check_split_invariants(case, res)
     assert hb.hpc_decode_read_error(res["plan"]) == 0
-    # the static split-KV schedule of the same kernel gives the same answer
+    del res
     st = _gpu.run(case, static_splits=w.static_splits)
     _gpu.check_plan_exact(st, case, static_splits=w.static_splits)
-    _gpu.check_sampled(case, st, _sample_requests(lens, 3, seed=w.seed + 1))
-    diff = (st["out"].float() - res["out"].float()).abs().max().item()
-    assert diff <= 2 * _gpu.tolerances(case)[0]
+    # (the e4m3 batches' static partials, 7824 of them, are left to the
+    # split/combine property: the oracle takes ~17 s per pass over that batch)
+    _gpu.check_full(case, st, host=host, rows=rows, check_splits=w.kv_dtype != "fp8",
+                    what=f"{name} static (S={w.static_splits})")
+    _gpu.check_split_invariants(case, st)
