@@ -8,7 +8,13 @@ the mixed-length Hy3-shape batch (64 requests, lengths log-uniform in
 
 Prints one JSON line. `value` = effective KV GB/s = (live K+V bytes + Q bytes
 + split-partial bytes written and read) / device time per step. The KV stream
-(2.75 GB) is larger than L2, so no flush is needed between steps.
+(2.4 GB) is larger than L2, so no flush is needed between steps. The line's
+`configs` record repeats the measurement on each of the five scope workloads
+(tiny, uniform, mixed, skew, e4m3): medians of 200 CUDA-graph replays of the
+step and of 200 attention launches (L2 flushed before each call where the KV
+fits in it), the attention kernel's fraction of the measured and nominal HBM
+peaks, the static split-KV schedule (S = 16) of the same kernel, and the
+oracle's time on the host cores (also single-threaded for tiny and uniform).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload mixed|uniform|skew|fp8|tiny]
@@ -54,6 +60,8 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="time eager launches only")
     ap.add_argument("--no-prologue", action="store_true", help="skip the fused-prologue timing")
     ap.add_argument("--no-multi-token", action="store_true", help="skip the q_len > 1 timings")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload record (tiny, uniform, mixed, skew, fp8)")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the plan -> prologue -> attention -> combine layer timing")
     ap.add_argument("--num-ctas", type=int, default=0,
@@ -172,6 +180,23 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm), "window": "timed region" if use is inside else "whole run"}
+
+
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (~8 TB/s)
+L2_BYTES = 129 * 1024 * 1024
+
+
+def workload_config(w):
+    """The line's `config`: what identifies the workload, the same in both arms."""
+    from load_balanced_paged_02_gb300 import workloads as wl
+    lens = wl.draw_lengths(w)
+    kv = wl.kv_bytes(lens, w.num_kv_heads, w.kv_dtype)
+    return {"workload": w.name, "detail": w.note, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "kv_dtype": "e4m3" if w.kv_dtype == "fp8" else "bf16",
+            "q_dtype": "e4m3" if w.q_dtype == "fp8" else "bf16", "q_len": w.q_len,
+            "live_tokens": int(np.maximum(lens, 0).sum()), "kv_bytes": int(kv),
+            "l2": ("inputs larger than L2 (no flush)" if kv > L2_BYTES else
+                   "inputs smaller than L2: the main loop does not flush; the configs record flushes")}
 
 
 def measured_peaks():
@@ -461,6 +486,117 @@ def multi_token_timing(w, case, plan, C, dev, q_lens=(2, 6), n_rep=100):
     return res
 
 
+def _median_us(fn, n, stream, flush=None):
+    """Median device time of n calls of fn, each bracketed by its own CUDA
+    events on ``stream``; ``flush`` (a buffer larger than L2) is rewritten
+    before every call, outside the events."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in ev:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return 1e3 * float(np.median([a.elapsed_time(b) for a, b in ev]))
+
+
+CONFIG_WORKLOADS = ("tiny", "uniform", "mixed", "skew", "fp8")
+
+
+def config_record(name, dev, n_rep=200, cpu_seconds=2.0, single_thread=False):
+    """One of the five scope workloads at N = 1: the step (plan + attention +
+    combine) captured as a CUDA graph, its median over n_rep replays; the
+    attention kernel alone (median of n_rep eager launches) against the HBM
+    roofline; the static split-KV schedule of the same kernel (S = 16); and the
+    float64 oracle on the host cores (a bounded sample, scaled to the batch).
+    Workloads whose KV fits in L2 flush it before every timed call."""
+    import torch
+    from load_balanced_paged_02_gb300 import binding as hb
+    from load_balanced_paged_02_gb300 import workloads as wl
+    w = wl.by_name(name)
+    case = wl.make_case(w, device=dev)
+    kvd = hb.kv_dtype_of(case["k_cache"])
+    C = w.num_ctas or hb.default_num_ctas(kvd)
+    Hkv = w.num_kv_heads
+    lens = case["seq_lens"].cpu().numpy()
+    stream = torch.cuda.current_stream(dev)
+    plan = hb.Plan(w.batch, Hkv, C, dev)
+    hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
+    splan = hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits)
+    so, sl = hb.split_buffers(plan)
+    sso, ssl = hb.split_buffers(splan)
+    out = torch.empty(case["q"].shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(case["q"].shape[:-1], dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    n_splits, s_splits = int(plan.buf[3].item()), int(splan.buf[3].item())
+    byt = step_bytes(lens, w, n_splits)
+    flush = None
+    if byt["kv"] <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def attn(pl, a, b):
+        hb.hpc_decode_attn(case["q"], case["k_cache"], case["v_cache"], case["page_table"], case["seq_lens"], pl,
+                           a, b, case["k_scale"], case["v_scale"], num_pages=case["num_pages"],
+                           q_scale=case["q_scale"])
+
+    def step():
+        hb.hpc_decode_plan(case["seq_lens"], Hkv, C, w.min_chunks, plan=plan)
+        attn(plan, so, sl)
+        hb.hpc_decode_combine(plan, so, sl, out, lse, Hkv)
+
+    def sstep():
+        hb.hpc_decode_plan_static(case["seq_lens"], Hkv, w.static_splits, plan=splan)
+        attn(splan, sso, ssl)
+        hb.hpc_decode_combine(splan, sso, ssl, out, lse, Hkv)
+
+    graphs = []
+    for fn in (step, sstep):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g.replay()
+        graphs.append(g)
+    torch.cuda.synchronize()
+    if hb.hpc_decode_read_error(plan) != 0 or hb.hpc_decode_read_error(splan) != 0:
+        raise RuntimeError(f"{name}: device error word set")
+    step_us = _median_us(graphs[0].replay, n_rep, stream, flush)
+    static_us = _median_us(graphs[1].replay, n_rep, stream, flush)
+    attn_us = _median_us(lambda: attn(plan, so, sl), n_rep, stream, flush)
+    peak, peak_kind = measured_peaks()
+    gbs = byt["attn"] / (attn_us * 1e-6) / 1e9
+    rec = {"detail": w.note, "num_ctas": C, "min_chunks": w.min_chunks, "splits": n_splits,
+           "replays": n_rep, "l2": "flushed before every call" if flush is not None else "inputs larger than L2",
+           "step_us_median": step_us, "value_GBps": byt["metric"] / (step_us * 1e-6) / 1e9,
+           "attn_us_median": attn_us, "attn_algorithmic_bytes": byt["attn"], "attn_GBps": gbs,
+           "frac_of_measured": gbs / peak, "measured_peak": peak, "peak_kind": peak_kind,
+           "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
+           "static_split_kv": {"num_splits": w.static_splits, "splits": s_splits, "step_us_median": static_us,
+                               "balanced_speedup": static_us / step_us}}
+    del graphs, so, sl, sso, ssl
+    if cpu_seconds > 0:
+        import oracle
+        full_s, cores, text = oracle_sample(case, w, cpu_seconds)
+        rec["oracle"] = {"ms_per_step": full_s * 1e3, "value_GBps": byt["metric"] / full_s / 1e9,
+                         "threads": cores, "sample": text}
+        if single_thread:
+            prev = oracle.num_threads()
+            oracle.set_num_threads(1)
+            try:
+                full_s, cores, text = oracle_sample(case, w, cpu_seconds)
+            finally:
+                oracle.set_num_threads(prev)
+            rec["oracle_1_thread"] = {"ms_per_step": full_s * 1e3, "value_GBps": byt["metric"] / full_s / 1e9,
+                                      "threads": cores, "sample": text}
+    del case, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -486,7 +622,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "detail": w.note},
+            "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -630,17 +766,18 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if kvd == hb.KV_BF16 else ("e4m3 (q and kv)" if w.q_dtype == "fp8" else "e4m3 kv, bf16 q"),
             "data": "synthetic",
-            "config": {"workload": w.name, "detail": w.note, "num_ctas": C, "min_chunks": w.min_chunks,
-                       "engine": args.engine if w.q_len > 1 else "one-token kernel",
-                       "live_tokens": int(lens.sum()), "splits": n_splits,
-                       "bytes_per_step": byt, "l2": "inputs larger than L2 (no flush)",
-                       "step": "cuda graph replay" if graph is not None else "eager launches",
-                       "us_per_step": {"plan": plan_us, "attn": attn_us, "combine": comb_us,
-                                       "eager_total": eager_ms * 1e3,
-                                       "graph_total": graph_ms * 1e3 if graph_ms is not None else None,
-                                       "layer_attn_combine": layer_us}},
+            "config": workload_config(w),
+            "breakdown": {"num_ctas": C, "min_chunks": w.min_chunks,
+                          "engine": args.engine if w.q_len > 1 else "one-token kernel",
+                          "splits": n_splits, "bytes_per_step": byt,
+                          "step": "cuda graph replay" if graph is not None else "eager launches",
+                          "us_per_step": {"plan": plan_us, "attn": attn_us, "combine": comb_us,
+                                          "eager_total": eager_ms * 1e3,
+                                          "graph_total": graph_ms * 1e3 if graph_ms is not None else None,
+                                          "layer_attn_combine": layer_us}},
             "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                          "frac": attn_gbs / peak, "peak_kind": peak_kind,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": attn_gbs / NOMINAL_HBM_GBS,
                          "traffic": recorded_traffic(w.name, "bf16" if kvd == hb.KV_BF16 else "e4m3", kname),
                          "kernel": kname, "algorithmic_bytes_per_launch": byt["attn"]},
             "gpu_launches": (6 if graph is not None else 3) * args.steps,
@@ -746,6 +883,12 @@ def run_ours(args):
     # ---- the layer chained with the prologue, KV gathered before Q is ready (NEXT-3)
     if rank == 0 and not args.no_chain and w.q_len == 1 and w.q_dtype == "bf16":
         result["chained_layer"] = chained_layer_timing(w, case, C, dev)
+
+    # ---- the five scope workloads, each with its static split-KV comparison (N = 1 only)
+    if rank == 0 and world == 1 and not args.no_configs:
+        result["configs"] = {n: config_record(n, dev, cpu_seconds=0.0 if args.no_cpu_baseline else 2.0,
+                                              single_thread=n in ("tiny", "uniform"))
+                             for n in CONFIG_WORKLOADS}
 
     # ---- CPU oracle baseline (rank 0 only, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
