@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--no-multi-token", action="store_true", help="skip the q_len > 1 timings")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the per-workload record (tiny, uniform, mixed, skew, fp8)")
+    ap.add_argument("--prologue-only", action="store_true",
+                    help="time only the fused prologue for the workload's head shape and cache dtype "
+                         "(a decode step and an 8192-token prefill; no attention batch is created)")
+    ap.add_argument("--prologue-reps", type=int, default=200, help="graph replays per prologue timing")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the plan -> prologue -> attention -> combine layer timing")
     ap.add_argument("--num-ctas", type=int, default=0,
@@ -642,6 +646,12 @@ def run_ours(args):
     from load_balanced_paged_02_gb300 import workloads as wl
     _build.build()
     hb.lib()
+    if args.prologue_only:
+        w = wl.by_name(args.workload)
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "prologue": prologue_timing(w, dev, n_rep=args.prologue_reps)}),
+                  flush=True)
+        return 0
 
     w = rank_workload(wl.by_name(args.workload), rank)
     case = wl.make_case(w, device=dev)

@@ -168,6 +168,77 @@ def test_large_call_instance_matches_oracle(fp8):
         assert np.array_equal(vc, rv.astype(np.float32))
 
 
+def _check_large(pc, q_fp8, kv_fp8, slots, pages, what):
+    q, qs, k, v, ks, vs = run_prologue(pc, q_fp8, kv_fp8, num_pages=pages)
+    rq, rk, rv = _oracle(pc)
+    Hkv = pc["num_kv_heads"]
+    tol = lambda r: 2.0 ** -8 * np.abs(r) + 2e-5  # noqa: E731
+    if q_fp8:
+        check_e4m3_rows(q.view(torch.uint8).cpu().numpy(), qs.cpu().numpy(), rq, f"{what} q")
+    else:
+        assert np.all(np.abs(q.float().cpu().numpy() - rq) <= tol(rq)), f"{what} q"
+    live = slots >= 0
+    sl = slots[live]
+    if kv_fp8:
+        kc = k.view(torch.uint8).cpu().numpy().reshape(pages * 64, Hkv, 128)
+        vc = v.view(torch.uint8).cpu().numpy().reshape(pages * 64, Hkv, 128)
+        ksc = ks.cpu().numpy().transpose(0, 2, 1).reshape(pages * 64, Hkv)
+        vsc = vs.cpu().numpy().transpose(0, 2, 1).reshape(pages * 64, Hkv)
+        check_e4m3_rows(kc[sl], ksc[sl], rk[live], f"{what} k")
+        check_e4m3_rows(vc[sl], vsc[sl], rv[live], f"{what} v")
+        untouched = np.ones(pages * 64, dtype=bool)
+        untouched[sl] = False
+        assert np.all(ksc[untouched] == -7.0) and np.all(vsc[untouched] == -7.0), f"{what}: stray writes"
+    else:
+        kc = k.float().cpu().numpy().reshape(pages * 64, Hkv, 128)
+        vc = v.float().cpu().numpy().reshape(pages * 64, Hkv, 128)
+        assert np.all(np.abs(kc[sl] - rk[live]) <= tol(rk[live])), f"{what} k"
+        assert np.array_equal(vc[sl], rv[live].astype(np.float32)), f"{what} v"
+        untouched = np.ones(pages * 64, dtype=bool)
+        untouched[sl] = False
+        assert np.all(kc[untouched] == 3.0) and np.all(vc[untouched] == 3.0), f"{what}: stray writes"
+
+
+@pytest.mark.parametrize("Hq,Hkv,T", [(8, 1, 5001), (12, 3, 2500), (64, 8, 1203)])
+@pytest.mark.parametrize("q_fp8,kv_fp8", [(False, False), (True, True), (False, True), (True, False)])
+def test_prefill_ring_kernel_matches_oracle(Hq, Hkv, T, q_fp8, kv_fp8):
+    """Prefill-sized calls (at least two ring stages per SM) run the ring-fed
+    kernel: 8/1 heads (16 tokens per stage), 12/3 heads (18 rows per token, so
+    a 4-row unit straddles two tokens), 64/8 heads; a partial last stage;
+    padding slots (-1, nothing written) among shuffled slots; every output
+    format combination."""
+    rng = np.random.default_rng(T + Hq)
+    pos = rng.integers(0, 4000, size=T).astype(np.int32)
+    pages = (T + 63) // 64 + 2
+    slots = rng.permutation(pages * 64)[:T].astype(np.int32)
+    slots[::97] = -1
+    pc = wl.make_prologue_case(pos, Hq, Hkv, seed=T, device=DEV, max_pos=4096, slots=slots)
+    _check_large(pc, q_fp8, kv_fp8, slots, pages, f"{Hq}/{Hkv} T={T}")
+
+
+def test_prefill_ring_kernel_error_bits():
+    """A bad position (not rotated) and an out-of-range slot (nothing written)
+    in a prefill-sized call set their error bits; the other rows are exact."""
+    T, Hq, Hkv = 5000, 8, 1
+    pos = (np.arange(T) % 4000).astype(np.int32)
+    pos[17] = 5000
+    pages = (T + 63) // 64
+    slots = np.arange(T, dtype=np.int32)
+    slots[33] = pages * 64 + 5
+    pc = wl.make_prologue_case(pos, Hq, Hkv, seed=5, device=DEV, max_pos=4096, slots=slots)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, _, k, _, _, _ = run_prologue(pc, False, False, num_pages=pages, err=err)
+    assert int(err.item()) & 32 and int(err.item()) & 4
+    good = pos.copy()
+    good[17] = 0  # the bad position's rows are normalised but not rotated (identity rotation at 0)
+    rq, rk, _ = _oracle(dict(pc, positions=torch.from_numpy(good).to(DEV)))
+    tol = lambda r: 2.0 ** -8 * np.abs(r) + 2e-5  # noqa: E731
+    assert np.all(np.abs(q.float().cpu().numpy() - rq) <= tol(rq))
+    kc = k.float().cpu().numpy().reshape(pages * 64, Hkv, 128)
+    live = np.arange(T) != 33
+    assert np.all(np.abs(kc[slots[live]] - rk[live]) <= tol(rk[live]))
+
+
 def test_bad_position_sets_error_bit():
     pc = wl.make_prologue_case([3, 9000, 5], 8, 1, seed=3, device=DEV, max_pos=16)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
