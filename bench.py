@@ -69,8 +69,8 @@ def parse():
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the plan -> prologue -> attention -> combine layer timing")
     ap.add_argument("--num-ctas", type=int, default=0,
-                    help="CTAs the task map is planned for (0: the workload's stated count, else one "
-                         "wave of the deep attention instance)")
+                    help="CTAs the task map is planned for (0: the workload's stated count, else the "
+                         "library's suggestion for the batch, hpc_decode_suggest_num_ctas)")
     ap.add_argument("--engine", choices=["auto", "mma_sync", "tcgen05"], default="auto",
                     help="attention kernel for workloads with several new tokens per request "
                          "(<workload>:qlen<N>); auto = the library's own choice")
@@ -506,7 +506,7 @@ def _median_us(fn, n, stream, flush=None):
     return 1e3 * float(np.median([a.elapsed_time(b) for a, b in ev]))
 
 
-CONFIG_WORKLOADS = ("tiny", "uniform", "mixed", "skew", "fp8")
+CONFIG_WORKLOADS = ("tiny", "uniform", "mixed", "skew", "fp8", "short")
 
 
 def config_record(name, dev, n_rep=200, cpu_seconds=2.0, single_thread=False):
@@ -522,7 +522,7 @@ def config_record(name, dev, n_rep=200, cpu_seconds=2.0, single_thread=False):
     w = wl.by_name(name)
     case = wl.make_case(w, device=dev)
     kvd = hb.kv_dtype_of(case["k_cache"])
-    C = w.num_ctas or hb.default_num_ctas(kvd)
+    C = w.num_ctas or hb.suggest_num_ctas(case["seq_lens"], w.num_kv_heads, kvd, w.min_chunks)
     Hkv = w.num_kv_heads
     lens = case["seq_lens"].cpu().numpy()
     stream = torch.cuda.current_stream(dev)
@@ -656,9 +656,10 @@ def run_ours(args):
     w = rank_workload(wl.by_name(args.workload), rank)
     case = wl.make_case(w, device=dev)
     kvd = hb.kv_dtype_of(case["k_cache"])
-    # the CTA count a workload states (tiny: 16, uniform: 148), else one wave of the
-    # deep attention instance; --num-ctas overrides both
-    C = args.num_ctas if args.num_ctas > 0 else (w.num_ctas or hb.default_num_ctas(kvd))
+    # the CTA count a workload states (tiny: 16, uniform: 148), else the library's
+    # suggestion for the batch (hpc_decode_suggest_num_ctas); --num-ctas overrides both
+    C = args.num_ctas if args.num_ctas > 0 else (
+        w.num_ctas or hb.suggest_num_ctas(wl.draw_lengths(w), w.num_kv_heads, kvd, w.min_chunks, w.q_len))
     eng = {"auto": None, "mma_sync": hb.ENGINE_MMA_SYNC, "tcgen05": hb.ENGINE_TCGEN05}[args.engine]
     if w.q_len == 1:
         eng = None  # one new token: hpc_decode_attn's kernel

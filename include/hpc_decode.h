@@ -144,6 +144,23 @@ size_t hpc_decode_split_capacity(int batch, int num_kv_heads, int num_ctas);
 int hpc_decode_default_num_ctas(int kv_dtype);
 
 /*
+ * A CTA count to plan a batch for, from its lengths on the host (int32
+ * [batch], host memory; nothing is enqueued). The pages leave the CTA count to
+ * the caller ([SGL] "Scheduling around live KV work": the planner divides the
+ * work by the number of CTAs). The rule: plan the batch for
+ * hpc_decode_default_num_ctas(kv_dtype) CTAs (one per SM); if some CTA of that
+ * plan would hold 16 or more descriptors (a batch of many short requests, each
+ * descriptor paying a fixed cost beyond its chunks), return the count of the
+ * shallow instance instead (two CTAs per SM), which halves such lists;
+ * otherwise the default count. With several new tokens per request (q_len >
+ * 1) the default count. Any count gives the same outputs up to rounding; the
+ * task map for each count is exact. Returns 0 for bad arguments or when the
+ * device cannot be queried.
+ */
+int hpc_decode_suggest_num_ctas(const int32_t* h_seq_lens, int batch, int num_kv_heads,
+                                int min_chunks_per_cta, int kv_dtype, int q_len);
+
+/*
  * Load-balanced planner ([SGL] "Scheduling around live KV work"; [VLLM]
  * "解决方案：按步负载均衡的 decode 调度器", assign stage). For each request
  * n_b = ceil(seq_lens[b] / 64); T = num_kv_heads * sum(n_b);

@@ -50,6 +50,7 @@ SIGNATURES = {
     "hpc_decode_plan_bytes": (_sz, [_i, _i, _i]),
     "hpc_decode_split_capacity": (_sz, [_i, _i, _i]),
     "hpc_decode_default_num_ctas": (_i, [_i]),
+    "hpc_decode_suggest_num_ctas": (_i, [_vp, _i, _i, _i, _i, _i]),
     "hpc_decode_attn_multi_auto_engine": (_i, [_i, _i]),
     "hpc_decode_plan": (_i, [_vp, _i, _i, _i, _i, _P, _vp]),
     "hpc_decode_plan_static": (_i, [_vp, _i, _i, _i, _P, _vp]),
@@ -154,6 +155,19 @@ def default_num_ctas(kv_dtype: int = KV_BF16) -> int:
     n = lib().hpc_decode_default_num_ctas(kv_dtype)
     if n <= 0:
         raise HpcError("hpc_decode_default_num_ctas", detail="device query failed")
+    return n
+
+
+def suggest_num_ctas(seq_lens, num_kv_heads: int, kv_dtype: int = KV_BF16, min_chunks_per_cta: int = 2,
+                     q_len: int = 1) -> int:
+    """hpc_decode_suggest_num_ctas on host lengths (a CPU int32 tensor or array)."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens.cpu().numpy() if isinstance(seq_lens, torch.Tensor) else seq_lens,
+                              dtype=np.int32)
+    n = lib().hpc_decode_suggest_num_ctas(ctypes.c_void_p(sl.ctypes.data), int(sl.shape[0]), num_kv_heads,
+                                          min_chunks_per_cta, kv_dtype, q_len)
+    if n <= 0:
+        raise HpcError("hpc_decode_suggest_num_ctas", detail="bad arguments or device query failed")
     return n
 
 

@@ -2,7 +2,9 @@
 // host-side argument checks, then the launches in plan.cu, attn.cu and
 // combine.cu. Nothing here allocates device memory or synchronises, except
 // hpc_decode_read_error.
+#include <algorithm>
 #include <new>
+#include <vector>
 
 #include "hpc_internal.cuh"
 
@@ -13,6 +15,13 @@ namespace {
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// hpc_decode_suggest_num_ctas: the most descriptors one CTA of the one-per-SM plan
+// may hold before two CTAs per SM are suggested. On GB300 (bf16, 64/8 heads)
+// 1024 requests of 128 tokens (54 descriptors per CTA) and the 32 x 128 + 32 x
+// 4096 mix (56 in its first CTAs) ran faster on 304 CTAs; batches whose CTAs
+// hold a few descriptors each ran faster on 152.
+constexpr int kManyDescriptorsPerCta = 16;
 
 bool sizes_ok(int batch, int num_kv_heads, long long num_ctas) {
     return batch >= 1 && batch <= HPC_MAX_BATCH && num_kv_heads >= 1 &&
@@ -92,6 +101,46 @@ size_t hpc_decode_split_capacity(int batch, int num_kv_heads, int num_ctas) {
 int hpc_decode_default_num_ctas(int kv_dtype) {
     if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return 0;
     return attn_default_ctas(kv_dtype == HPC_KV_FP8_E4M3);
+}
+
+int hpc_decode_suggest_num_ctas(const int32_t* h_seq_lens, int batch, int num_kv_heads, int min_chunks_per_cta,
+                                int kv_dtype, int q_len) {
+    if (!h_seq_lens || !sizes_ok(batch, num_kv_heads, 1) || min_chunks_per_cta < 0) return 0;
+    if (kv_dtype != HPC_KV_BF16 && kv_dtype != HPC_KV_FP8_E4M3) return 0;
+    if (q_len < 1 || q_len > HPC_MAX_Q_LEN) return 0;
+    const bool fp8 = kv_dtype == HPC_KV_FP8_E4M3;
+    const int deep = attn_default_ctas(fp8);
+    if (deep <= 0 || q_len > 1) return deep;  // the multi-token kernels keep one CTA per SM
+    // chunk counts per request and the total over the head-major walk
+    long long per_head = 0;
+    for (int b = 0; b < batch; ++b) per_head += h_seq_lens[b] > 0 ? (h_seq_lens[b] + kChunk - 1) / kChunk : 0;
+    const long long T = per_head * num_kv_heads;
+    if (T == 0) return deep;
+    const long long bucket = std::max<long long>({(T + deep - 1) / deep, (long long)min_chunks_per_cta, 1LL});
+    // descriptors per CTA of the deep plan: pair (h, b) with chunks [g0, g0 + n) of
+    // the walk has one descriptor in every CTA its range touches; every head
+    // walks the same requests, so the walk is a head's run repeated
+    std::vector<int> desc((size_t)deep + 1, 0);
+    long long g0 = 0;
+    int most = 0;
+    for (int h = 0; h < num_kv_heads; ++h) {
+        for (int b = 0; b < batch; ++b) {
+            const int L = h_seq_lens[b];
+            const long long n = L > 0 ? (L + kChunk - 1) / kChunk : 0;
+            if (n == 0) continue;
+            const long long c0 = g0 / bucket, c1 = (g0 + n - 1) / bucket;
+            for (long long c = c0; c <= c1 && c <= deep; ++c) most = std::max(most, ++desc[(size_t)c]);
+            g0 += n;
+        }
+    }
+    // A CTA whose list holds many descriptors pays a fixed cost for each (query
+    // staging, the merge of its warps' states, the partial's write) on top of
+    // its share of the stream; two CTAs per SM halve such lists and overlap one
+    // CTA's merges with the other's loads. Batches of a few long requests keep
+    // one CTA per SM: more CTAs only add partials to combine.
+    if (most < kManyDescriptorsPerCta) return deep;
+    const int shallow = attn_shallow_ctas(fp8);
+    return shallow > deep ? shallow : deep;
 }
 
 hpc_status hpc_decode_plan(const int32_t* d_seq_lens, int batch, int num_kv_heads, int num_ctas,

@@ -492,6 +492,14 @@ int attn_default_ctas(int fp8) {
     return sms * (per > 0 ? per : 1);
 }
 
+int attn_shallow_ctas(int fp8) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    const int per = fp8 ? StaticFp8::ctas_per_sm() : StaticBf16::ctas_per_sm();
+    return sms * (per > 0 ? per : 1);
+}
+
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     CUtensorMap maps[4];  // K, V, K scales, V scales (the last two unused for bf16)
     memset(maps, 0, sizeof maps);

@@ -85,6 +85,8 @@ struct AttnArgs {
 };
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s);
 int attn_default_ctas(int fp8);
+// CTAs of the shallow one-token instance resident in one wave (SMs x its CTAs per SM).
+int attn_shallow_ctas(int fp8);
 
 // Host-side checks of one decode step's arguments (api.cu): those that
 // hpc_decode_plan, hpc_decode_attn and hpc_decode_combine make, minus the ones

@@ -241,3 +241,17 @@ def test_noalloc_refuses_before_any_work(L):
                 dict(out=ctypes.c_void_p(0x10002)), dict(m=-1), dict(pages=0), dict(stride=0),
                 dict(dt=1), dict(dt=1, ks=FAKE), dict(B=0), dict(C=0)):
         assert call(**bad) == 1, bad
+
+
+def test_suggest_num_ctas_refuses_bad_arguments(L):
+    """Host-side checks of hpc_decode_suggest_num_ctas (0 for bad arguments)."""
+    import numpy as np
+    sl = np.full(8, 100, dtype=np.int32)
+    p = ctypes.c_void_p(sl.ctypes.data)
+    assert L.hpc_decode_suggest_num_ctas(None, 8, 8, 2, 0, 1) == 0
+    assert L.hpc_decode_suggest_num_ctas(p, 0, 8, 2, 0, 1) == 0
+    assert L.hpc_decode_suggest_num_ctas(p, 8, 0, 2, 0, 1) == 0
+    assert L.hpc_decode_suggest_num_ctas(p, 8, 8, -1, 0, 1) == 0
+    assert L.hpc_decode_suggest_num_ctas(p, 8, 8, 2, 7, 1) == 0
+    assert L.hpc_decode_suggest_num_ctas(p, 8, 8, 2, 0, 0) == 0
+    assert L.hpc_decode_suggest_num_ctas(p, 8, 8, 2, 0, 9) == 0

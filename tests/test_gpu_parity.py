@@ -208,6 +208,31 @@ def test_max_kv_heads_full(dtype, q_dtype):
     assert hb.hpc_decode_read_error(res["plan"]) == 0
 
 
+def test_suggested_cta_count():
+    """One CTA per SM unless a CTA of that plan would hold 16 or more
+    descriptors; then the shallow instance's two per SM. The rule recomputed
+    here from the planner's bucket arithmetic, on the scope workloads."""
+    deep = hb.default_num_ctas(hb.KV_BF16)
+    shallow = 2 * hb.sm_count()
+    for name, expect in (("tiny", deep), ("uniform", deep), ("mixed", deep), ("skew", deep), ("short", shallow)):
+        w = wl.WORKLOADS[name]
+        assert hb.suggest_num_ctas(wl.draw_lengths(w), w.num_kv_heads) == expect, name
+    fp8 = wl.WORKLOADS["fp8"]
+    assert hb.suggest_num_ctas(wl.draw_lengths(fp8), 8, hb.KV_FP8_E4M3) == hb.default_num_ctas(hb.KV_FP8_E4M3)
+    mix = wl.table3_workload("32x0.125K+32x4K", 64, 8)
+    assert hb.suggest_num_ctas(wl.draw_lengths(mix), 8) == shallow
+    assert hb.suggest_num_ctas(wl.draw_lengths(mix), 8, q_len=2) == deep
+    assert hb.suggest_num_ctas(np.zeros(5, np.int32), 8) == deep
+    # the boundary: the first CTA holds the two-chunk requests and the start of
+    # the first long one, so 14 short requests make 15 descriptors there (one
+    # CTA per SM) and 15 make 16 (two per SM)
+    for n_short, expect in ((14, deep), (15, shallow)):
+        lens = [128] * n_short + [64 * 64 * 40] * 4
+        T = 2 * n_short + 4 * 64 * 40
+        assert (T + deep - 1) // deep > 2 * n_short  # all short requests in CTA 0, then a long one
+        assert hb.suggest_num_ctas(np.array(lens, np.int32), 1) == expect, n_short
+
+
 def test_all_lengths_zero():
     case = case_for([0, 0, 0], 1, seed=6, pool=4)
     res = _gpu.run(case, num_ctas=8)
@@ -460,7 +485,9 @@ def test_full_size_workload_every_row(name):
     case = wl.make_case(w, device=DEV)
     host = wl.to_numpy_case(case)
     rows = oracle.attn_rows(host)
-    C = hb.default_num_ctas(hb.kv_dtype_of(case["k_cache"]))
+    # the CTA count the library suggests for the batch (one per SM; two per SM,
+    # the shallow instance, for the batch of many short requests)
+    C = hb.suggest_num_ctas(case["seq_lens"], w.num_kv_heads, hb.kv_dtype_of(case["k_cache"]), w.min_chunks)
     res = _gpu.run(case, num_ctas=C, min_chunks=w.min_chunks)
     _gpu.check_plan_exact(res, case, min_chunks=w.min_chunks)
     _gpu.check_full(case, res, host=host, rows=rows, what=f"{name} balanced (C={C})")
