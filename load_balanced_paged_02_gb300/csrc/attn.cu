@@ -77,7 +77,7 @@ template <bool FP8, bool QF8>
 __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, int nv,
                                               const uint32_t (&qf)[8][2], const float (&qsc)[2],
                                               float (&o)[8][4], float (&m)[2], float (&l)[2],
-                                              float scale_log2) {
+                                              float scale_log2, int ks_off) {
     const int g = lane >> 2, c = lane & 3;
     const uint32_t sb = smem_u32(stage);
     float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -117,8 +117,8 @@ __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, 
             mma_bf16(o[i], a, pb0, pb1);
         }
     } else {
-        const float* ksc = reinterpret_cast<const float*>(stage + 16384);
-        const float* vsc = ksc + 64;
+        const float* ksc = reinterpret_cast<const float*>(stage + 16384) + ks_off;
+        const float* vsc = reinterpret_cast<const float*>(stage + 16384) + (kChunk - ks_off);
         const int r0 = 16 * wq + g;
         const uint32_t kb = sb;
         // ---- S^T: thread reads dims [32c, 32c+32) of token rows r0 and r0+8
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(Layout<FP8, STAGES, NG>::kThreads, 1)
                 const int nv = meta[st] - 16 * wq;
                 if (nv > 0)
                     chunk_compute<FP8, QF8>(smem + (size_t)st * Cfg::kStageBytes, wq, lane, nv < 16 ? nv : 16,
-                                            qf, qsc, o, m, l, p.scale_log2);
+                                            qf, qsc, o, m, l, p.scale_log2, p.ks_off);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
             }
@@ -416,6 +416,35 @@ bool make_scale_map(CUtensorMap* map, const float* base, int num_pages, int Hkv)
     return r == CUDA_SUCCESS;
 }
 
+// One 3-D map over both scale arrays: [2 arrays at their distance][num_pages *
+// Hkv rows][64 float32] from the lower array; box = one row of each (the lower
+// array's first), so a page's two 256-byte scale rows land with one copy.
+bool make_scale_maps(CUtensorMap* ks_map, CUtensorMap* vs_map, const float* k_scale, const float* v_scale,
+                     int num_pages, int Hkv, int* pair, int* ks_off) {
+    *pair = 0;
+    *ks_off = 0;
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const uintptr_t k = reinterpret_cast<uintptr_t>(k_scale), v = reinterpret_cast<uintptr_t>(v_scale);
+    const bool k_low = k < v;
+    const uintptr_t lo = k_low ? k : v, dist = k_low ? v - k : k - v;
+    if (dist > 0 && dist % 16 == 0 && dist < (1ull << 40)) {
+        cuuint64_t dims[3] = {(cuuint64_t)kChunk, (cuuint64_t)num_pages * Hkv, 2};
+        cuuint64_t strides[2] = {kChunk * sizeof(float), (cuuint64_t)dist};
+        cuuint32_t box[3] = {(cuuint32_t)kChunk, 1u, 2u};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (fn(ks_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, reinterpret_cast<void*>(lo), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+            memset(vs_map, 0, sizeof(CUtensorMap));
+            *pair = 1;
+            *ks_off = k_low ? 0 : kChunk;
+            return true;
+        }
+    }
+    return make_scale_map(ks_map, k_scale, num_pages, Hkv) && make_scale_map(vs_map, v_scale, num_pages, Hkv);
+}
+
 // 3-D map over a paged cache [num_pages*64 tokens][Hkv][128]; box = 64 tokens
 // x 1 head x (64 bf16 or 128 e4m3 = 128 bytes), 128-byte swizzle.
 bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int Hkv) {
@@ -506,12 +535,15 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t s) {
     if (!make_kv_map(&maps[0], a.k_cache, a.fp8, a.num_pages, a.num_kv_heads) ||
         !make_kv_map(&maps[1], a.v_cache, a.fp8, a.num_pages, a.num_kv_heads))
         return cudaErrorInvalidValue;
-    if (a.fp8 && (!make_scale_map(&maps[2], a.k_scale, a.num_pages, a.num_kv_heads) ||
-                  !make_scale_map(&maps[3], a.v_scale, a.num_pages, a.num_kv_heads)))
+    int pair = 0, ks_off = 0;
+    if (a.fp8 &&
+        !make_scale_maps(&maps[2], &maps[3], a.k_scale, a.v_scale, a.num_pages, a.num_kv_heads, &pair, &ks_off))
         return cudaErrorInvalidValue;
     const PlanLayout L = plan_layout(a.batch, a.num_kv_heads, a.num_ctas);
     Params p;
     memset(&p, 0, sizeof p);
+    p.scale_pair = pair;
+    p.ks_off = ks_off;
     p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     p.q8 = reinterpret_cast<const uint8_t*>(a.q);
     p.q_scale = a.q_scale;

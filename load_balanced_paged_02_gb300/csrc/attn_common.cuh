@@ -62,6 +62,14 @@ struct Params {
     // kTestWaitLimitNs, on a barrier that nothing completes, so the CTA takes
     // its timeout path
     int test_wait_expiry;
+    // e4m3: 1 when tm_ks is one 3-D map over both scale arrays (the lower
+    // array's row, then the upper's, at their fixed distance), so a page's two
+    // scale rows arrive in one copy; else two 2-D copies, K then V
+    int scale_pair;
+    // e4m3: where a stage's K scales sit among its two scale rows, in floats
+    // from the first (0, or 64 when the V array lies below the K array and the
+    // one copy lands V first); the V scales are in the other row
+    int ks_off;
 };
 
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
@@ -302,13 +310,17 @@ __device__ __forceinline__ void issue_chunk(const Params& p, const CUtensorMap* 
     mbar_arrive_expect_tx(full_st, Cfg::kTxBytes);
     const int tok = page * kChunk;
     if constexpr (FP8) {
-        // The 256-byte scale rows go through 2-D tensor maps: on GB300 that
+        // The 256-byte scale rows go through tensor maps (on GB300 that
         // measured 6 % faster for the whole kernel than plain bulk copies of
-        // the same rows. Issued first, so they are not the last bytes of the
-        // stage to land.
+        // the same rows), both rows in one copy when the arrays allow it.
+        // Issued first, so they are not the last bytes of the stage to land.
         const int srow = page * p.num_kv_heads + h;
-        tma_load_2d(sbuf + 16384, tm_ks, full_st, 0, srow, pol);
-        tma_load_2d(sbuf + 16640, tm_vs, full_st, 0, srow, pol);
+        if (p.scale_pair) {
+            tma_load_3d(sbuf + 16384, tm_ks, full_st, 0, srow, 0, pol);  // both rows, lower array first
+        } else {
+            tma_load_2d(sbuf + 16384, tm_ks, full_st, 0, srow, pol);
+            tma_load_2d(sbuf + 16640, tm_vs, full_st, 0, srow, pol);
+        }
         tma_load_3d(sbuf, tm_k, full_st, 0, h, tok, pol);
         tma_load_3d(sbuf + 8192, tm_v, full_st, 0, h, tok, pol);
     } else {
@@ -480,5 +492,12 @@ __device__ __forceinline__ void produce(const Params& p, const CUtensorMap* tm_k
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool make_kv_map(CUtensorMap* map, const void* base, int fp8, int num_pages, int Hkv);
 bool make_scale_map(CUtensorMap* map, const float* base, int num_pages, int Hkv);
+// The e4m3 scale maps of a launch: one 3-D map over both arrays, from the
+// lower one (*pair = 1, vs_map unused; *ks_off = 0 when the K array is the
+// lower, else 64), or one 2-D map each (*pair = 0, *ks_off = 0) when the
+// arrays' distance is not a multiple of 16 bytes below 2^40 or the 3-D map
+// cannot be encoded. False if a map cannot be encoded.
+bool make_scale_maps(CUtensorMap* ks_map, CUtensorMap* vs_map, const float* k_scale, const float* v_scale,
+                     int num_pages, int Hkv, int* pair, int* ks_off);
 
 }  // namespace hpc

@@ -80,7 +80,8 @@ struct MtLayout {
 template <bool FP8, int NTW, int MPW>
 __device__ __forceinline__ void chunk_compute_mt(uint8_t* stage, int lane, int mt0, int nv, int lim0, int ntl,
                                                  const uint32_t (&qf)[NTW][8][2], float (&o)[NTW][8][4],
-                                                 float (&m)[NTW][2], float (&l)[NTW][2], float scale_log2) {
+                                                 float (&m)[NTW][2], float (&l)[NTW][2], float scale_log2,
+                                                 int ks_off) {
     const int g = lane >> 2, c = lane & 3, rr = lane & 7;
     const uint32_t sb = smem_u32(stage);
     const int last_lim = lim0 + ntl - 1;  // the warp's widest causal limit
@@ -137,8 +138,8 @@ __device__ __forceinline__ void chunk_compute_mt(uint8_t* stage, int lane, int m
                     if (t < ntl) mma_bf16(o[t][i], a, pb[t][0], pb[t][1]);
             }
         } else {
-            const float* ksc = reinterpret_cast<const float*>(stage + 16384);
-            const float* vsc = ksc + 64;
+            const float* ksc = reinterpret_cast<const float*>(stage + 16384) + ks_off;
+            const float* vsc = reinterpret_cast<const float*>(stage + 16384) + (kChunk - ks_off);
             const int r0 = 16 * mt + g;
             {
                 // ---- S^T: thread reads dims [32c, 32c+32) of token rows r0, r0+8
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(MtLayout<FP8, NTW, QS, TS, NG, STAGES>::kThrea
                 const int lim0 = L - kChunk * cc - (Q - 1 - j0);
                 if (nv > 0 && ntl > 0)
                     chunk_compute_mt<FP8, NTW, MPW>(smem + (size_t)st * Cfg::kStageBytes, lane, ts * MPW, nv, lim0,
-                                                    ntl, qf, o, m, l, p.scale_log2);
+                                                    ntl, qf, o, m, l, p.scale_log2, p.ks_off);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
             }
@@ -584,12 +585,15 @@ cudaError_t launch_attn_mt(const AttnArgs& a, int q_len, cudaStream_t s) {
     if (!make_kv_map(&maps[0], a.k_cache, a.fp8, a.num_pages, a.num_kv_heads) ||
         !make_kv_map(&maps[1], a.v_cache, a.fp8, a.num_pages, a.num_kv_heads))
         return cudaErrorInvalidValue;
-    if (a.fp8 && (!make_scale_map(&maps[2], a.k_scale, a.num_pages, a.num_kv_heads) ||
-                  !make_scale_map(&maps[3], a.v_scale, a.num_pages, a.num_kv_heads)))
+    int pair = 0, ks_off = 0;
+    if (a.fp8 &&
+        !make_scale_maps(&maps[2], &maps[3], a.k_scale, a.v_scale, a.num_pages, a.num_kv_heads, &pair, &ks_off))
         return cudaErrorInvalidValue;
     const PlanLayout L = plan_layout(a.batch, a.num_kv_heads, a.num_ctas);
     Params p;
     memset(&p, 0, sizeof p);
+    p.scale_pair = pair;
+    p.ks_off = ks_off;
     p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     p.k_scale = a.k_scale;
     p.v_scale = a.v_scale;

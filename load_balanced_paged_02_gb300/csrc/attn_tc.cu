@@ -597,7 +597,7 @@ __global__ void __maxnreg__(168)
                 const int nv = meta[st];  // 0: page id out of range (nothing loaded)
                 if constexpr (FP8) {
                     // score column c times its K scale (tokens past nv are masked below)
-                    const float* ks = reinterpret_cast<const float*>(smem + (size_t)st * C::kStageBytes + 16384);
+                    const float* ks = reinterpret_cast<const float*>(smem + (size_t)st * C::kStageBytes + 16384) + p.ks_off;
 #pragma unroll
                     for (int m = 0; m < 8; ++m) {
                         const float2 f = *reinterpret_cast<const float2*>(ks + 8 * m + 2 * cq);
@@ -712,7 +712,8 @@ __global__ void __maxnreg__(168)
                     // minimum of four 16-byte bank-group passes. The slot was last read by
                     // the P . V of chunk k - 4, waited for above.
                     const uint8_t* sbv = smem + (size_t)st * C::kStageBytes + 8192;
-                    const float* vs = reinterpret_cast<const float*>(smem + (size_t)st * C::kStageBytes + 16640);
+                    const float* vs =
+                        reinterpret_cast<const float*>(smem + (size_t)st * C::kStageBytes + 16384) + (kChunk - p.ks_off);
                     uint8_t* ob = opbase + (size_t)(2 * g + pj) * C::kOpBytes;
 #pragma unroll
                     for (int rr = 0; rr < 2; ++rr) {
@@ -921,12 +922,15 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int q_len, cudaStream_t s) {
         !make_kv_map(&maps[1], a.v_cache, a.fp8, a.num_pages, a.num_kv_heads) ||
         !make_q_map(&maps[2], a.q, a.batch, q_len, a.num_q_heads))
         return cudaErrorInvalidValue;
-    if (a.fp8 && (!make_scale_map(&maps[3], a.k_scale, a.num_pages, a.num_kv_heads) ||
-                  !make_scale_map(&maps[4], a.v_scale, a.num_pages, a.num_kv_heads)))
+    int pair = 0, ks_off = 0;
+    if (a.fp8 &&
+        !make_scale_maps(&maps[3], &maps[4], a.k_scale, a.v_scale, a.num_pages, a.num_kv_heads, &pair, &ks_off))
         return cudaErrorInvalidValue;
     const PlanLayout L = plan_layout(a.batch, a.num_kv_heads, a.num_ctas);
     Params p;
     memset(&p, 0, sizeof p);
+    p.scale_pair = pair;
+    p.ks_off = ks_off;
     p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
     p.k_scale = a.k_scale;
     p.v_scale = a.v_scale;

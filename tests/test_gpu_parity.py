@@ -233,6 +233,40 @@ def test_suggested_cta_count():
         assert hb.suggest_num_ctas(np.array(lens, np.int32), 1) == expect, n_short
 
 
+@pytest.mark.parametrize("order", ["v_above_k", "k_above_v", "shared"])
+def test_e4m3_scale_rows_in_one_copy_or_two(order):
+    """The kernels fetch a page's two scale rows with one 3-D copy from the
+    lower of the two arrays (K first when the K array is the lower, V first
+    otherwise), and with two 2-D copies when both are one array (a caller
+    sharing the scales of K and V). Each layout, every row and split against
+    the oracle, on the one-token kernel and both multi-token kernels."""
+    from dataclasses import replace
+    lens = [1, 63, 64, 65, 127, 200, 0, 333, 1000, 4097]
+    for q_len, engine in ((1, None), (2, hb.ENGINE_MMA_SYNC), (3, hb.ENGINE_TCGEN05)):
+        w = wl.Workload("scales", len(lens), 16, 2, "fp8", 95 + q_len, lens=lens, q_len=q_len)
+        case = wl.make_case(w, device=DEV)
+        ks, vs = case["k_scale"], case["v_scale"]
+        n = ks.numel()
+        buf = torch.full((2 * n + 64,), float("nan"), dtype=torch.float32, device=DEV)
+        lo, hi = buf[:n].view(ks.shape), buf[n + 64:].view(vs.shape)  # 256 bytes apart
+        if order == "v_above_k":
+            lo.copy_(ks)
+            hi.copy_(vs)
+            case = dict(case, k_scale=lo, v_scale=hi)
+        elif order == "k_above_v":
+            lo.copy_(vs)
+            hi.copy_(ks)
+            case = dict(case, k_scale=hi, v_scale=lo)
+        else:
+            lo.copy_(ks)
+            case = dict(case, k_scale=lo, v_scale=lo)
+        for C in (7, 40):
+            res = _gpu.run(case, num_ctas=C, min_chunks=1, engine=engine)
+            _gpu.check_plan_exact(res, case, min_chunks=1)
+            _gpu.check_full(case, res, what=f"{order} q_len {q_len} C={C}")
+            assert hb.hpc_decode_read_error(res["plan"]) == 0
+
+
 def test_all_lengths_zero():
     case = case_for([0, 0, 0], 1, seed=6, pool=4)
     res = _gpu.run(case, num_ctas=8)
