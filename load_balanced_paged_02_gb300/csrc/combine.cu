@@ -9,6 +9,9 @@
 //    lane k owning dims [4k, 4k+4); the weights of a tile of splits are staged
 //    in shared memory and eight partial rows per lane are loaded before they
 //    are accumulated (a long request can leave a pair with ~100 partials);
+//    grids of at most one wave of blocks, whose time is their slowest row,
+//    load a row's first 128 LSEs once for its max and its weights and its
+//    partials sixteen at a time, the last batch predicated;
 //  - pairs: one warp per (KV-head pair, new token): the 8 query heads of the
 //    pair share its split range, so one lookup of (n, s0) serves 8 rows and
 //    each split contributes 8 independent row loads per lane.
@@ -26,7 +29,9 @@ namespace {
 constexpr int kCombineWarps = 8;
 constexpr int kWTile = 64;     // pair form: splits whose 8 weights are staged per warp at a time
 constexpr int kRowTile = 256;  // row form: split weights staged per warp at a time
-constexpr int kUnroll = 8;     // row form: split rows in flight per lane
+constexpr int kUnrollShort = 8;  // row form, many rows: split rows in flight per lane
+constexpr int kUnrollLong = 16;  // row form, few rows: split rows in flight per lane (last batch predicated)
+constexpr int kLsePerLane = 4;   // row form, few rows: LSEs a lane keeps from the max pass for the weights
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -176,6 +181,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, 2)
     }
 }
 
+template <bool LONG>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     combine_rows_kernel(const int32_t* __restrict__ pair_nsplit, const int32_t* __restrict__ pair_split0,
                    const float* __restrict__ split_o, const float* __restrict__ split_lse,
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
     if (n == 1) {
         acc = *reinterpret_cast<const float4*>(split_o + (s0 * rs + j) * kHeadDim + 4 * lane);
         lse = split_lse[s0 * rs + j];
-    } else if (n > 1) {
+    } else if (n > 1 && !LONG) {
         float M = -INFINITY;
         for (int i = lane; i < n; i += 32) M = fmaxf(M, split_lse[(s0 + i) * rs + j]);
         M = warp_max(M);
@@ -218,16 +224,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                     wpart += w;
                 }
                 __syncwarp();
-                // weighted rows, kUnroll independent loads in flight per lane
+                // weighted rows, kUnrollShort independent loads in flight per lane
                 const float* base = split_o + ((s0 + t0) * rs + j) * kHeadDim + 4 * lane;
                 int i = 0;
-                for (; i + kUnroll <= tn; i += kUnroll) {
-                    float4 x[kUnroll];
+                for (; i + kUnrollShort <= tn; i += kUnrollShort) {
+                    float4 x[kUnrollShort];
 #pragma unroll
-                    for (int u = 0; u < kUnroll; ++u)
+                    for (int u = 0; u < kUnrollShort; ++u)
                         x[u] = *reinterpret_cast<const float4*>(base + (long long)(i + u) * rs * kHeadDim);
 #pragma unroll
-                    for (int u = 0; u < kUnroll; ++u) {
+                    for (int u = 0; u < kUnrollShort; ++u) {
                         const float w = wsh[warp][i + u];
                         acc.x += w * x[u].x;
                         acc.y += w * x[u].y;
@@ -242,6 +248,67 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
                     acc.y += w * x.y;
                     acc.z += w * x.z;
                     acc.w += w * x.w;
+                }
+                __syncwarp();
+            }
+            const float wsum = warp_sum(wpart);
+            const float inv = 1.f / wsum;
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
+            lse = M + log2f(wsum) * kLn2;
+        }
+    } else if (n > 1) {
+        // the LSEs of the first 32 * kLsePerLane splits load once, all at a time,
+        // and serve both the max and the weights
+        float lv[kLsePerLane];
+#pragma unroll
+        for (int t = 0; t < kLsePerLane; ++t) {
+            const int i = lane + 32 * t;
+            lv[t] = i < n ? split_lse[(s0 + i) * rs + j] : -INFINITY;
+        }
+        float M = lv[0];
+#pragma unroll
+        for (int t = 1; t < kLsePerLane; ++t) M = fmaxf(M, lv[t]);
+        for (int i = lane + 32 * kLsePerLane; i < n; i += 32) M = fmaxf(M, split_lse[(s0 + i) * rs + j]);
+        M = warp_max(M);
+        if (M != -INFINITY) {
+            float wpart = 0.f;
+            for (int t0 = 0; t0 < n; t0 += kRowTile) {
+                const int tn = min(kRowTile, n - t0);
+                // weights of this tile, one per lane-strided split
+                for (int i = lane, t = 0; i < tn; i += 32, ++t) {
+                    float l = 0.f;
+                    if (t0 == 0 && t < kLsePerLane) {
+#pragma unroll
+                        for (int k = 0; k < kLsePerLane; ++k) l = t == k ? lv[k] : l;
+                    } else {
+                        l = split_lse[(s0 + t0 + i) * rs + j];
+                    }
+                    const float w = exp2f((l - M) * kLog2e);
+                    wsh[warp][i] = w;
+                    wpart += w;
+                }
+                __syncwarp();
+                // weighted rows, kUnrollLong independent loads in flight per lane; the
+                // last batch loads only the splits that exist
+                const float* base = split_o + ((s0 + t0) * rs + j) * kHeadDim + 4 * lane;
+                for (int i = 0; i < tn; i += kUnrollLong) {
+                    float4 x[kUnrollLong];
+#pragma unroll
+                    for (int u = 0; u < kUnrollLong; ++u)
+                        x[u] = i + u < tn ? *reinterpret_cast<const float4*>(base + (long long)(i + u) * rs * kHeadDim)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < kUnrollLong; ++u) {
+                        if (i + u >= tn) break;
+                        const float w = wsh[warp][i + u];
+                        acc.x += w * x[u].x;
+                        acc.y += w * x[u].y;
+                        acc.z += w * x[u].z;
+                        acc.w += w * x[u].w;
+                    }
                 }
                 __syncwarp();
             }
@@ -284,7 +351,14 @@ cudaError_t launch_combine(const int32_t* plan, int C, const float* split_o, con
     }
     const long long rows = tasks * kGroup;
     const long long blocks = (rows + kCombineWarps - 1) / kCombineWarps;
-    return launch_pdl(combine_rows_kernel, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+    // At most one wave of blocks (2 per SM at the long form's registers): the
+    // grid's latency is its slowest row, a pair with many partials, so rows
+    // load their LSEs once and their partials 16 at a time. More blocks: the
+    // lighter form keeps more of them resident.
+    if (blocks <= full_wave / kCombineWarps)
+        return launch_pdl(combine_rows_kernel<true>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+                          plan + L.pair_nsplit, plan + L.pair_split0, split_o, split_lse, out, out_lse, B, Hq, q_len);
+    return launch_pdl(combine_rows_kernel<false>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
                       plan + L.pair_nsplit, plan + L.pair_split0, split_o, split_lse, out, out_lse, B, Hq, q_len);
 }
 

@@ -267,6 +267,22 @@ def test_e4m3_scale_rows_in_one_copy_or_two(order):
             assert hb.hpc_decode_read_error(res["plan"]) == 0
 
 
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_combine_rows_with_hundreds_of_partials(q_len):
+    """A request split into 300 partials (600 chunks on a map for 600 CTAs):
+    the row combine of small grids keeps the first 128 LSEs of a row in
+    registers and walks its partials in tiles of 256, sixteen at a time; every
+    row and split against the oracle."""
+    lens = [38400, 5000, 1, 0]
+    w = wl.Workload("longpair", len(lens), 8, 1, "bf16", 96 + q_len, lens=lens, q_len=q_len)
+    case = wl.make_case(w, device=DEV)
+    res = _gpu.run(case, num_ctas=600, min_chunks=1)
+    _gpu.check_plan_exact(res, case, min_chunks=1)
+    parsed = oracle.parse_plan(res["plan"].buf.cpu().numpy())
+    assert int(parsed["pair_nsplit"].max()) == 300
+    _gpu.check_full(case, res, what=f"300 partials, q_len {q_len}")
+
+
 def test_all_lengths_zero():
     case = case_for([0, 0, 0], 1, seed=6, pool=4)
     res = _gpu.run(case, num_ctas=8)
