@@ -148,11 +148,11 @@ int hpc_decode_default_num_ctas(int kv_dtype);
  * [batch], host memory; nothing is enqueued). The pages leave the CTA count to
  * the caller ([SGL] "Scheduling around live KV work": the planner divides the
  * work by the number of CTAs). The rule: plan the batch for
- * hpc_decode_default_num_ctas(kv_dtype) CTAs (one per SM); if some CTA of that
- * plan would hold 16 or more descriptors (a batch of many short requests, each
- * descriptor paying a fixed cost beyond its chunks), return the count of the
- * shallow instance instead (two CTAs per SM), which halves such lists;
- * otherwise the default count. With several new tokens per request (q_len >
+ * hpc_decode_default_num_ctas(kv_dtype) CTAs (one per SM); if the CTA of that
+ * plan with the most descriptors holds at least 4 of them and at least 0.15
+ * per chunk of its budget (each descriptor costs a fixed amount beyond its
+ * chunks, a sizable share there), return the count of the shallow instance
+ * (two CTAs per SM), which halves such lists; otherwise the default count. With several new tokens per request (q_len >
  * 1) the default count. Any count gives the same outputs up to rounding; the
  * task map for each count is exact. Returns 0 for bad arguments or when the
  * device cannot be queried.

@@ -16,12 +16,18 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// hpc_decode_suggest_num_ctas: the most descriptors one CTA of the one-per-SM plan
-// may hold before two CTAs per SM are suggested. On GB300 (bf16, 64/8 heads)
-// 1024 requests of 128 tokens (54 descriptors per CTA) and the 32 x 128 + 32 x
-// 4096 mix (56 in its first CTAs) ran faster on 304 CTAs; batches whose CTAs
-// hold a few descriptors each ran faster on 152.
-constexpr int kManyDescriptorsPerCta = 16;
+// hpc_decode_suggest_num_ctas: two CTAs per SM when some CTA of the one-per-SM
+// plan holds at least kFewDescriptors descriptors and at least
+// kDescriptorsPerChunkPct descriptors per hundred chunks of its budget, i.e.
+// when fixed per-descriptor costs are a sizable share of that CTA's work. On
+// GB300 every batch measured followed the rule (step time planned for 152 and
+// for 304 CTAs): 1024 x 128 tokens (54 descriptors in 108 chunks), the
+// decode-latency table's 32 x 128 + 32 x 4096 mix at 8/1 (7 in 14) and 64/8
+// heads (34 in 112) and its 64 x 512 mix at 64/8 (5 in 27) ran faster on 304;
+// the mixed-length (12 in 491), e4m3 (13 in 3195) and skewed (10 in 134)
+// batches and the table's other mixes ran faster, or the same, on 152.
+constexpr int kFewDescriptors = 4;
+constexpr int kDescriptorsPerChunkPct = 15;
 
 bool sizes_ok(int batch, int num_kv_heads, long long num_ctas) {
     return batch >= 1 && batch <= HPC_MAX_BATCH && num_kv_heads >= 1 &&
@@ -133,12 +139,12 @@ int hpc_decode_suggest_num_ctas(const int32_t* h_seq_lens, int batch, int num_kv
             g0 += n;
         }
     }
-    // A CTA whose list holds many descriptors pays a fixed cost for each (query
-    // staging, the merge of its warps' states, the partial's write) on top of
-    // its share of the stream; two CTAs per SM halve such lists and overlap one
-    // CTA's merges with the other's loads. Batches of a few long requests keep
-    // one CTA per SM: more CTAs only add partials to combine.
-    if (most < kManyDescriptorsPerCta) return deep;
+    // Each descriptor costs its CTA a fixed amount (query staging, the merge of
+    // its warps' states, the partial's write) on top of its chunks; where that
+    // is a sizable share of the busiest CTA's work, two CTAs per SM halve the
+    // lists and overlap one CTA's merges with the other's loads. Otherwise one
+    // CTA per SM: more CTAs only add partials to combine.
+    if (most < kFewDescriptors || 100LL * most < (long long)kDescriptorsPerChunkPct * bucket) return deep;
     const int shallow = attn_shallow_ctas(fp8);
     return shallow > deep ? shallow : deep;
 }

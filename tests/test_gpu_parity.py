@@ -209,27 +209,34 @@ def test_max_kv_heads_full(dtype, q_dtype):
 
 
 def test_suggested_cta_count():
-    """One CTA per SM unless a CTA of that plan would hold 16 or more
-    descriptors; then the shallow instance's two per SM. The rule recomputed
-    here from the planner's bucket arithmetic, on the scope workloads."""
+    """One CTA per SM unless the busiest CTA of that plan holds at least 4
+    descriptors and at least 0.15 per chunk of its budget; then the shallow
+    instance's two per SM. Checked on the scope workloads and the Table 3
+    mixes, whose measured step times the rule follows."""
     deep = hb.default_num_ctas(hb.KV_BF16)
+    deep8 = hb.default_num_ctas(hb.KV_FP8_E4M3)
     shallow = 2 * hb.sm_count()
     for name, expect in (("tiny", deep), ("uniform", deep), ("mixed", deep), ("skew", deep), ("short", shallow)):
         w = wl.WORKLOADS[name]
         assert hb.suggest_num_ctas(wl.draw_lengths(w), w.num_kv_heads) == expect, name
     fp8 = wl.WORKLOADS["fp8"]
-    assert hb.suggest_num_ctas(wl.draw_lengths(fp8), 8, hb.KV_FP8_E4M3) == hb.default_num_ctas(hb.KV_FP8_E4M3)
+    assert hb.suggest_num_ctas(wl.draw_lengths(fp8), 8, hb.KV_FP8_E4M3) == deep8
+    for mix, shape, expect in (("32x0.125K+32x4K", (64, 8), shallow), ("32x0.125K+32x4K", (8, 1), shallow),
+                               ("64x0.5K", (64, 8), shallow), ("64x0.5K", (8, 1), deep8), ("64x4K", (64, 8), deep8),
+                               ("1x128K+31x4K", (8, 1), deep8), ("2x32K+30x4K", (64, 8), deep8)):
+        w = wl.table3_workload(mix, *shape)
+        got = hb.suggest_num_ctas(wl.draw_lengths(w), w.num_kv_heads, hb.KV_FP8_E4M3)
+        assert got == (2 * hb.sm_count() if expect == shallow else expect), (mix, shape)
     mix = wl.table3_workload("32x0.125K+32x4K", 64, 8)
-    assert hb.suggest_num_ctas(wl.draw_lengths(mix), 8) == shallow
     assert hb.suggest_num_ctas(wl.draw_lengths(mix), 8, q_len=2) == deep
     assert hb.suggest_num_ctas(np.zeros(5, np.int32), 8) == deep
-    # the boundary: the first CTA holds the two-chunk requests and the start of
-    # the first long one, so 14 short requests make 15 descriptors there (one
-    # CTA per SM) and 15 make 16 (two per SM)
-    for n_short, expect in ((14, deep), (15, shallow)):
+    # the boundary: the first CTA (budget 68 chunks) holds the two-chunk requests
+    # and the start of the first long one; 9 short requests make 10 descriptors
+    # there (10 < 0.15 x 68), 10 make 11
+    for n_short, expect in ((9, deep), (10, shallow)):
         lens = [128] * n_short + [64 * 64 * 40] * 4
         T = 2 * n_short + 4 * 64 * 40
-        assert (T + deep - 1) // deep > 2 * n_short  # all short requests in CTA 0, then a long one
+        assert (T + deep - 1) // deep == 68
         assert hb.suggest_num_ctas(np.array(lens, np.int32), 1) == expect, n_short
 
 
