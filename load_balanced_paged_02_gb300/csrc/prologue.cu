@@ -24,6 +24,7 @@
 // four xor-shuffle steps inside the half-warp. Row kinds (query, key, value)
 // are per-lane predicates, so all lanes run every shuffle.
 #include <algorithm>
+#include <atomic>
 
 #include "hpc_internal.cuh"
 
@@ -584,13 +585,10 @@ cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s) {
     p.err = a.err;
     if (a.num_tokens == 0) return cudaSuccess;
     const int H3 = a.num_q_heads + 2 * a.num_kv_heads;
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-            sms = n;
-    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        sms = 0;
     // Prefill-sized calls whose tokens fit the ring's stages: the persistent
     // ring kernel, when there are at least two stages per SM.
     if (H3 <= ring::kStageRows && sms > 0) {
@@ -601,12 +599,15 @@ cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s) {
         rp.num_stages = (a.num_tokens + rp.G - 1) / rp.G;
         rp.h3_magic = (uint32_t)((0x100000000ull + H3 - 1) / H3);
         if (rp.num_stages >= 2 * sms) {
-            static bool attr_set = false;
-            if (!attr_set) {
+            // the shared-memory opt-in, once per device (the launch path then makes
+            // no extra runtime calls, which keeps it capturable)
+            static std::atomic<unsigned long long> attr_set{0};
+            const unsigned long long bit = 1ull << (dev & 63);
+            if (!(attr_set.load(std::memory_order_acquire) & bit)) {
                 cudaError_t e = cudaFuncSetAttribute(ring::rope_norm_ring_kernel,
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, ring::kSmemBytes);
                 if (e != cudaSuccess) return e;
-                attr_set = true;
+                attr_set.fetch_or(bit, std::memory_order_acq_rel);
             }
             const int grid = std::min(rp.num_stages, sms);
             return launch_pdl(ring::rope_norm_ring_kernel, dim3(grid), dim3(ring::kThreads), ring::kSmemBytes, s, rp);
