@@ -245,10 +245,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
 // is one contiguous run of H3 rows of 256 bytes, so a stage holds G whole
 // tokens (G * H3 <= 160 rows) and arrives with one bulk copy, plus each
 // token's 512-byte rotary row. One CTA per SM: a producer warp streams the
-// stages of its tokens into a 4-deep ring; 24 consumer warps process them.
+// stages of its tokens into a 4-deep ring; 24 consumer warps (22 when the
+// query is written as e4m3) process them.
 // A consumer quarter-warp owns one row (lane k of it: dims [8k, 8k+8) and
 // their rotation partners [64+8k, 64+8k+8)); a warp takes units of 4 rows,
-// unit u of the CTA's i-th stage going to warp (i * units + u) mod 24, so the
+// unit u of the CTA's i-th stage going to warp (i * units + u) mod warps, so the
 // warps share the rows evenly over the stages. Reductions take three xor
 // shuffles inside the quarter-warp. Bound: instruction issue and latency (ncu
 // on the 16-warp version: issue slots 60 % busy, short-scoreboard stalls
@@ -265,11 +266,19 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, MINB) rope_norm_kernel(co
 // (Markstein's correction step, see rope_norm_kernel).
 namespace ring {
 
-// 24 consumer warps (six per sub-partition): on GB300 an 8192-token prefill at
-// 64/8 heads with e4m3 outputs took 63.1 us with 16, 58.6 with 24 and 58.6
-// with 28 (bf16 outputs: 56.7, 55.7, 56.0 us).
-constexpr int kConsumerWarps = 24;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// Two instances. Calls that write a bf16 query: 24 consumer warps (on GB300
+// an 8192-token prefill at 64/8 heads with bf16 outputs took 56.7 us with 16,
+// 55.7 with 24, 56.0 with 28). Calls that write an e4m3 query: each lane keeps
+// its 16 query norm weights in registers instead of loading them from shared
+// memory for every query row (each row needs 128 bytes per lane of weights and
+// rotary terms, four times its own data, and shared-memory wavefronts bound the
+// e4m3 instance), which leaves room for 22 warps without spills: 59.0 -> 56.5
+// us (e4m3 outputs; the bf16 instance lost 1.7 us with the same change).
+template <bool QW>
+struct RingCfg {
+    static constexpr int kConsumerWarps = QW ? 22 : 24;
+    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+};
 constexpr int kStages = 4;
 constexpr int kStageRows = 160;   // QKV rows per stage at most
 constexpr int kStageTokens = 16;  // tokens per stage at most
@@ -353,7 +362,9 @@ __device__ __forceinline__ uint2 e4m3x8(const float* v) {
     return make_uint2(w[0], w[1]);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) rope_norm_ring_kernel(const RingParams rp) {
+template <bool QW>
+__global__ void __launch_bounds__(RingCfg<QW>::kThreads, 1) rope_norm_ring_kernel(const RingParams rp) {
+    constexpr int kConsumerWarps = RingCfg<QW>::kConsumerWarps;
     const PrologueParams& p = rp.p;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
@@ -369,14 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1) rope_norm_ring_kernel(const RingP
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // the norm weights do not come from the preceding kernel
-    if (threadIdx.x < 2 * kHeadDim / 4) {
+    grid_dependency_wait();  // the QKV projection (and any input) may still be finishing
+    grid_launch_dependents();
+    if (threadIdx.x < 2 * kHeadDim / 4) {  // the norm weights, into shared memory
         const float* src = threadIdx.x < kHeadDim / 4 ? p.qw + 4 * threadIdx.x : p.kw + 4 * (threadIdx.x - 32);
         *reinterpret_cast<float4*>(wsm + 4 * threadIdx.x) = __ldg(reinterpret_cast<const float4*>(src));
     }
     __syncthreads();
-    grid_dependency_wait();  // the QKV projection may still be finishing
-    grid_launch_dependents();
     const int H3 = rp.H3, G = rp.G;
     const int rows_per_stage = G * H3;
     const int units = (rows_per_stage + 3) >> 2;
@@ -444,6 +454,15 @@ __global__ void __launch_bounds__(kThreads, 1) rope_norm_ring_kernel(const RingP
     const int q = lane >> 3, hl = lane & 7;
     const uint32_t qmask = 0xffu << (lane & 24);
     const bool q_fp8 = p.q_scale != nullptr, kv_fp8 = p.kv_fp8 != 0;
+    float wq[16];
+    if constexpr (QW) {
+        const uint32_t wb = smem_u32(wsm + 8 * hl);
+        const float4 w0 = lds_f4(wb), w1 = lds_f4(wb + 16), w2 = lds_f4(wb + 256), w3 = lds_f4(wb + 272);
+        const float ww[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                              w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) wq[e] = ww[e];
+    }
     uint32_t i = 0;
     for (int k = blockIdx.x; k < rp.num_stages; k += gridDim.x, ++i) {
         const int st = (int)(i % kStages);
@@ -482,11 +501,16 @@ __global__ void __launch_bounds__(kThreads, 1) rope_norm_ring_kernel(const RingP
                 for (int e = 0; e < 16; ++e) s2 = fmaf(y[e], y[e], s2);
                 s2 = quarter_sum(s2, qmask);
                 inv = rsqrtf(s2 * (1.f / kHeadDim) + p.eps);
-                const float4 w0 = lds_f4(wb), w1 = lds_f4(wb + 16), w2 = lds_f4(wb + 256), w3 = lds_f4(wb + 272);
-                const float ww[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                                      w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+                if (QW && is_q) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) y[e] *= ww[e];
+                    for (int e = 0; e < 16; ++e) y[e] *= wq[e];
+                } else {
+                    const float4 w0 = lds_f4(wb), w1 = lds_f4(wb + 16), w2 = lds_f4(wb + 256), w3 = lds_f4(wb + 272);
+                    const float ww[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                                          w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) y[e] *= ww[e];
+                }
                 if (meta.x >= 0) {
                     // rotary pairs (i, i + 64), both in this lane: y[e] and y[e + 8]
                     const float4 c0 = lds_f4(cb), c1 = lds_f4(cb + 16), s0 = lds_f4(cb + 256), s1 = lds_f4(cb + 272);
@@ -604,13 +628,20 @@ cudaError_t launch_rope_norm(const RopeNormArgs& a, cudaStream_t s) {
             static std::atomic<unsigned long long> attr_set{0};
             const unsigned long long bit = 1ull << (dev & 63);
             if (!(attr_set.load(std::memory_order_acquire) & bit)) {
-                cudaError_t e = cudaFuncSetAttribute(ring::rope_norm_ring_kernel,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, ring::kSmemBytes);
-                if (e != cudaSuccess) return e;
+                for (const void* fn : {(const void*)ring::rope_norm_ring_kernel<false>,
+                                       (const void*)ring::rope_norm_ring_kernel<true>}) {
+                    cudaError_t e =
+                        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ring::kSmemBytes);
+                    if (e != cudaSuccess) return e;
+                }
                 attr_set.fetch_or(bit, std::memory_order_acq_rel);
             }
             const int grid = std::min(rp.num_stages, sms);
-            return launch_pdl(ring::rope_norm_ring_kernel, dim3(grid), dim3(ring::kThreads), ring::kSmemBytes, s, rp);
+            if (a.q_scale)
+                return launch_pdl(ring::rope_norm_ring_kernel<true>, dim3(grid), dim3(ring::RingCfg<true>::kThreads),
+                                  ring::kSmemBytes, s, rp);
+            return launch_pdl(ring::rope_norm_ring_kernel<false>, dim3(grid), dim3(ring::RingCfg<false>::kThreads),
+                              ring::kSmemBytes, s, rp);
         }
     }
     // Few tokens (decode): one round of 16 rows per block, so that a token's
