@@ -1,4 +1,6 @@
-// Task-map planners (one block, integer only).
+// Task-map planners (integer only). The balanced map's planner runs over
+// several blocks when the batch has many (kv head, request) pairs; the static
+// map's planner is one block.
 //
 // Load-balanced map: HPC-Ops/SGLang blog, "Scheduling around live KV work";
 // vLLM x HPC-Ops blog, "解决方案：按步负载均衡的 decode 调度器" (assign stage).
@@ -18,6 +20,9 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanWarps = kPlanThreads / 32;
+// Blocks of the balanced planner: one per 1024 pairs, at most this many (each
+// block then takes several 1024-pair tiles).
+constexpr int kPlanMaxBlocks = 64;
 
 // Exclusive scan of one value per thread across the block. All threads must
 // call it. Returns the exclusive prefix; *total receives the block sum.
@@ -53,9 +58,9 @@ __device__ V block_exclusive_scan(V v, V* total, V* warp_sums) {
 // integers using multiplication", PLDI 1994, section 4): with l = ceil(log2 d)
 // and m = floor(2^32 (2^l - d) / d) + 1, the quotient is
 // (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0), t = high half of m * n, for
-// 1 <= d < 2^32 and every 32-bit n. The planner is one block and bound by
-// instruction issue and latency; hardware-sequence divisions by the bucket and
-// the batch for every pair cost about a tenth of its time.
+// 1 <= d < 2^32 and every 32-bit n. A planner block is bound by instruction
+// issue and latency; hardware-sequence divisions by the bucket and the batch
+// for every pair cost about a tenth of its time.
 struct FastDiv {
     uint32_t m;
     int s1, s2;
@@ -165,38 +170,51 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
 
     // Chunk indices stay below T <= INT32_MAX (checked in chunk_prefix), and so do
     // split and task-row indices (P + 2C rows), so the per-pair work runs in 32-bit
-    // unsigned arithmetic: the planner is one block and bound by instruction issue.
+    // unsigned arithmetic (each block is bound by instruction issue and latency).
     // A CTA range ends below T + bucket < 2^32.
     const unsigned ubucket = (unsigned)bucket, uB = (unsigned)B, uN = (unsigned)N, uT = (unsigned)T;
     const FastDiv by_bucket(ubucket), by_batch(uB);
     const int Pi = (int)P;  // P <= HPC_MAX_CTAS
 
-    // split count of every (kv head, request) pair, then its first split index
+    // Block k takes pairs [p_lo, p_hi), a whole number of 1024-pair tiles; every
+    // block computes the same chunk prefixes, bucket and error bits itself, and
+    // starts its split indices at the number of descriptors of all earlier pairs,
+    // which it sums in closed form (no block waits for another).
+    const int per_block = (int)(((P + kPlanThreads - 1) / kPlanThreads + gridDim.x - 1) / gridDim.x) * kPlanThreads;
+    const int p_lo = min(Pi, (int)blockIdx.x * per_block), p_hi = min(Pi, p_lo + per_block);
+    auto pair_splits = [&](int p) -> unsigned {
+        const unsigned h = by_batch.div((unsigned)p), b = (unsigned)p - h * uB;
+        const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
+        const unsigned g0 = h * uN + (unsigned)pre[b];
+        return nb ? by_bucket.div(g0 + nb - 1) - by_bucket.div(g0) + 1 : 0u;
+    };
     unsigned running = 0;
-    for (int base = 0; base < Pi; base += kPlanThreads) {
+    {
+        unsigned acc = 0;
+        for (int p = tid; p < p_lo; p += kPlanThreads) acc += pair_splits(p);
+        unsigned tot;
+        (void)block_exclusive_scan<unsigned>(acc, &tot, warp_sums32);
+        running = tot;
+    }
+
+    // split count of each of the block's pairs, then its first split index
+    for (int base = p_lo; base < p_hi; base += kPlanThreads) {
         const int p = base + tid;
-        unsigned ns = 0;
-        if (p < Pi) {
-            const unsigned h = by_batch.div((unsigned)p), b = (unsigned)p - h * uB;
-            const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
-            const unsigned g0 = h * uN + (unsigned)pre[b];
-            ns = nb ? by_bucket.div(g0 + nb - 1) - by_bucket.div(g0) + 1 : 0;
-        }
+        const unsigned ns = p < p_hi ? pair_splits(p) : 0u;
         unsigned tot;
         const unsigned ex = block_exclusive_scan<unsigned>(ns, &tot, warp_sums32);
-        if (p < Pi) {
+        if (p < p_hi) {
             nsplit[p] = (int32_t)ns;
             split0[p] = (int32_t)(running + ex);
         }
         running += tot;
     }
-    const long long total = running;
 
     // Descriptors, by the thread that scanned the pair (its split0 write is its own).
     // Descriptor k of a pair lies in CTA first + k; the one that reaches the end of
     // its CTA's range [cta*bucket, min((cta+1)*bucket, T)) is the CTA's last, and the
     // CTA's terminator row follows it.
-    for (int p = tid; p < Pi; p += kPlanThreads) {
+    for (int p = p_lo + tid; p < p_hi; p += kPlanThreads) {
         const unsigned h = by_batch.div((unsigned)p), b = (unsigned)p - h * uB;
         const unsigned nb = (unsigned)(pre[b + 1] - pre[b]);
         if (!nb) continue;
@@ -216,6 +234,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1)
             if (ce == hi || ce == uT) write_term(row + kTaskInts);
         }
     }
+    // the last block, whose running count is now every pair's, fills the rest
+    if (blockIdx.x != gridDim.x - 1) return;
+    const long long total = running;
 
     // unused CTAs: an empty task list each, then terminators up to the row capacity
     for (long long j = used + tid; j <= C; j += kPlanThreads) cta_off[j] = (int32_t)(total + j);
@@ -312,7 +333,9 @@ cudaError_t launch_plan(const int32_t* seq_lens, int B, int Hkv, int C, int m, i
     const size_t smem = sizeof(int32_t) * ((size_t)B + 1);
     cudaError_t e = set_smem((const void*)plan_balanced_kernel, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(plan_balanced_kernel, dim3(1), dim3(kPlanThreads), smem, s, seq_lens, B, Hkv, C, m, buf);
+    const long long tiles = ((long long)Hkv * B + kPlanThreads - 1) / kPlanThreads;
+    const int blocks = (int)(tiles < kPlanMaxBlocks ? tiles : kPlanMaxBlocks);
+    return launch_pdl(plan_balanced_kernel, dim3(blocks), dim3(kPlanThreads), smem, s, seq_lens, B, Hkv, C, m, buf);
 }
 
 cudaError_t launch_plan_static(const int32_t* seq_lens, int B, int Hkv, int S, int32_t* buf,

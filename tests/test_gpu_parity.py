@@ -61,9 +61,18 @@ def test_plan_bit_exact_random_and_edges():
     for B in (2, 3, 4, 5, 127, 128, 129, 1023, 1024, 1025):
         for C, m in ((1, 0), (B, 0), (3 * B + 1, 1), (256, 4)):
             cases.append((rng.integers(0, 5000, size=B).tolist(), int(rng.integers(1, 9)), C, m))
-    # more than 1024 requests / pairs: several scan tiles in the planner
+    # more than 1024 requests / pairs: several scan tiles, over several planner
+    # blocks (one per 1024 pairs, at most 64)
     cases.append((rng.integers(0, 3000, size=3000).tolist(), 8, 304, 2))
     cases.append((rng.integers(0, 300, size=HB_MAX_B).tolist(), 1, 1000, 1))
+    # 65 tiles: 64 blocks of two tiles each, the last 31 blocks without pairs
+    cases.append((rng.integers(0, 400, size=8320).tolist(), 8, 152, 2))
+    # 128 tiles, two per block, and a bucket well above one chunk
+    cases.append((rng.integers(0, 200, size=HB_MAX_B).tolist(), 8, 1000, 2))
+    # empty requests at block edges: pairs 1023 / 1024 / 2047 / 2048 have no chunks
+    edge = rng.integers(1, 900, size=4096)
+    edge[[1023, 1024, 2047, 2048, 4095]] = 0
+    cases.append((edge.tolist(), 1, 152, 2))
     for lens, hkv, C, m in cases:
         sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
         plan = hb.hpc_decode_plan(sl, hkv, C, m)
