@@ -343,6 +343,24 @@ __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float (
     }
 }
 
+// Packed single precision (two float32 per 64-bit register, one issue slot for
+// both; each half rounds as the scalar instruction would): r = a * b and
+// r = a * b + c on the pairs (a0, a1), (b0, b1), (c0, c1).
+__device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     const uint4 v = lds128(addr);
     return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
@@ -497,30 +515,57 @@ __global__ void __launch_bounds__(RingCfg<QW>::kThreads, 1) rope_norm_ring_kerne
                 const uint32_t wb = smem_u32(wsm + (is_q ? 0 : kHeadDim) + 8 * hl);
                 const uint32_t cb = sbase + kRotOff + (uint32_t)tl * kRotBytes + 32u * hl;
                 float s2 = 0.f;
+                if constexpr (QW) {
+                    // two interleaved partial sums on the packed pipe
+                    float sa = 0.f, sb = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) s2 = fmaf(y[e], y[e], s2);
+                    for (int e = 0; e < 16; e += 2) fma2(sa, sb, y[e], y[e + 1], y[e], y[e + 1], sa, sb);
+                    s2 = sa + sb;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) s2 = fmaf(y[e], y[e], s2);
+                }
                 s2 = quarter_sum(s2, qmask);
                 inv = rsqrtf(s2 * (1.f / kHeadDim) + p.eps);
                 if (QW && is_q) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) y[e] *= wq[e];
+                    for (int e = 0; e < 16; e += 2) mul2(y[e], y[e + 1], y[e], y[e + 1], wq[e], wq[e + 1]);
                 } else {
                     const float4 w0 = lds_f4(wb), w1 = lds_f4(wb + 16), w2 = lds_f4(wb + 256), w3 = lds_f4(wb + 272);
                     const float ww[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
                                           w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+                    if constexpr (QW) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) y[e] *= ww[e];
+                        for (int e = 0; e < 16; e += 2) mul2(y[e], y[e + 1], y[e], y[e + 1], ww[e], ww[e + 1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) y[e] *= ww[e];
+                    }
                 }
                 if (meta.x >= 0) {
                     // rotary pairs (i, i + 64), both in this lane: y[e] and y[e + 8]
                     const float4 c0 = lds_f4(cb), c1 = lds_f4(cb + 16), s0 = lds_f4(cb + 256), s1 = lds_f4(cb + 272);
                     const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                     const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                    if constexpr (QW) {
+                        // the same roundings as below: a c - RN(b s) and b c + RN(a s)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float a = y[e], b = y[e + 8];
-                        y[e] = fmaf(a, cc[e], -b * ss[e]);
-                        y[e + 8] = fmaf(b, cc[e], a * ss[e]);
+                        for (int e = 0; e < 8; e += 2) {
+                            const float a0 = y[e], a1 = y[e + 1], b0 = y[e + 8], b1 = y[e + 9];
+                            float ns0, ns1, nbs0, nbs1, as0, as1;
+                            mul2(ns0, ns1, ss[e], ss[e + 1], -1.f, -1.f);
+                            mul2(nbs0, nbs1, b0, b1, ns0, ns1);
+                            mul2(as0, as1, a0, a1, ss[e], ss[e + 1]);
+                            fma2(y[e], y[e + 1], a0, a1, cc[e], cc[e + 1], nbs0, nbs1);
+                            fma2(y[e + 8], y[e + 9], b0, b1, cc[e], cc[e + 1], as0, as1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float a = y[e], b = y[e + 8];
+                            y[e] = fmaf(a, cc[e], -b * ss[e]);
+                            y[e + 8] = fmaf(b, cc[e], a * ss[e]);
+                        }
                     }
                 }
             }
@@ -550,17 +595,33 @@ __global__ void __launch_bounds__(RingCfg<QW>::kThreads, 1) rope_norm_ring_kerne
                     // z * (448 / max|z|), scale inv * max|z| / 448
                     const float rz = am > 0.f ? __fdividef(448.f, am) : 0.f;
                     scale = am > 0.f ? inv * am * kInv448 : 1.f;
+                    if constexpr (QW) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) y[e] *= rz;
+                        for (int e = 0; e < 16; e += 2) mul2(y[e], y[e + 1], y[e], y[e + 1], rz, rz);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) y[e] *= rz;
+                    }
                 } else {
                     // correctly rounded max|x| / 448 and x / scale
                     const float q0 = am * kInv448;
                     scale = am > 0.f ? fmaf(fmaf(-q0, 448.f, am), kInv448, q0) : 1.f;
                     const float rcp = __frcp_rn(scale);
+                    if constexpr (QW) {
+                        const float ns = -scale;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float qq = y[e] * rcp;
-                        y[e] = fmaf(fmaf(-qq, scale, y[e]), rcp, qq);
+                        for (int e = 0; e < 16; e += 2) {
+                            float q0, q1, r0, r1;
+                            mul2(q0, q1, y[e], y[e + 1], rcp, rcp);
+                            fma2(r0, r1, q0, q1, ns, ns, y[e], y[e + 1]);
+                            fma2(y[e], y[e + 1], r0, r1, rcp, rcp, q0, q1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float qq = y[e] * rcp;
+                            y[e] = fmaf(fmaf(-qq, scale, y[e]), rcp, qq);
+                        }
                     }
                 }
                 uint8_t* d8 = static_cast<uint8_t*>(dst) + dst_elem;
