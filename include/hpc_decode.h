@@ -220,8 +220,9 @@ hpc_status hpc_decode_attn(const void* q, const void* k_cache, const void* v_cac
  * kv_dtype = HPC_KV_FP8_E4M3; the query is q8[b][qh][d] * q_scale[b][qh].
  *   q8        device e4m3 codes [batch][num_q_heads][128], 16-byte aligned
  *   q_scale   device float32 [batch][num_q_heads], 16-byte aligned, not NULL
- * QK^T runs on e4m3 operands directly (K and Q codes, float32 accumulation);
- * the scores are then multiplied by the K and Q scales.
+ * QK^T multiplies the K and Q codes, both widened exactly to f16, with float32
+ * accumulation (exact products: the same values as e4m3 x e4m3 products); the
+ * scores are then multiplied by the K and Q scales.
  */
 hpc_status hpc_decode_attn_q8(const void* q8, const float* q_scale, const void* k_cache,
                               const void* v_cache, const float* k_scale, const float* v_scale,

@@ -128,28 +128,17 @@ __device__ __forceinline__ void chunk_compute(uint8_t* stage, int wq, int lane, 
         const uint4 k11 = lds128(kb + (uint32_t)(r0 + 8) * 128u + ((uint32_t)((2 * c + 1) ^ g) << 4));
         const uint32_t w0[8] = {k00.x, k00.y, k00.z, k00.w, k01.x, k01.y, k01.z, k01.w};
         const uint32_t w1[8] = {k10.x, k10.y, k10.z, k10.w, k11.x, k11.y, k11.z, k11.w};
-        if constexpr (QF8) {
-            // e4m3 x e4m3 straight from shared memory: 4 k-steps of 32 dims, the
-            // codes of K and Q in the same permuted order, no widening
+        // K widened exactly to f16 (a bf16 query was rounded to f16, an e4m3 one
+        // widened exactly, in load_q_frags)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t a[4] = {w0[2 * ks], w1[2 * ks], w0[2 * ks + 1], w1[2 * ks + 1]};
-                if (ks & 1)
-                    mma_e4m3(acc1, a, qf[ks][0], qf[ks][1]);
-                else
-                    mma_e4m3(acc0, a, qf[ks][0], qf[ks][1]);
-            }
-        } else {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t a[4];
-                e4m3x4_to_f16x2x2(w0[ks], a[0], a[2]);
-                e4m3x4_to_f16x2x2(w1[ks], a[1], a[3]);
-                if (ks & 1)
-                    mma_f16(acc1, a, qf[ks][0], qf[ks][1]);
-                else
-                    mma_f16(acc0, a, qf[ks][0], qf[ks][1]);
-            }
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            e4m3x4_to_f16x2x2(w0[ks], a[0], a[2]);
+            e4m3x4_to_f16x2x2(w1[ks], a[1], a[3]);
+            if (ks & 1)
+                mma_f16(acc1, a, qf[ks][0], qf[ks][1]);
+            else
+                mma_f16(acc0, a, qf[ks][0], qf[ks][1]);
         }
         const float ks0 = ksc[r0] * scale_log2, ks1 = ksc[r0 + 8] * scale_log2;
         // score columns 2c and 2c+1 are query heads 2c, 2c+1 (their Q scales)
